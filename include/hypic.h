@@ -1,0 +1,217 @@
+/*
+ * hypic.h -- C ABI of the linear-attention hot path of position-independent
+ * caching (PIC) for hybrid-attention models, as described in the HYPIC pages
+ * (codernav.top summary, sections "线性层", "全注意力层" and "段并行";
+ * xix.ai article, paragraphs on linear layers, seam windows and segment-level
+ * parallelism).
+ *
+ * The method.  A linear-attention layer keeps a state S (d_k x d_v, fp32 here)
+ * per head that every token advances:
+ *     S_t = A_t S_{t-1} + W_t ,          o_t = S_t^T q_t ,
+ * in the gated-delta convention
+ *     A_t = alpha_t (I - beta_t k_t k_t^T),   W_t = beta_t k_t v_t^T,
+ * or one of the two named specialisations
+ *     scalar decay (RetNet):        A_t = gamma_h I,      W_t = k_t v_t^T,
+ *     diagonal gate (Mamba2/GLA):   A_t = diag(alpha_t),  W_t = k_t v_t^T.
+ * For a segment C the pair (T_C, S(C|0)) -- the ordered product of the
+ * segment's transitions and its final state from zero -- depends only on the
+ * segment's own tokens, so it is cached once ("线性层": cache the pair at the
+ * segment's first prefill) and reused in any prefix through the composition
+ * law S(C1 C2) = T(C2) S(C1) + S(C2).  The first w tokens of a segment (its
+ * seam window, w = 8 by default, "全注意力层") are not cached: at reuse they
+ * are re-run under the composed prefix state, advancing it and emitting their
+ * per-token outputs.
+ *
+ * Three calls form the hot path:
+ *   hypic_segment_build   -- the cached pair of every segment body, all
+ *                            segments x layers x heads in one launch (the
+ *                            single-GPU stand-in for "段并行"'s scatter stage,
+ *                            longest segment first as in its LPT schedule);
+ *   hypic_compose         -- the running state over a request's segment order,
+ *                            with each entry's seam re-run in the same pass;
+ *   hypic_seam_advance    -- the seams alone, all entries in parallel, from
+ *                            given prefix states.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All device pointers are caller-owned device memory; the library never
+ *   allocates or frees device memory and keeps no device state between calls.
+ *   Host pointers (segment offsets, request order, descriptors) are read
+ *   before the call returns and may be freed afterwards.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *   stream) and runs asynchronously; outputs are valid once the stream has
+ *   reached the call.  Calls on the same stream are ordered.
+ * - Every argument is validated on the host before anything is enqueued.  On
+ *   any error nothing is launched, no output is touched, and the call returns
+ *   a nonzero hypic_status; hypic_last_error() then describes it (per thread).
+ *   A failed launch returns HYPIC_ERR_CUDA.
+ * - Layouts are row-major and packed, layer-major, token-major:
+ *     q, k, v   [L][N][H][d]   (in_dtype; raw pre-convolution tokens when
+ *                               conv_k > 0)
+ *     alpha     gated delta [L][N][H]; diagonal gate [L][N][H][d_k];
+ *               scalar decay [L][H] (one gamma per head), all in in_dtype
+ *     beta      [L][N][H] in in_dtype (gated delta only; NULL otherwise)
+ *     conv_w    fp32 [L][3][H][d][conv_k]: channels of q, k, v; tap j
+ *               multiplies the token j positions earlier
+ *     T         gated delta fp32 [L][n_seg][H][d_k][d_k];
+ *               diagonal gate fp32 [L][n_seg][H][d_k] (the diagonal);
+ *               scalar decay fp32 [L][n_seg][H] (the scalar)
+ *     S, states fp32 [..][d_k][d_v], row = key channel
+ *   Token, alpha and beta pointers must be 16-byte aligned, as must every
+ *   fp32 output.  d_k == d_v is required.
+ * - Segments are contiguous token ranges of the packed token axis given by
+ *   host offsets seg_off[0..n_seg] (non-decreasing, seg_off[n_seg] <= N).  A
+ *   request is a host array order[0..n_order) of segment indices; the same
+ *   segment may appear more than once.  n_seg and n_order are at most
+ *   HYPIC_MAX_SEGMENTS.
+ */
+#ifndef HYPIC_H
+#define HYPIC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HYPIC_ABI_VERSION 1
+#define HYPIC_MAX_SEGMENTS 2048
+
+typedef struct CUstream_st *hypic_stream; /* same type as cudaStream_t */
+
+typedef enum hypic_status {
+    HYPIC_OK = 0,
+    HYPIC_ERR_INVALID_ARG = 1,  /* NULL or misaligned pointer, bad enum */
+    HYPIC_ERR_SHAPE = 2,        /* sizes, offsets or order out of range */
+    HYPIC_ERR_DTYPE = 3,        /* unknown dtype */
+    HYPIC_ERR_UNSUPPORTED = 4,  /* valid request this build does not serve */
+    HYPIC_ERR_WORKSPACE = 5,    /* workspace missing, misaligned or too small */
+    HYPIC_ERR_CUDA = 6,         /* the CUDA runtime reported an error */
+    HYPIC_ERR_TIMEOUT = 7       /* a bounded device-side wait gave up */
+} hypic_status;
+
+typedef enum hypic_mode {
+    HYPIC_GATED_DELTA = 0,   /* A_t = alpha_t (I - beta_t k k^T), W = beta k v^T */
+    HYPIC_SCALAR_DECAY = 1,  /* A_t = gamma_h I,                  W = k v^T      */
+    HYPIC_DIAG_GATE = 2      /* A_t = diag(alpha_t),              W = k v^T      */
+} hypic_mode;
+
+typedef enum hypic_dtype {
+    HYPIC_F32 = 0,
+    HYPIC_BF16 = 1
+} hypic_dtype;
+
+/* Shape and variant of one stack of linear-attention layers. */
+typedef struct hypic_desc {
+    int32_t n_layers;  /* L >= 1 */
+    int32_t n_heads;   /* H >= 1 */
+    int32_t d_k;       /* key width: 16, 32, 64 or 128 */
+    int32_t d_v;       /* value width: must equal d_k */
+    int32_t seam_w;    /* seam window w in [0, 64]; 0 = no seams */
+    int32_t conv_k;    /* causal depthwise conv taps: 0 (none) or 2..4 */
+    int32_t mode;      /* hypic_mode */
+    int32_t in_dtype;  /* hypic_dtype of q, k, v, alpha, beta */
+} hypic_desc;
+
+/* The packed per-token inputs of a request's tokens (all device pointers). */
+typedef struct hypic_tokens {
+    const void *q;       /* [L][N][H][d_k]; needed for seam outputs only */
+    const void *k;       /* [L][N][H][d_k] */
+    const void *v;       /* [L][N][H][d_v] */
+    const void *alpha;   /* see layouts above */
+    const void *beta;    /* [L][N][H] (gated delta only) */
+    const float *conv_w; /* fp32 [L][3][H][d][conv_k] when conv_k > 0 */
+    int64_t n_tokens;    /* N, < 2^31 */
+} hypic_tokens;
+
+/* ABI version of the loaded library (HYPIC_ABI_VERSION). */
+int hypic_version(void);
+
+/* Description of the last error on the calling thread ("" if none). */
+const char *hypic_last_error(void);
+
+/*
+ * Bytes of device workspace hypic_segment_build needs (always > 0, a
+ * multiple of 256).  The workspace carries the build's work-queue counter and
+ * its device status word; it need not be initialised and may be reused by
+ * consecutive calls on one stream.
+ */
+size_t hypic_workspace_size(const hypic_desc *desc);
+
+/*
+ * Segment build: for every segment s, layer l and head h, the cached pair of
+ * the segment's body -- the segment's tokens after its first min(w, len)
+ * seam tokens -- computed from a zero state:
+ *     T[l][s][h] = A_{n} ... A_{1}     (ordered product over the body)
+ *     S[l][s][h] = S(body | 0)
+ * (HYPIC pages: "线性层" -- the pair depends only on the segment's own tokens
+ * and is cached at its first prefill; "全注意力层" -- seam tokens are not
+ * cached.)  An empty body yields (I, 0).  With conv_k > 0 the body's q/k/v
+ * are the causal convolution of the raw tokens (history inside the segment;
+ * requires seam_w >= conv_k - 1 so that bodies stay prefix-independent)
+ * followed by per-head L2 normalisation of k.
+ *
+ * All segments x layers x heads run in one launch, longest body first.
+ * T_out/S_out: layouts above.  workspace: device, 256-byte aligned, at least
+ * hypic_workspace_size(desc) bytes, not used concurrently by another call.
+ */
+int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok,
+                        const int64_t *seg_off, int32_t n_seg,
+                        float *T_out, float *S_out,
+                        void *workspace, size_t workspace_bytes,
+                        hypic_stream stream);
+
+/*
+ * Compose: the running state of every (layer, head) over the request
+ * order[0..n_order), starting from S_init (NULL = zero):
+ *     for e in 0..n_order-1, s = order[e]:
+ *         S_prefix_out[l][e][h] = S                      (if non-NULL)
+ *         if seam_w > 0: re-run the first min(w, len_s) tokens of s from S,
+ *             writing o_out[l][e][j][h][:] = S_j^T q_j and advancing S
+ *         S = T[l][s][h] S + S[l][s][h]                  (composition law)
+ *     S_final[l][h] = S
+ * (HYPIC pages: "线性层" -- left-multiply by T_C then add; "全注意力层" --
+ * seams re-run under the full prefix, advancing the running state and passing
+ * each seam token's output up.)  With conv_k > 0 a seam token's convolution
+ * history is the previous entry's last raw tokens (zero before the request
+ * start): the pages' "convolution state warm-up".
+ *
+ * T, S: the cache, as written by hypic_segment_build with the same desc and
+ * n_seg.  tok: the request's tokens (may be NULL when seam_w == 0).
+ * o_out: fp32 [L][n_order][w][H][d_v]; rows past a short seam are zeroed
+ * (NULL allowed when seam_w == 0).  S_prefix_out: fp32 [L][n_order][H][d_k][d_v]
+ * or NULL.  S_final: fp32 [L][H][d_k][d_v], may alias S_init.
+ * n_order == 0 copies S_init (or zero) to S_final.
+ */
+int hypic_compose(const hypic_desc *desc, const hypic_tokens *tok,
+                  const int64_t *seg_off, int32_t n_seg,
+                  const int32_t *order, int32_t n_order,
+                  const float *T, const float *S, const float *S_init,
+                  float *S_prefix_out, float *S_final, float *o_out,
+                  hypic_stream stream);
+
+/*
+ * Seam advance: every entry's seam re-run from a given state, all entries in
+ * parallel (the seams of a request are independent once their prefix states
+ * are known, e.g. from hypic_compose's S_prefix_out):
+ *     for each e, l, h:  S = S_in[l][e][h];
+ *         for the first min(w, len) tokens of order[e]: advance S, emit o
+ *         o_out[l][e][j][h][:] = S_j^T q_j ;  S_out[l][e][h] = S
+ * (HYPIC pages: "全注意力层" -- the linear layer computes the seam window's
+ * T and S on the fly while advancing the running state and forwards each seam
+ * token's output.)  Same conv history rule as hypic_compose.
+ * S_in: fp32 [L][n_order][H][d_k][d_v]; o_out: fp32 [L][n_order][w][H][d_v];
+ * S_out: same layout as S_in or NULL; S_out may alias S_in.
+ */
+int hypic_seam_advance(const hypic_desc *desc, const hypic_tokens *tok,
+                       const int64_t *seg_off, int32_t n_seg,
+                       const int32_t *order, int32_t n_order,
+                       const float *S_in, float *o_out, float *S_out,
+                       hypic_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYPIC_H */
