@@ -1,0 +1,265 @@
+// api.cu -- the C ABI of include/hypic.h: host-side validation, the
+// longest-first work order of the build, and kernel launches on the caller's
+// stream.  No device memory is allocated here.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+#include "kernels.h"
+
+using namespace hypic;
+
+namespace {
+
+thread_local char g_err[512];
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_desc(const hypic_desc *d)
+{
+    if (!d) return fail(HYPIC_ERR_INVALID_ARG, "desc is NULL");
+    if (d->mode < HYPIC_GATED_DELTA || d->mode > HYPIC_DIAG_GATE)
+        return fail(HYPIC_ERR_INVALID_ARG, "unknown mode %d", d->mode);
+    if (d->in_dtype != HYPIC_F32 && d->in_dtype != HYPIC_BF16)
+        return fail(HYPIC_ERR_DTYPE, "unknown in_dtype %d", d->in_dtype);
+    if (d->n_layers < 1 || d->n_heads < 1 || (int64_t)d->n_layers * d->n_heads > 65536)
+        return fail(HYPIC_ERR_SHAPE, "n_layers=%d n_heads=%d out of range", d->n_layers, d->n_heads);
+    if (d->d_k != d->d_v)
+        return fail(HYPIC_ERR_UNSUPPORTED, "d_k (%d) != d_v (%d)", d->d_k, d->d_v);
+    if (d->d_k != 16 && d->d_k != 32 && d->d_k != 64 && d->d_k != 128)
+        return fail(HYPIC_ERR_UNSUPPORTED, "d_k=%d not in {16, 32, 64, 128}", d->d_k);
+    if (d->seam_w < 0 || d->seam_w > 64)
+        return fail(HYPIC_ERR_SHAPE, "seam_w=%d not in [0, 64]", d->seam_w);
+    if (d->conv_k != 0 && (d->conv_k < 2 || d->conv_k > 4))
+        return fail(HYPIC_ERR_UNSUPPORTED, "conv_k=%d not in {0, 2, 3, 4}", d->conv_k);
+    if (d->conv_k > 0 && d->seam_w < d->conv_k - 1)
+        return fail(HYPIC_ERR_UNSUPPORTED,
+                    "conv_k=%d needs seam_w >= %d so that cached bodies are prefix-independent",
+                    d->conv_k, d->conv_k - 1);
+    return HYPIC_OK;
+}
+
+int check_tokens(const hypic_desc *d, const hypic_tokens *t, bool need_q)
+{
+    if (!t) return fail(HYPIC_ERR_INVALID_ARG, "tokens is NULL");
+    if (t->n_tokens < 0 || t->n_tokens >= ((int64_t)1 << 31))
+        return fail(HYPIC_ERR_SHAPE, "n_tokens=%lld out of range", (long long)t->n_tokens);
+    struct { const void *p; const char *name; bool need; } ps[] = {
+        {t->q, "q", need_q},
+        {t->k, "k", true},
+        {t->v, "v", true},
+        {t->alpha, "alpha", true},
+        {t->beta, "beta", d->mode == HYPIC_GATED_DELTA},
+        {t->conv_w, "conv_w", d->conv_k > 0},
+    };
+    for (auto &x : ps) {
+        if (!x.need) continue;
+        if (!x.p) return fail(HYPIC_ERR_INVALID_ARG, "tokens.%s is NULL", x.name);
+        if (!aligned(x.p, 16)) return fail(HYPIC_ERR_INVALID_ARG, "tokens.%s is not 16-byte aligned", x.name);
+    }
+    return HYPIC_OK;
+}
+
+int check_segments(const int64_t *seg_off, int32_t n_seg, int64_t n_tokens)
+{
+    if (n_seg < 0 || n_seg > HYPIC_MAX_SEGMENTS)
+        return fail(HYPIC_ERR_SHAPE, "n_seg=%d not in [0, %d]", n_seg, HYPIC_MAX_SEGMENTS);
+    if (!seg_off) return fail(HYPIC_ERR_INVALID_ARG, "seg_off is NULL");
+    if (seg_off[0] < 0) return fail(HYPIC_ERR_SHAPE, "seg_off[0]=%lld < 0", (long long)seg_off[0]);
+    for (int32_t i = 0; i < n_seg; ++i)
+        if (seg_off[i + 1] < seg_off[i])
+            return fail(HYPIC_ERR_SHAPE, "seg_off decreases at %d (%lld > %lld)", i,
+                        (long long)seg_off[i], (long long)seg_off[i + 1]);
+    if (seg_off[n_seg] > n_tokens)
+        return fail(HYPIC_ERR_SHAPE, "seg_off[n_seg]=%lld > n_tokens=%lld", (long long)seg_off[n_seg],
+                    (long long)n_tokens);
+    return HYPIC_OK;
+}
+
+int check_order(const int32_t *order, int32_t n_order, int32_t n_seg)
+{
+    if (n_order < 0 || n_order > HYPIC_MAX_SEGMENTS)
+        return fail(HYPIC_ERR_SHAPE, "n_order=%d not in [0, %d]", n_order, HYPIC_MAX_SEGMENTS);
+    if (n_order > 0 && !order) return fail(HYPIC_ERR_INVALID_ARG, "order is NULL");
+    for (int32_t i = 0; i < n_order; ++i)
+        if (order[i] < 0 || order[i] >= n_seg)
+            return fail(HYPIC_ERR_SHAPE, "order[%d]=%d not in [0, %d)", i, order[i], n_seg);
+    return HYPIC_OK;
+}
+
+int check_out(const void *p, const char *name)
+{
+    if (!p) return fail(HYPIC_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, 16)) return fail(HYPIC_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return HYPIC_OK;
+}
+
+Dims make_dims(const hypic_desc *d)
+{
+    return Dims{d->n_layers, d->n_heads, d->d_k, d->seam_w, d->conv_k, d->mode, d->in_dtype};
+}
+
+TokPtrs make_tok(const hypic_tokens *t)
+{
+    TokPtrs p{};
+    if (t) {
+        p.q = t->q; p.k = t->k; p.v = t->v; p.alpha = t->alpha; p.beta = t->beta;
+        p.conv_w = t->conv_w;
+        p.N = (int32_t)t->n_tokens;
+    }
+    return p;
+}
+
+void fill_offsets(SegTable &tab, const int64_t *seg_off, int32_t n_seg)
+{
+    tab.n_seg = n_seg;
+    for (int32_t i = 0; i <= n_seg; ++i) tab.off[i] = (int32_t)seg_off[i];
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(HYPIC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+int hypic_version(void) { return HYPIC_ABI_VERSION; }
+
+const char *hypic_last_error(void) { return g_err; }
+
+size_t hypic_workspace_size(const hypic_desc *desc)
+{
+    (void)desc;
+    return 256;
+}
+
+int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok, const int64_t *seg_off,
+                        int32_t n_seg, float *T_out, float *S_out, void *workspace,
+                        size_t workspace_bytes, hypic_stream stream)
+{
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_desc(desc))) return rc;
+    if ((rc = check_tokens(desc, tok, false))) return rc;
+    if ((rc = check_segments(seg_off, n_seg, tok->n_tokens))) return rc;
+    if ((rc = check_out(T_out, "T_out"))) return rc;
+    if ((rc = check_out(S_out, "S_out"))) return rc;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < hypic_workspace_size(desc))
+        return fail(HYPIC_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes",
+                    hypic_workspace_size(desc));
+    if (n_seg == 0) return HYPIC_OK;
+
+    static thread_local SegTable tab;
+    fill_offsets(tab, seg_off, n_seg);
+    // Longest body first (ties: lower index first): the greedy LPT order.
+    const int w = desc->seam_w;
+    auto body = [&](int s) {
+        const int64_t len = seg_off[s + 1] - seg_off[s];
+        return len - std::min<int64_t>(w, len);
+    };
+    std::vector<int32_t> idx(n_seg);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return body(a) > body(b); });
+    for (int32_t i = 0; i < n_seg; ++i) tab.perm[i] = idx[i];
+    tab.n_perm = n_seg;
+
+    BuildArgs a{};
+    a.dm = make_dims(desc);
+    a.tok = make_tok(tok);
+    a.T_out = T_out;
+    a.S_out = S_out;
+    a.work_counter = static_cast<unsigned int *>(workspace);
+    a.status = reinterpret_cast<int *>(static_cast<char *>(workspace) + 128);
+    cudaError_t e = launch_build_rec(a, tab, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "segment build launch");
+    return HYPIC_OK;
+}
+
+int hypic_compose(const hypic_desc *desc, const hypic_tokens *tok, const int64_t *seg_off,
+                  int32_t n_seg, const int32_t *order, int32_t n_order, const float *T,
+                  const float *S, const float *S_init, float *S_prefix_out, float *S_final,
+                  float *o_out, hypic_stream stream)
+{
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_desc(desc))) return rc;
+    const bool seams = desc->seam_w > 0 && n_order > 0;
+    if (seams && (rc = check_tokens(desc, tok, true))) return rc;
+    if ((rc = check_segments(seg_off, n_seg, seams ? tok->n_tokens : INT64_MAX))) return rc;
+    if ((rc = check_order(order, n_order, n_seg))) return rc;
+    if (n_order > 0) {
+        if ((rc = check_out(T, "T"))) return rc;
+        if ((rc = check_out(S, "S"))) return rc;
+    }
+    if (S_init && !aligned(S_init, 16)) return fail(HYPIC_ERR_INVALID_ARG, "S_init is not 16-byte aligned");
+    if (S_prefix_out && !aligned(S_prefix_out, 16))
+        return fail(HYPIC_ERR_INVALID_ARG, "S_prefix_out is not 16-byte aligned");
+    if ((rc = check_out(S_final, "S_final"))) return rc;
+    if (seams && (rc = check_out(o_out, "o_out"))) return rc;
+
+    static thread_local SegTable tab;
+    fill_offsets(tab, seg_off, n_seg);
+    for (int32_t i = 0; i < n_order; ++i) tab.perm[i] = order[i];
+    tab.n_perm = n_order;
+
+    ComposeArgs a{};
+    a.dm = make_dims(desc);
+    if (!seams) a.dm.w = 0;
+    a.tok = make_tok(seams ? tok : nullptr);
+    a.T = T;
+    a.S = S;
+    a.S_init = S_init;
+    a.S_prefix = S_prefix_out;
+    a.S_final = S_final;
+    a.o_out = o_out;
+    cudaError_t e = launch_compose(a, tab, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "compose launch");
+    return HYPIC_OK;
+}
+
+int hypic_seam_advance(const hypic_desc *desc, const hypic_tokens *tok, const int64_t *seg_off,
+                       int32_t n_seg, const int32_t *order, int32_t n_order, const float *S_in,
+                       float *o_out, float *S_out, hypic_stream stream)
+{
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_desc(desc))) return rc;
+    if ((rc = check_tokens(desc, tok, true))) return rc;
+    if ((rc = check_segments(seg_off, n_seg, tok->n_tokens))) return rc;
+    if ((rc = check_order(order, n_order, n_seg))) return rc;
+    if (desc->seam_w == 0 || n_order == 0) return HYPIC_OK;
+    if ((rc = check_out(S_in, "S_in"))) return rc;
+    if ((rc = check_out(o_out, "o_out"))) return rc;
+    if (S_out && !aligned(S_out, 16)) return fail(HYPIC_ERR_INVALID_ARG, "S_out is not 16-byte aligned");
+
+    static thread_local SegTable tab;
+    fill_offsets(tab, seg_off, n_seg);
+    for (int32_t i = 0; i < n_order; ++i) tab.perm[i] = order[i];
+    tab.n_perm = n_order;
+
+    SeamArgs a{};
+    a.dm = make_dims(desc);
+    a.tok = make_tok(tok);
+    a.S_in = S_in;
+    a.o_out = o_out;
+    a.S_out = S_out;
+    cudaError_t e = launch_seam(a, tab, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "seam advance launch");
+    return HYPIC_OK;
+}
+
+}  // extern "C"

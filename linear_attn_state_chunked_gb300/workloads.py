@@ -127,7 +127,9 @@ def request_order(name, r=0):
 
 
 def _layer_seed(name, seed, l, L):
-    return seed if L == 1 else seed * 1000 + l
+    # single-layer workloads keep their seed for layer 0; extra layers drawn
+    # for tests (and every layer of a stack) use seed*1000 + l
+    return seed if (L == 1 and l == 0) else seed * 1000 + l
 
 
 def make(name, device="cpu", layers=None, lengths=None, order=None,

@@ -1,0 +1,142 @@
+"""GPU parity on the small workloads and edge cases: every output block of
+the C-ABI calls against the fp64 oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+from linear_attn_state_chunked_gb300 import hypic, workloads as W
+from oracle import reference as ref
+from _parity import (run_pipeline, check_pairs, check_request, tol_of, alloc_outputs,
+                     T_FLOOR)
+
+pytestmark = pytest.mark.gpu
+
+
+def _all_items(wl):
+    d = wl.desc
+    return [(l, s, h) for l in range(d["n_layers"]) for s in range(wl.n_seg)
+            for h in range(d["n_heads"])]
+
+
+def _all_chains(wl):
+    d = wl.desc
+    return [(l, h) for l in range(d["n_layers"]) for h in range(d["n_heads"])]
+
+
+@pytest.mark.parametrize("name", ["tiny_gdn", "stress_tiny", "decay_retnet", "decay_diag"])
+def test_small_workloads(name):
+    """tiny_gdn: build per segment, compose in order, against the sequential
+    recurrence over all 256 tokens; decay_*: scalar-decay and diagonal-gate
+    specialisations; stress_tiny: slow gate so that T_C matters."""
+    wl = W.make(name, device="cuda")
+    out = run_pipeline(wl)
+    tol = tol_of(wl.desc)
+    check_pairs(wl, out, _all_items(wl), tol)
+    res = check_request(wl, out, _all_chains(wl), tol)
+    if name == "stress_tiny":
+        # the composition term is far from negligible here
+        T = out["T"].cpu().numpy()
+        assert np.abs(T).max() > 1e-3
+
+
+@pytest.mark.parametrize("name", ["decay_retnet", "decay_diag", "stress_tiny"])
+def test_naive_addition_is_wrong(name):
+    """Negative control: summing the GPU's zero-initial states (dropping T)
+    misses the recurrence by far more than the tolerance."""
+    wl = W.make(name, device="cuda")
+    out = run_pipeline(wl)
+    S = out["S"].cpu().numpy()
+    Sf = out["S_final"].cpu().numpy()
+    tol = tol_of(wl.desc)
+    errs = []
+    for (l, h) in _all_chains(wl):
+        naive = S[l, :, h].sum(axis=0)
+        errs.append(ref.rel_fro(naive, Sf[l, h]))
+    assert min(errs) > 100 * tol
+
+
+EDGE_LENGTHS = [0, 1, 5, 8, 9, 70, 130, 3, 64, 65]
+EDGE_ORDER = [5, 0, 9, 2, 2, 7, 1, 6, 3, 4, 8, 5]
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("dtype", [hypic.F32, hypic.BF16])
+@pytest.mark.parametrize("mode", [hypic.GATED_DELTA, hypic.SCALAR_DECAY, hypic.DIAG_GATE])
+def test_edge_cases_ragged_seams_order(d, dtype, mode):
+    """Empty, one-token, shorter-than-seam and ragged segments, a shuffled
+    request order with a repeated segment, seams of w = 8, two layers."""
+    name = {hypic.GATED_DELTA: "stress_tiny", hypic.SCALAR_DECAY: "decay_retnet",
+            hypic.DIAG_GATE: "decay_diag"}[mode]
+    wl = W.make(name, device="cuda", layers=2, lengths=EDGE_LENGTHS, order=EDGE_ORDER,
+                n_heads=2, d_k=d, d_v=d, seam_w=8, in_dtype=dtype)
+    out = run_pipeline(wl)
+    tol = tol_of(wl.desc)
+    check_pairs(wl, out, _all_items(wl), tol)
+    check_request(wl, out, _all_chains(wl), tol)
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_conv_warmup_small(d):
+    """Causal conv (4 taps) with warm-up across segment boundaries, including
+    segments shorter than the conv history, in a shuffled order."""
+    wl = W.make("cold_30l", device="cuda", layers=2, lengths=[9, 40, 3, 1, 25, 12, 0, 17],
+                order=[4, 2, 3, 0, 7, 5, 1, 6], n_heads=2, d_k=d, d_v=d)
+    out = run_pipeline(wl)
+    tol = tol_of(wl.desc)
+    check_pairs(wl, out, _all_items(wl), tol)
+    check_request(wl, out, _all_chains(wl), tol)
+
+
+def test_nonzero_initial_state_and_empty_request():
+    wl = W.make("stress_tiny", device="cuda", n_heads=3)
+    d = wl.desc
+    L, H, D = d["n_layers"], d["n_heads"], d["d_k"]
+    g = torch.Generator(device="cuda").manual_seed(77)
+    S0 = torch.randn((L, H, D, D), generator=g, device="cuda")
+    out = alloc_outputs(d, wl.n_seg, len(wl.order))
+    hypic.segment_build(d, wl.tok, wl.seg_off, out["T"], out["S"], out["ws"])
+    hypic.compose(d, None, wl.seg_off, wl.order, out["T"], out["S"], out["S_final"],
+                  S_init=S0, S_prefix_out=out["S_prefix"])
+    torch.cuda.synchronize()
+    chains = [(0, h) for h in range(H)]
+    check_request(wl, out, chains, tol_of(d), S_init=S0[0].cpu().numpy())
+    # empty request: S_final = S_init, in place
+    Sx = S0.clone()
+    hypic.compose(d, None, wl.seg_off, [], out["T"], out["S"], Sx, S_init=Sx)
+    torch.cuda.synchronize()
+    assert torch.equal(Sx, S0)
+    Z = torch.full_like(S0, 5.0)
+    hypic.compose(d, None, wl.seg_off, [], out["T"], out["S"], Z)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(Z).item() == 0
+
+
+@pytest.mark.parametrize("conv", [False, True])
+def test_seam_advance_matches_compose(conv):
+    """All seams in parallel from the prefix states equal the fused pass and
+    the oracle; S_out may alias S_in."""
+    if conv:
+        wl = W.make("cold_30l", device="cuda", layers=2, lengths=[9, 40, 3, 1, 25, 12, 17],
+                    order=[4, 2, 3, 0, 5, 1, 6], n_heads=2, d_k=32, d_v=32)
+    else:
+        wl = W.make("stress_tiny", device="cuda", lengths=EDGE_LENGTHS, order=EDGE_ORDER,
+                    n_heads=2, seam_w=8, in_dtype=hypic.BF16, d_k=64, d_v=64)
+    d = wl.desc
+    out = run_pipeline(wl)
+    o2 = torch.full_like(out["o"], float("nan"))
+    S_after = out["S_prefix"].clone()
+    hypic.seam_advance(d, wl.tok, wl.seg_off, wl.order, S_after, o2, S_out=S_after)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, out["o"])
+    # oracle: seams re-run from the oracle's own prefix states
+    chains = [(l, h) for l in range(d["n_layers"]) for h in range(d["n_heads"])]
+    exp = ref.request_reference(d, wl.tok, wl.seg_off, wl.order, chains)
+    entries = list(range(len(wl.order)))
+    Sa = S_after.cpu().numpy()
+    tol = tol_of(d)
+    for ci, (l, h) in enumerate(chains):
+        o_ref, s_ref = ref.seam_reference(d, wl.tok, wl.seg_off, wl.order, [(l, h)],
+                                          [exp["S_prefix"][ci]], entries)
+        for e in entries:
+            assert ref.rel_fro(Sa[l, e, h], s_ref[0, e]) <= tol
+            assert ref.rel_fro(o2[l, e, :, h].cpu().numpy(), o_ref[0, e]) <= tol
