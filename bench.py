@@ -1,0 +1,393 @@
+"""Benchmark of the linear-attention PIC hot path on one GB300.
+
+A step is one pass of the whole hot path over the cold 100k-token prompt of a
+30-layer stack (32 heads, d = 128, bf16 q/k/v/alpha/beta, fp32 state, causal
+conv of 4 taps, w = 8, 200 lognormal segments, all cache misses):
+
+  1. hypic_segment_build -- the (T_C, S(C|0)) pair of every segment body x
+     layer x head, conv warm-up inside each body, one launch;
+  2. hypic_compose       -- the running state over the request, every seam
+     re-run under its prefix (conv warm-up across segment boundaries), one
+     launch.
+
+value = tokens x layers processed per second (Mtok/s, all heads), inputs
+resident in HBM.  The JSON line also carries each call's own throughput
+(build Mtok/s, compose segs/s), the dominant kernel's roofline, an end-to-end
+figure through the C ABI from pinned host buffers, SM clocks sampled during
+the timed region, and the fp64 oracle timed on the host cores on a bounded
+sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this path) on a bounded sample of the same workload, per step.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "cold_30l"
+METRIC = "segment-build Mtok/s and compose segs/s per layer, % of roofline (1 GB300)"
+UNIT = "Mtok/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, sm_max_mhz=2070.0,
+                source="fallback")
+
+
+def _config():
+    from linear_attn_state_chunked_gb300 import workloads as W
+    d = W.describe(WORKLOAD)
+    lens = W.segment_lengths(WORKLOAD)
+    n = int(lens.sum())
+    in_bytes = d["n_layers"] * n * d["n_heads"] * (3 * d["d_k"] * 2 + 2 * 2)
+    return {
+        "workload": "cold_30l: cold 100k-token prompt, %d layers x %d heads, d_k=d_v=%d, "
+                    "%d lognormal segments (median %d, clipped [64,4096], sum %d), "
+                    "causal conv %d taps, seam w=%d, bf16 q/k/v/alpha/beta, fp32 state; "
+                    "step = batched build of every segment pair + compose with fused seams"
+                    % (d["n_layers"], d["n_heads"], d["d_k"], len(lens), int(np.median(lens)), n,
+                       d["conv_k"], d["seam_w"]),
+        "tokens": n, "layers": d["n_layers"], "heads": d["n_heads"], "d": d["d_k"],
+        "segments": int(len(lens)),
+        "l2": "inputs larger than L2 (%.1f GB of token inputs per step)" % (in_bytes / 1e9),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _reduce_max(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# fp64 oracle on a bounded sample (cpu_baseline leg and --impl reference)
+
+def oracle_sample(wl, n_heads, n_segments):
+    """Time the oracle on layer 0, heads [0, n_heads), the first n_segments of
+    the request: conv + normalisation, every body pair, the compose chain and
+    every seam.  Returns (seconds, layer-tokens covered)."""
+    import oracle
+    from oracle import reference as ref
+    d = wl.desc
+    order = [int(s) for s in wl.order[:n_segments]]
+    off = wl.seg_off
+    idx = np.concatenate([np.arange(off[s], off[s + 1]) for s in order])
+    starts = np.cumsum([0] + [int(off[s + 1] - off[s]) for s in order])
+    # inputs leave the device before the clock starts
+    cpu_tok = {k: (None if v is None else v.detach().cpu()) for k, v in wl.tok.items()}
+    w = d["seam_w"]
+    t0 = time.perf_counter()
+    streams = [ref.chain_stream(cpu_tok, d["mode"], 0, h, idx, d["conv_k"]) for h in range(n_heads)]
+    q, k, v, a = (np.stack([s[i] for s in streams]) for i in range(4))
+    b = np.stack([s[4] for s in streams])
+    C, D = n_heads, d["d_k"]
+    S = np.zeros((C, D, D))
+    for e in range(len(order)):
+        lo, hi = starts[e], starts[e + 1]
+        sw = min(w, hi - lo)
+        S, _, _ = oracle.recurrence(d["mode"], q[:, lo:lo + sw], k[:, lo:lo + sw], v[:, lo:lo + sw],
+                                    a[:, lo:lo + sw], b[:, lo:lo + sw], S0=S, want_o=True)
+        T, Sc = oracle.pair(d["mode"], k[:, lo + sw:hi], v[:, lo + sw:hi], a[:, lo + sw:hi],
+                            b[:, lo + sw:hi])
+        S = oracle.compose(T, Sc, S)
+    dt = time.perf_counter() - t0
+    layer_tokens = len(idx) * n_heads / d["n_heads"]
+    return dt, layer_tokens
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return 0
+    import torch
+    from linear_attn_state_chunked_gb300 import workloads as W
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = W.make(WORKLOAD, device=dev, layers=1)
+    heads, segs = 4, 12
+    for _ in range(args.warmup):
+        oracle_sample(wl, heads, segs)
+    tot_t, tot_tok = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, lt = oracle_sample(wl, heads, segs)
+        tot_t += dt
+        tot_tok += lt
+    value = tot_tok / tot_t / 1e6
+    sample = ("fp64 oracle, layer 0, heads 0-%d, first %d segments of the request (%d tokens): "
+              "conv, every body pair, compose, seams" % (heads - 1, segs, int(tot_tok / args.steps * W.describe(WORKLOAD)["n_heads"] / heads)))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+
+def run_gpu(args):
+    import torch
+    from linear_attn_state_chunked_gb300 import hypic, workloads as W
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+
+    wl = W.make(WORKLOAD, device=dev)
+    d = wl.desc
+    L, H, D, w = d["n_layers"], d["n_heads"], d["d_k"], d["seam_w"]
+    n_seg, n_ord = wl.n_seg, len(wl.order)
+    tshape, sshape = hypic.pair_shapes(d, n_seg)
+    T = torch.empty(tshape, device=dev)
+    S = torch.empty(sshape, device=dev)
+    Sf = torch.empty((L, H, D, D), device=dev)
+    o = torch.empty((L, n_ord, w, H, D), device=dev)
+    wsp = torch.empty(hypic.workspace_size(d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        hypic.segment_build(d, wl.tok, wl.seg_off, T, S, wsp, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        hypic.compose(d, wl.tok, wl.seg_off, wl.order, T, S, Sf, o_out=o, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.4)  # let the sampler emit its first line
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    _barrier(ws)
+    ms_total = _reduce_max(start.elapsed_time(end), ws)
+    build_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    comp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+
+    tokens = wl.n_tokens
+    body_tokens = int(sum(max(0, int(x) - min(w, int(x))) for x in wl.lengths))
+    ms_step = ms_total / args.steps
+    value = tokens * L * ws / (ms_step * 1e-3) / 1e6
+    build_mtok = body_tokens * L / (build_ms * 1e-3) / 1e6
+    comp_segs = n_ord * L / (comp_ms * 1e-3)
+
+    # roofline of the dominant kernel (the build): algorithmic flops of the
+    # recurrence, 4 d_k (d_k + d_v) per body token and head, on CUDA cores
+    flops = body_tokens * L * H * 4.0 * D * (2 * D)
+    achieved = flops / (build_ms * 1e-3) / 1e12
+    alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+    roof = {"kernel": "build_rec_kernel", "bound": "alu", "achieved": achieved,
+            "peak": alu_peak, "unit": "TFLOP/s", "frac": achieved / alu_peak, "traffic": None,
+            "peak_source": "152 SMs x 128 fp32 lanes x 2 flop x %d MHz" % peaks["sm_max_mhz"]}
+    # compose + seams: HBM-bound; algorithmic bytes = pairs read + seam inputs + outputs
+    pair_bytes = L * n_ord * H * (2 * D * D) * 4
+    seam_tok = int(sum(min(w, int(wl.lengths[s])) for s in wl.order))
+    # seam tokens: raw q, k, v (bf16) and alpha, beta in; fp32 outputs out
+    seam_bytes = L * seam_tok * H * (3 * D * 2 + 2 * 2 + D * 4)
+    comp_bytes = pair_bytes + seam_bytes + L * H * D * D * 4
+    comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI from pinned host buffers (h2d inputs,
+    # d2h final state and seam outputs inside the timed region)
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for key, v in wl.tok.items():
+            if v is not None:
+                host[key] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                host[key].copy_(v)
+        h_Sf = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
+        h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = Sf.numel() * 4 + o.numel() * 4
+        n_e2e = max(1, min(args.steps, 3))
+
+        def e2e_step():
+            for key, hv in host.items():
+                if hv is not None:
+                    wl.tok[key].copy_(hv, non_blocking=True)
+            step()
+            h_Sf.copy_(Sf, non_blocking=True)
+            h_o.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = _reduce_max(e0.elapsed_time(e1), ws) / n_e2e
+        e2e = {"value": tokens * L * ws / (ms_e2e * 1e-3) / 1e6, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": n_e2e, "ms_per_step": ms_e2e}
+        del host
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        heads, segs = 32, 30
+        dt, lt = oracle_sample(wl, heads, segs)
+        cpu = {"value": lt / dt / 1e6, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+               "sample": "fp64 oracle on layer 0, all %d heads, first %d segments of the request "
+                         "(%d tokens): conv, body pairs, compose, seams; %.1f s"
+                         % (heads, segs, int(lt * d["n_heads"] / heads), dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": _config(),
+            "components": {
+                "build": {"mtok_s_per_layer": build_mtok, "ms": build_ms, "launches_per_step": 1},
+                "compose_with_seams": {"segs_s_per_layer": comp_segs, "ms": comp_ms,
+                                       "gbs": comp_gbs, "hbm_frac": comp_gbs / peaks["hbm_gbs"],
+                                       "launches_per_step": 1}},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clk,
+            "gpu_launches": 2 * args.steps,
+            "peaks": peaks,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -79,7 +79,7 @@ def pair_reference(desc, tok, seg_off, items):
     return np.stack(Ts), np.stack(Ss)
 
 
-def request_reference(desc, tok, seg_off, order, chains, S_init=None):
+def request_reference(desc, tok, seg_off, order, chains, S_init=None, want_naive=False):
     """Run the recurrence over the whole request (segments in `order`) for
     each chain (l, h) in chains.
 
@@ -88,8 +88,8 @@ def request_reference(desc, tok, seg_off, order, chains, S_init=None):
       o_seam   [n_chain, n_order, w, dv]: outputs of each entry's seam tokens
                 (rows past the seam length are zero)
       S_final  [n_chain, dk, dv]
-      S_naive  [n_chain, dk, dv]: sum of the entries' zero-initial final
-                states (the straw man that drops T; negative control)
+      S_naive  [n_chain, dk, dv] (want_naive only): sum of the entries'
+                zero-initial final states (the straw man that drops T)
     """
     mode, w, ck = desc["mode"], desc["seam_w"], desc.get("conv_k", 0)
     order = [int(s) for s in order]
@@ -97,27 +97,31 @@ def request_reference(desc, tok, seg_off, order, chains, S_init=None):
                          ) if order else np.zeros(0, np.int64)
     starts = np.cumsum([0] + [int(seg_off[s + 1] - seg_off[s]) for s in order])
     out = {"S_prefix": [], "o_seam": [], "S_final": [], "S_naive": []}
-    for ci, (l, h) in enumerate(chains):
-        q, k, v, a, b = chain_stream(tok, mode, l, h, idx, ck)
-        dk, dv = k.shape[1], v.shape[1]
-        S0 = None if S_init is None else _np(S_init[ci])[None]
-        Sf, o, Srec = recurrence(mode, q[None], k[None], v[None], a[None],
-                                 None if b is None else b[None], S0=S0,
-                                 record_at=starts[:-1], want_o=True)
+    if not chains:
+        return {key: np.zeros(0) for key in out}
+    streams = [chain_stream(tok, mode, l, h, idx, ck) for (l, h) in chains]
+    q, k, v, a = (np.stack([st[i] for st in streams]) for i in range(4))
+    b = None if mode != GATED_DELTA else np.stack([st[4] for st in streams])
+    dk, dv = k.shape[2], v.shape[2]
+    S0 = None if S_init is None else np.stack([_np(x) for x in S_init])
+    # all chains in one call: independent chains run in parallel
+    Sf, o, Srec = recurrence(mode, q, k, v, a, b, S0=S0, record_at=starts[:-1], want_o=True)
+    for ci in range(len(chains)):
         oseam = np.zeros((len(order), w, dv))
         naive = np.zeros((dk, dv))
         for e, s in enumerate(order):
             sw = seam_len(seg_off, s, w)
-            oseam[e, :sw] = o[0, starts[e]:starts[e] + sw]
-            lo, hi = starts[e], starts[e + 1]
-            _, Sz = pair(mode, k[None, lo:hi], v[None, lo:hi], a[None, lo:hi],
-                         None if b is None else b[None, lo:hi])
-            naive += Sz[0]
-        out["S_prefix"].append(Srec[0])
+            oseam[e, :sw] = o[ci, starts[e]:starts[e] + sw]
+            if want_naive:
+                lo, hi = starts[e], starts[e + 1]
+                _, Sz = pair(mode, k[ci:ci + 1, lo:hi], v[ci:ci + 1, lo:hi], a[ci:ci + 1, lo:hi],
+                             None if b is None else b[ci:ci + 1, lo:hi])
+                naive += Sz[0]
+        out["S_prefix"].append(Srec[ci])
         out["o_seam"].append(oseam)
-        out["S_final"].append(Sf[0])
+        out["S_final"].append(Sf[ci])
         out["S_naive"].append(naive)
-    return {key: np.stack(val) if val else np.zeros(0) for key, val in out.items()}
+    return {key: np.stack(val) for key, val in out.items()}
 
 
 def seam_reference(desc, tok, seg_off, order, chains, S_in, entries):

@@ -1,0 +1,48 @@
+"""GPU parity at the full workload sizes, in the same calls the benchmark
+times: one batched build of every (segment, layer, head) pair, then one
+compose of the request with fused seams.  Outputs are checked on sampled
+blocks the fp64 oracle can compute one by one (whole pairs; whole chains over
+the full request: every prefix state, every seam output, the final state),
+plus properties that hold at any size (finite, deterministic)."""
+import numpy as np
+import pytest
+import torch
+
+from linear_attn_state_chunked_gb300 import hypic, workloads as W
+from _parity import run_pipeline, check_pairs, check_request, tol_of
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _sample(wl, n_items, n_chains, seed):
+    d = wl.desc
+    rng = np.random.default_rng(seed)
+    lens = wl.lengths
+    longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
+    items = {(d["n_layers"] - 1, longest, d["n_heads"] - 1), (0, shortest, 0)}
+    while len(items) < n_items:
+        items.add((int(rng.integers(d["n_layers"])), int(rng.integers(wl.n_seg)),
+                   int(rng.integers(d["n_heads"]))))
+    chains = {(0, 0), (d["n_layers"] - 1, d["n_heads"] - 1)}
+    while len(chains) < n_chains:
+        chains.add((int(rng.integers(d["n_layers"])), int(rng.integers(d["n_heads"]))))
+    return sorted(items), sorted(chains)
+
+
+@pytest.mark.parametrize("name", ["gdn_bf16", "stress_gdn", "warm_30l", "cold_30l"])
+def test_full_size(name):
+    wl = W.make(name, device="cuda")
+    out = run_pipeline(wl, prefix=True)
+    tol = tol_of(wl.desc)
+    for key in ("T", "S", "S_final", "S_prefix", "o"):
+        assert torch.isfinite(out[key]).all(), key
+    items, chains = _sample(wl, 8, 4, seed=sum(map(ord, name)))
+    check_pairs(wl, out, items, tol)
+    check_request(wl, out, chains, tol)
+    if name == "stress_gdn":
+        # the slow gate keeps T_C well away from zero, so composition matters
+        assert out["T"].abs().amax().item() > 1e-3
+    # the build has no atomics or races: a second run is bitwise identical
+    out2 = run_pipeline(wl, prefix=False)
+    assert torch.equal(out["T"], out2["T"]) and torch.equal(out["S"], out2["S"])
+    assert torch.equal(out["S_final"], out2["S_final"])
