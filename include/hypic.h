@@ -140,6 +140,15 @@ const char *hypic_last_error(void);
 size_t hypic_workspace_size(const hypic_desc *desc);
 
 /*
+ * Device status of a workspace after the builds that used it: waits for
+ * `stream`, then returns HYPIC_OK, or HYPIC_ERR_TIMEOUT if a bounded
+ * device-side wait of the build gave up (its outputs are then incomplete; the
+ * kernel returned instead of hanging).  The next build on the workspace
+ * clears the word.
+ */
+int hypic_workspace_status(const void *workspace, hypic_stream stream);
+
+/*
  * Segment build: for every segment s, layer l and head h, the cached pair of
  * the segment's body -- the segment's tokens after its first min(w, len)
  * seam tokens -- computed from a zero state:

@@ -184,8 +184,26 @@ int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok, const i
     a.S_out = S_out;
     a.work_counter = static_cast<unsigned int *>(workspace);
     a.status = reinterpret_cast<int *>(static_cast<char *>(workspace) + 128);
-    cudaError_t e = launch_build_rec(a, tab, (cudaStream_t)stream);
+    // Gated delta at d = 128 with bf16 inputs runs on the tensor cores (tf32
+    // products, 2e-3 class); everything else, including every fp32-input
+    // request (1e-5 class), runs the token-serial fp32 recurrence.
+    cudaError_t e = build_tc_supported(a.dm) ? launch_build_tc(a, tab, (cudaStream_t)stream)
+                                             : launch_build_rec(a, tab, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "segment build launch");
+    return HYPIC_OK;
+}
+
+int hypic_workspace_status(const void *workspace, hypic_stream stream)
+{
+    g_err[0] = 0;
+    if (!workspace || !aligned(workspace, 256))
+        return fail(HYPIC_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, static_cast<const char *>(workspace) + 128, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (word != 0) return fail(HYPIC_ERR_TIMEOUT, "a device-side wait of the last build gave up (status %d)", word);
     return HYPIC_OK;
 }
 

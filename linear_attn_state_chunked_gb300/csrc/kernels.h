@@ -35,6 +35,8 @@ struct SeamArgs {
 };
 
 cudaError_t launch_build_rec(const BuildArgs &a, const SegTable &tab, cudaStream_t st);
+bool build_tc_supported(const Dims &dm);
+cudaError_t launch_build_tc(const BuildArgs &a, const SegTable &tab, cudaStream_t st);
 cudaError_t launch_compose(const ComposeArgs &a, const SegTable &tab, cudaStream_t st);
 cudaError_t launch_seam(const SeamArgs &a, const SegTable &tab, cudaStream_t st);
 

@@ -23,7 +23,8 @@ STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_INVALID_ARG", 2: "HYPIC_ERR_SHAPE", 3: "H
 
 # Every symbol include/hypic.h declares.
 EXPORTS = ("hypic_version", "hypic_last_error", "hypic_workspace_size",
-           "hypic_segment_build", "hypic_compose", "hypic_seam_advance")
+           "hypic_workspace_status", "hypic_segment_build", "hypic_compose",
+           "hypic_seam_advance")
 
 
 class HypicError(RuntimeError):
@@ -61,6 +62,8 @@ def lib():
         L.hypic_last_error.restype = ctypes.c_char_p
         L.hypic_workspace_size.restype = ctypes.c_size_t
         L.hypic_workspace_size.argtypes = [ctypes.POINTER(Desc)]
+        L.hypic_workspace_status.restype = ctypes.c_int
+        L.hypic_workspace_status.argtypes = [vp, vp]
         L.hypic_segment_build.restype = ctypes.c_int
         L.hypic_segment_build.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p, i32,
                                           fp, fp, vp, ctypes.c_size_t, vp]
@@ -127,6 +130,12 @@ def _tok_n(tok, n_tokens):
 def workspace_size(desc):
     d = make_desc(desc)
     return int(lib().hypic_workspace_size(ctypes.byref(d)))
+
+
+def workspace_status(workspace, stream=None):
+    """Raise HypicError(HYPIC_ERR_TIMEOUT) if a device-side wait of a build on
+    this workspace gave up; waits for the stream."""
+    _check(lib().hypic_workspace_status(_p(workspace), _stream(stream)))
 
 
 def pair_shapes(desc, n_seg):
