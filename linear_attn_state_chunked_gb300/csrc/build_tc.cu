@@ -9,17 +9,32 @@
 //   L_tj = beta_j exp(g_t - g_j) k_t.k_j  (j < t),  D = diag(beta_j exp(g_C - g_j)).
 // The same map advances T (with V replaced by 0), so X = [T | S] (d_k x 2d)
 // is carried as one matrix.  Kept transposed in tensor memory (Xt = X^T,
-// 256 rows x 128), one chunk is
+// two 128-lane halves x 128 columns), one chunk is
 //   Pt = Xt K^T                       (tf32 MMA, A = Xt from tensor memory)
-//   Rt = [0 | V]^T - Pt diag(Gamma)   (CUDA cores)
-//   Xt = Gamma_C Xt + Rt U~,  U~^T = K^T D (I + L)^{-1}   (tf32 MMAs)
-// with the Gram matrix K K^T on the tensor core and the 64 x 64 unit lower
-// triangular inverse by blocked substitution on CUDA cores.  Every operand
-// written to shared memory is rounded to tf32 (the tensor core truncates).
+//   Rt = [0 | V]^T - Pt diag(Gamma)   (CUDA cores, written back over Pt)
+//   Xt = Gamma_C Xt + Rt U~           (tf32 MMA, A = Rt from tensor memory)
+//   U~^T = K^T D (I + L)^{-1}         (Gram K K^T and U~ on the tensor core,
+//                                      the 64 x 64 unit lower inverse by
+//                                      blocked substitution on CUDA cores)
+// Operands written by threads are rounded to tf32 (the tensor core
+// truncates).
 //
-// Work items (segment body, layer, head) are taken longest body first from a
-// device counter by persistent CTAs, one per SM: the greedy LPT schedule of
-// the pages' "段并行" section as a single-GPU stand-in.
+// Warp roles (one CTA per SM, persistent over work items):
+//   warp 9      TMA producer: raw bf16 K/V rows (+ conv history) and gates of
+//               each chunk into a 3-stage ring;
+//   warp 8      one thread issues every tcgen05.mma, interleaving the chunk
+//               pipeline (Pt, Xt updates) with the next chunk's preparation
+//               (Gram, U~) as their inputs become ready;
+//   warps 4-7   preparation of chunk n+1 while chunk n runs: gates, conv +
+//               normalisation, tf32 K, L, the inverse, U~;
+//   warps 0-3   epilogue of chunk n: Rt and the Gamma_C rescale of Xt, both
+//               halves, and the emission of each finished pair.
+// Work items (segment body, layer, head) arrive longest body first; CTA b
+// takes items b, b + grid, ... -- the greedy LPT order of the pages' "段并行"
+// section as a single-GPU stand-in for its scatter workers.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_util.cuh"
@@ -29,57 +44,129 @@ namespace {
 
 constexpr int D = 128;   // head width
 constexpr int C = 64;    // chunk length
-constexpr int NT = 128;  // threads = tensor-memory lanes
+constexpr int RS = 3;    // raw-input ring stages
+constexpr int HMAX = 3;  // conv history rows kept per chunk (conv_k <= 4)
+constexpr int ROWS = C + HMAX;
+constexpr int NT = 320;  // 10 warps
+constexpr int WARP_MMA = 8, WARP_TMA = 9;
+constexpr int BAR_EPI = 1, BAR_PREP = 2;
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds
 
 // tensor-memory columns
 constexpr uint32_t TM_XT = 0;    // Xt, T half: 128 lanes x 128
 constexpr uint32_t TM_XS = 128;  // Xt, S half
-constexpr uint32_t TM_PT = 256;  // Pt, T half: 128 x 64
-constexpr uint32_t TM_PS = 320;  // Pt, S half
-constexpr uint32_t TM_G = 384;   // Gram K K^T (M = 64 layout): 64 x 64
+constexpr uint32_t TM_PT = 256;  // Pt then Rt, T half: 128 x 64
+constexpr uint32_t TM_PS = 320;  // Pt then Rt, S half
+constexpr uint32_t TM_G = 384;   // Gram (M = 64 layout), then K^T (A of U~): 64 columns
 constexpr uint32_t TM_U = 448;   // U~^T: 128 x 64
 constexpr uint32_t TM_COLS = 512;
 
+// raw stage: K rows, V rows (bf16 [ROWS][128]), alpha[64], beta[64] (fp32)
+constexpr uint32_t ST_K = 0;
+constexpr uint32_t ST_V = ROWS * D * 2;
+constexpr uint32_t ST_A = 2 * ROWS * D * 2;
+constexpr uint32_t ST_B = ST_A + C * 4;
+constexpr uint32_t ST_BYTES = ST_B + C * 4;
+
 // shared memory (byte offsets from a 1024-aligned base)
-constexpr uint32_t SM_K32 = 0;               // K   [64][128]  tf32, sw128
-constexpr uint32_t SM_UT = 32768;            // U~^T [128][64] tf32, sw128 (B of the X update)
-constexpr uint32_t SM_RT = 65536;            // Rt  [2][128][64] tf32, sw128
-constexpr uint32_t SM_KT = SM_RT;            // K^T [128][64] (aliases Rt T half)
-constexpr uint32_t SM_MT = SM_RT + 32768;    // (D M)^T [64][64] (aliases Rt S half)
-constexpr uint32_t SM_V = 131072;            // V   [64][128] fp32
-constexpr int LP = C + 1;                    // padded row of L and M
-constexpr uint32_t SM_L = 163840;            // L   [64][65] fp32
-constexpr uint32_t SM_M = SM_L + C * LP * 4; // M = (I + L)^-1 [64][65]
-constexpr uint32_t SM_Q = SM_M + C * LP * 4; // block products [3][16][17]
-constexpr uint32_t SM_GATE = SM_Q + 3 * 16 * 17 * 4 + 64;  // 5 x 64 floats
-constexpr uint32_t SM_BYTES = SM_GATE + 5 * 64 * 4;
-constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t SM_RAW = 0;
+constexpr uint32_t SM_K32 = RS * ST_BYTES;     // K [64][128] tf32, sw128
+constexpr uint32_t SM_UT = SM_K32 + 32768;     // U~^T [128][64] tf32, sw128 (B of the Xt update)
+constexpr uint32_t SM_MT = SM_UT + 32768;      // (D M)^T [64][64] tf32, sw128 (B of U~)
+constexpr int LP = C + 1;
+constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][65]
+constexpr uint32_t SM_M = SM_L + C * LP * 4;   // (I + L)^-1 [64][65]
+constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // block products [3][16][17]
+constexpr uint32_t SM_GATE = SM_Q + 3 * 16 * 17 * 4;  // 2 x Gates
+constexpr uint32_t SM_BAR = SM_GATE + 2 * 1024;
+constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;
+constexpr uint32_t SM_BYTES = SM_MISC + 64;
+constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
+static_assert(SM_K32 % 1024 == 0 && SM_UT % 1024 == 0 && SM_MT % 1024 == 0, "tile alignment");
+static_assert(ST_BYTES % 128 == 0 && ST_V % 128 == 0, "TMA destination alignment");
+static_assert(SMEM_DYN <= 232448, "shared memory budget");
 
 struct Gates {
-    float g[C];    // inclusive log-gate sums
-    float b[C];    // beta
-    float eg[C];   // exp(g_t)
-    float dc[C];   // beta_j exp(g_C - g_j)
-    float lg[C];   // log alpha
+    float g[C];   // inclusive log-gate sums
+    float eg[C];  // exp(g_t)
+    float dc[C];  // beta_j exp(g_C - g_j)
+    float b[C];   // beta
 };
+
+// mbarriers
+enum {
+    B_FULL = 0,          // [RS] raw stage loaded (TMA bytes + producer arrive)
+    B_EMPTY = RS,        // [RS] raw stage released (prep + epilogue)
+    B_KREADY = 2 * RS,   // K32 written                      prep -> mma
+    B_GRAM,              // Gram done                        mma -> prep
+    B_KTREADY,           // K^T in TMEM and (D M)^T written   prep -> mma
+    B_UDONE,             // U~ done                          mma -> prep
+    B_UTREADY,           // U~^T copied to smem               prep -> mma
+    B_PTDONE,            // Pt (T half) done                 mma -> epilogue
+    B_PSDONE,            // Pt (S half) done                 mma -> epilogue, prep (K32 free)
+    B_RTREADY,           // Rt (T half) written, Xt_T scaled  epilogue -> mma
+    B_RSREADY,           // Rt (S half) written, Xt_S scaled  epilogue -> mma
+    B_DSDONE,            // both Xt updates done              mma -> epilogue, prep (U~^T free)
+    B_XREADY,            // Xt initialised for a new item     epilogue -> mma
+    B_COUNT
+};
+
+struct Item {
+    int s, l, h;
+    int32_t seg0, b0, n;  // segment start, body start, body length
+    int nch;              // chunks
+};
+
+__device__ __forceinline__ Item decode_item(int item, const Dims &dm, const SegTable &tab)
+{
+    Item it;
+    const int LH = dm.L * dm.H;
+    it.s = tab.perm[item / LH];
+    const int lh = item % LH;
+    it.l = lh / dm.H;
+    it.h = lh % dm.H;
+    it.seg0 = tab.off[it.s];
+    const int32_t seg1 = tab.off[it.s + 1];
+    it.b0 = it.seg0 + min(dm.w, seg1 - it.seg0);
+    it.n = seg1 - it.b0;
+    it.nch = (it.n + C - 1) / C;
+    return it;
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 __device__ __forceinline__ void unpack8(const uint4 &u, float *x)
 {
     x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
     x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
 }
-
-// Blocked inverse of the unit lower triangular (I + L), 64 = 4 x 16 blocks:
-// diagonal blocks by substitution, then M_ij = -M_ii sum_{k=j}^{i-1} L_ik M_kj
-// level by level.
-__device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int tid)
+__device__ __forceinline__ float bf16_at(const uint8_t *tile, int row, int col)
 {
-    if (tid < 64) {
-        const int b = tid >> 4, cc = tid & 15, base = 16 * b;
+    const uint16_t u = *reinterpret_cast<const uint16_t *>(tile + (row * D + col) * 2);
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+
+// Bounded wait by one thread; any failure (or another role's) aborts the CTA.
+__device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
+{
+    const long long t0 = clock64();
+    while (!tc::mbar_test(mbar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// Blocked inverse of the unit lower triangular (I + L), 64 = 4 x 16 blocks,
+// by the 128 preparation threads (pt = 0..127): diagonal blocks by
+// substitution, then M_ij = -M_ii sum_{k=j}^{i-1} L_ik M_kj level by level.
+__device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt)
+{
+    if (pt < 64) {
+        const int b = pt >> 4, cc = pt & 15, base = 16 * b;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -91,17 +178,16 @@ __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int ti
 #pragma unroll
         for (int r = 0; r < 16; ++r) Ms[(base + r) * LP + base + cc] = x[r];
     }
-    // strictly upper blocks are zero
-    for (int e = tid; e < 6 * 256; e += NT) {
+    for (int e = pt; e < 6 * 256; e += 128) {
         const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
         const int bi = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
         const int bj = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
         Ms[(16 * bi + r) * LP + 16 * bj + cc] = 0.f;
     }
-    __syncthreads();
+    tc::bar_sync(BAR_PREP, 128);
     for (int delta = 1; delta <= 3; ++delta) {
         const int nblk = 4 - delta;
-        for (int e = tid; e < nblk * 256; e += NT) {
+        for (int e = pt; e < nblk * 256; e += 128) {
             const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int bj = blk, bi = blk + delta;
             float acc = 0.f;
@@ -112,8 +198,8 @@ __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int ti
             }
             Qs[(blk * 16 + r) * 17 + cc] = acc;
         }
-        __syncthreads();
-        for (int e = tid; e < nblk * 256; e += NT) {
+        tc::bar_sync(BAR_PREP, 128);
+        for (int e = pt; e < nblk * 256; e += 128) {
             const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
             const int bj = blk, bi = blk + delta;
             float acc = 0.f;
@@ -122,336 +208,516 @@ __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int ti
                 acc = fmaf(Ms[(16 * bi + r) * LP + 16 * bi + q], Qs[(blk * 16 + q) * 17 + cc], acc);
             Ms[(16 * bi + r) * LP + 16 * bj + cc] = -acc;
         }
-        __syncthreads();
+        tc::bar_sync(BAR_PREP, 128);
+    }
+}
+
+// Cursor over this CTA's chunks (non-empty items only), used by the MMA issuer.
+struct Cursor {
+    int item;  // global item index (blockIdx.x + k * gridDim.x)
+    int c;     // chunk within the item
+    int nch;
+    int n;     // CTA-wide chunk number
+    int xi;    // index of the item among this CTA's non-empty items
+};
+
+__device__ __forceinline__ void cursor_seek(Cursor &cu, int n_items, const Dims &dm, const SegTable &tab)
+{
+    while (cu.item < n_items) {
+        const Item it = decode_item(cu.item, dm, tab);
+        if (it.nch > 0) {
+            cu.nch = it.nch;
+            return;
+        }
+        cu.item += gridDim.x;
+    }
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &cu, int n_items, const Dims &dm, const SegTable &tab)
+{
+    ++cu.n;
+    if (++cu.c == cu.nch) {
+        cu.c = 0;
+        ++cu.xi;
+        cu.item += gridDim.x;
+        cursor_seek(cu, n_items, dm, tab);
     }
 }
 
 template <int CK>
 __global__ void __launch_bounds__(NT, 1)
-build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ SegTable tab)
+build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ SegTable tab,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV)
 {
+    constexpr int HIST = CK > 0 ? CK - 1 : 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t mbar;
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ int item_sh;
-
-    float *Vs = reinterpret_cast<float *>(sm + SM_V);
+    const uint32_t s_base = tc::smem_u32(sm);
+    const uint32_t sK32 = s_base + SM_K32, sUT = s_base + SM_UT, sMT = s_base + SM_MT;
+    auto bar = [&](int i) { return s_base + SM_BAR + 8u * i; };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM_MISC);
+    uint32_t *tmem_base_sh = reinterpret_cast<uint32_t *>(sm + SM_MISC + 16);
     float *Ls = reinterpret_cast<float *>(sm + SM_L);
     float *Ms = reinterpret_cast<float *>(sm + SM_M);
     float *Qs = reinterpret_cast<float *>(sm + SM_Q);
-    Gates &gt = *reinterpret_cast<Gates *>(sm + SM_GATE);
-    const uint32_t s_base = tc::smem_u32(sm);
-    const uint32_t sK32 = s_base + SM_K32, sUT = s_base + SM_UT, sRT = s_base + SM_RT;
-    const uint32_t sKT = s_base + SM_KT, sMT = s_base + SM_MT;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Dims dm = a.dm;
     const int32_t N = a.tok.N;
-    const int LH = dm.L * dm.H;
-    const int n_items = tab.n_seg * LH;
-    const uint32_t mb = tc::smem_u32(&mbar);
+    const int n_items = tab.n_seg * dm.L * dm.H;
 
     if (tid == 0) {
-        tc::mbar_init(mb, 1);
+        *abort_flag = 0;
+        for (int i = 0; i < B_COUNT; ++i) {
+            uint32_t cnt = 1;
+            if (i >= B_EMPTY && i < B_EMPTY + RS) cnt = 2;
+            tc::mbar_init(bar(i), cnt);
+        }
         tc::fence_mbar_init();
     }
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&tmem_base_sh), TM_COLS);
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_base_sh), TM_COLS);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    const uint32_t tb = tmem_base_sh;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t my = tb + lane_off;  // this thread's lane, column 0
-    uint32_t phase = 0;
-    bool failed = false;
+    const uint32_t tb = *tmem_base_sh;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t my = tb + lane_off;  // this thread's lane (quadrant of its warp), column 0
 
-    const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(a.tok.k);
-    const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(a.tok.v);
-    const __nv_bfloat16 *ap = static_cast<const __nv_bfloat16 *>(a.tok.alpha);
-    const __nv_bfloat16 *bp = static_cast<const __nv_bfloat16 *>(a.tok.beta);
-
-    // issue from one thread, then wait for completion on every thread
-    auto mma_done = [&]() -> bool {
-        const bool ok = tc::mbar_wait(mb, phase, kWaitCycles);
-        phase ^= 1u;
-        tc::fence_after();
-        return __syncthreads_and(ok);
-    };
-
-    while (true) {
-        if (tid == 0) item_sh = static_cast<int>(atomicAdd(a.work_counter, 1u));
-        __syncthreads();
-        const int item = item_sh;
-        if (item >= n_items) break;
-        const int s = tab.perm[item / LH];
-        const int lh = item % LH;
-        const int l = lh / dm.H, h = lh % dm.H;
-        const int32_t seg0 = tab.off[s], seg1 = tab.off[s + 1];
-        const int32_t b0 = seg0 + min(dm.w, seg1 - seg0);
-        const int32_t n = seg1 - b0;
-
-        // X = [I | 0]
-        {
-            float v[32];
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = (c + i == tid) ? 1.f : 0.f;
-                tc::tmem_st32(my + TM_XT + c, v);
+    if (warp == WARP_TMA) {
+        // ------------------------------------------------------------ producer
+        const __nv_bfloat16 *ap = static_cast<const __nv_bfloat16 *>(a.tok.alpha);
+        const __nv_bfloat16 *bp = static_cast<const __nv_bfloat16 *>(a.tok.beta);
+        int n = 0;
+        bool ok = true;
+        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
+            const Item it = decode_item(itx, dm, tab);
+            for (int c = 0; c < it.nch; ++c) {
+                const int s = n % RS, use = n / RS;
+                if (use > 0) {
+                    bool w = true;
+                    if (lane == 0) w = wait_bar(bar(B_EMPTY + s), (use - 1) & 1, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+                }
+                uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
+                const int32_t t0 = c * C;
+                const int nc = min(C, (int)(it.n - t0));
+                for (int tt = lane; tt < C; tt += 32) {
+                    float al = 1.f, be = 0.f;
+                    if (tt < nc) {
+                        const size_t gi = gate_index(dm, N, it.l, it.b0 + t0 + tt, it.h);
+                        al = __bfloat162float(ap[gi]);
+                        be = __bfloat162float(bp[gi]);
+                    }
+                    reinterpret_cast<float *>(stg + ST_A)[tt] = al;
+                    reinterpret_cast<float *>(stg + ST_B)[tt] = be;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t fb = bar(B_FULL + s);
+                    tc::mbar_arrive_expect_tx(fb, 2u * (C + HIST) * D * 2);
+                    const int row0 = it.b0 + t0 - HIST;
+                    tc::tma_load_4d(s_base + SM_RAW + s * ST_BYTES + ST_K, &tmK, 0, it.h, row0, it.l, fb);
+                    tc::tma_load_4d(s_base + SM_RAW + s * ST_BYTES + ST_V, &tmV, 0, it.h, row0, it.l, fb);
+                }
+                ++n;
             }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-#pragma unroll
-            for (int c = 0; c < D; c += 32) tc::tmem_st32(my + TM_XS + c, v);
         }
-
-        for (int32_t t0 = 0; t0 < n && !failed; t0 += C) {
-            const int nc = min(C, (int)(n - t0));
-            // ---- gates: inclusive scan of log alpha over the chunk
-            if (tid < C) {
-                const bool valid = tid < nc;
-                float al = 1.f, be = 0.f;
-                if (valid) {
-                    const size_t gi = gate_index(dm, N, l, b0 + t0 + tid, h);
-                    al = __bfloat162float(ap[gi]);
-                    be = __bfloat162float(bp[gi]);
+        if (!ok && lane == 0) {
+            // aborted: let the copies this warp started land before the CTA exits
+            for (int k = (n > RS ? n - RS : 0); k < n; ++k) {
+                const long long t0 = clock64();
+                while (!tc::mbar_test(bar(B_FULL + k % RS), (k / RS) & 1) && clock64() - t0 < kWaitCycles) {
                 }
-                float x = fmaxf(logf(al), -88.f);  // alpha = 0 -> exp(-88), below fp32 normals
-                gt.lg[tid] = x;
-                gt.b[tid] = be;
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            Cursor pc{static_cast<int>(blockIdx.x), 0, 0, 0, 0};
+            cursor_seek(pc, n_items, dm, tab);
+            Cursor mc = pc;
+            int pstep = 0, mstep = 0;
+            long long idle_since = clock64();
+            while ((pc.item < n_items || mc.item < n_items) && !*abort_flag) {
+                bool progressed = false;
+                if (pc.item < n_items) {
+                    if (pstep == 0 && tc::mbar_test(bar(B_KREADY), pc.n & 1)) {
+                        tc::fence_after();
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
+                        for (int ks = 0; ks < D / 8; ++ks)
+                            tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks),
+                                       tc::idesc_tf32(64, 64), ks > 0);
+                        tc::commit(bar(B_GRAM));
+                        pstep = 1;
+                        progressed = true;
+                    } else if (pstep == 1 && tc::mbar_test(bar(B_KTREADY), pc.n & 1)) {
+                        tc::fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < C / 8; ++ks)
+                            tc::mma_ts(tb + TM_U, tb + TM_G + ks * 8, tc::sdesc_kstep(sMT, C, ks),
+                                       tc::idesc_tf32(128, 64), ks > 0);
+                        tc::commit(bar(B_UDONE));
+                        pstep = 0;
+                        cursor_next(pc, n_items, dm, tab);
+                        progressed = true;
+                    }
                 }
-                gt.g[tid] = x;
+                if (mc.item < n_items) {
+                    // Gram(n) issued <=> the prep cursor passed step 0 of chunk n
+                    const bool gram_issued = pc.n > mc.n || (pc.n == mc.n && pstep == 1);
+                    const bool u_issued = pc.n > mc.n;
+                    if (mstep == 0 && gram_issued &&
+                        (mc.c != 0 || tc::mbar_test(bar(B_XREADY), mc.xi & 1))) {
+                        tc::fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < D / 8; ++ks)
+                            tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK32, C, ks),
+                                       tc::idesc_tf32(128, 64), ks > 0);
+                        tc::commit(bar(B_PTDONE));
+#pragma unroll
+                        for (int ks = 0; ks < D / 8; ++ks)
+                            tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks),
+                                       tc::idesc_tf32(128, 64), ks > 0);
+                        tc::commit(bar(B_PSDONE));
+                        mstep = 1;
+                        progressed = true;
+                    } else if (mstep == 1 && u_issued && tc::mbar_test(bar(B_UTREADY), mc.n & 1) &&
+                               tc::mbar_test(bar(B_RTREADY), mc.n & 1)) {
+                        tc::fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < C / 8; ++ks)
+                            tc::mma_ts(tb + TM_XT, tb + TM_PT + ks * 8, tc::sdesc_kstep(sUT, D, ks),
+                                       tc::idesc_tf32(128, 128), 1);
+                        mstep = 2;
+                        progressed = true;
+                    } else if (mstep == 2 && tc::mbar_test(bar(B_RSREADY), mc.n & 1)) {
+                        tc::fence_after();
+#pragma unroll
+                        for (int ks = 0; ks < C / 8; ++ks)
+                            tc::mma_ts(tb + TM_XS, tb + TM_PS + ks * 8, tc::sdesc_kstep(sUT, D, ks),
+                                       tc::idesc_tf32(128, 128), 1);
+                        tc::commit(bar(B_DSDONE));
+                        mstep = 0;
+                        cursor_next(mc, n_items, dm, tab);
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle_since = clock64();
+                } else {
+                    if (clock64() - idle_since > kWaitCycles) *abort_flag = 1;
+                    __nanosleep(32);
+                }
             }
-            __syncthreads();
-            if (tid >= 32 && tid < C) gt.g[tid] += gt.g[31];
-            __syncthreads();
-            if (tid < C) {
-                const float gC = gt.g[C - 1];
-                gt.eg[tid] = expf(gt.g[tid]);
-                gt.dc[tid] = gt.b[tid] * expf(gC - gt.g[tid]);
-            }
-            // ---- tokens: K (tf32, both orientations) and V, 8 channels per thread step
-            const float *wk = nullptr, *wv = nullptr;
-            if (CK > 0) {
-                wk = a.tok.conv_w + (((size_t)l * 3 + 1) * dm.H + h) * D * CK;
-                wv = a.tok.conv_w + (((size_t)l * 3 + 2) * dm.H + h) * D * CK;
-            }
-#pragma unroll 1
-            for (int it = 0; it < (C * D / 8) / NT; ++it) {
-                const int t = it * (NT / 16) + (tid >> 4);
-                const int c0 = (tid & 15) * 8;
-                float kx[8], vx[8];
-                if (t < nc) {
-                    const int32_t tok = b0 + t0 + t;
-                    if (CK == 0) {
-                        unpack8(*reinterpret_cast<const uint4 *>(kp + tok_index(dm, N, l, tok, h, c0)), kx);
-                        unpack8(*reinterpret_cast<const uint4 *>(vp + tok_index(dm, N, l, tok, h, c0)), vx);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ preparation
+        const int pt = tid - 128;
+        const float *wk = nullptr;
+        int n = 0;
+        bool ok = true;
+        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
+            const Item it = decode_item(itx, dm, tab);
+            if (CK > 0) wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
+            for (int c = 0; c < it.nch; ++c, ++n) {
+                const int s = n % RS;
+                const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
+                Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (n & 1) * 1024);
+                const int nc = min(C, (int)(it.n - c * C));
+                bool w = true;
+                if (pt == 0) {
+                    w = wait_bar(bar(B_FULL + s), (n / RS) & 1, abort_flag);
+                    if (w && n > 0) w = wait_bar(bar(B_PSDONE), (n - 1) & 1, abort_flag);  // K32 free
+                }
+                if (!tc::bar_and(BAR_PREP, 128, w)) { ok = false; break; }
+                // gates (one warp, two tokens per lane)
+                if (warp == 4) {
+                    const float *A = reinterpret_cast<const float *>(stg + ST_A);
+                    const float *B = reinterpret_cast<const float *>(stg + ST_B);
+                    const float x0 = fmaxf(logf(A[2 * lane]), -88.f);  // alpha = 0 -> exp(-88)
+                    const float x1 = fmaxf(logf(A[2 * lane + 1]), -88.f);
+                    float sum = x0 + x1;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, sum, o);
+                        if (lane >= o) sum += y;
+                    }
+                    const float total = __shfl_sync(0xffffffffu, sum, 31);
+                    const float g1 = sum, g0 = sum - x1;
+                    G.g[2 * lane] = g0;
+                    G.g[2 * lane + 1] = g1;
+                    G.eg[2 * lane] = expf(g0);
+                    G.eg[2 * lane + 1] = expf(g1);
+                    G.b[2 * lane] = B[2 * lane];
+                    G.b[2 * lane + 1] = B[2 * lane + 1];
+                    G.dc[2 * lane] = B[2 * lane] * expf(total - g0);
+                    G.dc[2 * lane + 1] = B[2 * lane + 1] * expf(total - g1);
+                }
+                // K -> tf32 (conv + L2 normalisation first when present)
+#pragma unroll 2
+                for (int iter = 0; iter < (C * D / 8) / 128; ++iter) {
+                    const int t = iter * 8 + (pt >> 4);
+                    const int c0 = (pt & 15) * 8;
+                    float kx[8];
+                    if (t < nc) {
+                        if (CK == 0) {
+                            unpack8(*reinterpret_cast<const uint4 *>(stg + ST_K + (t * D + c0) * 2), kx);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) kx[i] = 0.f;
+#pragma unroll
+                            for (int j = 0; j < CK; ++j) {
+                                float rk[8];
+                                unpack8(*reinterpret_cast<const uint4 *>(stg + ST_K + ((t + HIST - j) * D + c0) * 2),
+                                        rk);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) kx[i] = fmaf(__ldg(wk + (c0 + i) * CK + j), rk[i], kx[i]);
+                            }
+                        }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) kx[i] = vx[i] = 0.f;
+                        for (int i = 0; i < 8; ++i) kx[i] = 0.f;
+                    }
+                    if (CK > 0) {
+                        float ss = 0.f;
 #pragma unroll
-                        for (int j = 0; j < CK; ++j) {
-                            const int32_t tj = tok - j;
-                            if (tj >= seg0) {
-                                float rk[8], rv[8];
-                                unpack8(*reinterpret_cast<const uint4 *>(kp + tok_index(dm, N, l, tj, h, c0)), rk);
-                                unpack8(*reinterpret_cast<const uint4 *>(vp + tok_index(dm, N, l, tj, h, c0)), rv);
+                        for (int i = 0; i < 8; ++i) ss = fmaf(kx[i], kx[i], ss);
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    kx[i] = fmaf(__ldg(wk + (c0 + i) * CK + j), rk[i], kx[i]);
-                                    vx[i] = fmaf(__ldg(wv + (c0 + i) * CK + j), rv[i], vx[i]);
+                        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                        const float inv = 1.f / sqrtf(ss + kL2Eps);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) kx[i] *= inv;
+                    }
+                    *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(t, c0, C)) =
+                        make_float4(tc::round_tf32(kx[0]), tc::round_tf32(kx[1]), tc::round_tf32(kx[2]),
+                                    tc::round_tf32(kx[3]));
+                    *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(t, c0 + 4, C)) =
+                        make_float4(tc::round_tf32(kx[4]), tc::round_tf32(kx[5]), tc::round_tf32(kx[6]),
+                                    tc::round_tf32(kx[7]));
+                }
+                tc::fence_async_smem();
+                tc::bar_sync(BAR_PREP, 128);
+                if (pt == 0) {
+                    tc::mbar_arrive(bar(B_KREADY));
+                    tc::mbar_arrive(bar(B_EMPTY + s));  // K rows and gates consumed
+                }
+                // L from the Gram rows (M = 64 layout: row 16q + i in lane 32q + i)
+                if (pt == 0) w = wait_bar(bar(B_GRAM), n & 1, abort_flag);
+                if (!tc::bar_and(BAR_PREP, 128, w)) { ok = false; break; }
+                tc::fence_after();
+                {
+                    float gr[64];
+                    tc::tmem_ld32(my + TM_G, gr);
+                    tc::tmem_ld32(my + TM_G + 32, gr + 32);
+                    if (lane < 16) {
+                        const int t = 16 * (warp & 3) + lane;
+                        const float gt_t = G.g[t];
+#pragma unroll
+                        for (int j = 0; j < C; ++j)
+                            Ls[t * LP + j] = (j < t) ? G.b[j] * expf(gt_t - G.g[j]) * gr[j] : 0.f;
+                    }
+                }
+                tc::bar_sync(BAR_PREP, 128);
+                unit_lower_inverse(Ls, Ms, Qs, pt);
+                // K^T into tensor memory (A of U~): lane i holds K[j][i], j = 0..63
+                {
+                    float kt[32];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            kt[j] = *reinterpret_cast<const float *>(sm + SM_K32 + tc::sw128_f32(h2 * 32 + j, pt, C));
+                        tc::tmem_st32(my + TM_G + h2 * 32, kt);
+                    }
+                }
+                // B of U~: element (t, j) = dc_j M[j][t]
+                for (int e = pt; e < C * C; e += 128) {
+                    const int t = e >> 6, j = e & 63;
+                    *reinterpret_cast<float *>(sm + SM_MT + tc::sw128_f32(t, j, C)) =
+                        tc::round_tf32(G.dc[j] * Ms[j * LP + t]);
+                }
+                tc::fence_async_smem();
+                tc::fence_before();
+                tc::bar_sync(BAR_PREP, 128);
+                if (pt == 0) tc::mbar_arrive(bar(B_KTREADY));
+                // U~^T rows into shared memory once the previous chunk's Xt update is done
+                if (pt == 0) {
+                    w = wait_bar(bar(B_UDONE), n & 1, abort_flag);
+                    if (w && n > 0) w = wait_bar(bar(B_DSDONE), (n - 1) & 1, abort_flag);
+                }
+                if (!tc::bar_and(BAR_PREP, 128, w)) { ok = false; break; }
+                tc::fence_after();
+                {
+                    float u[32];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        tc::tmem_ld32(my + TM_U + h2 * 32, u);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(sm + SM_UT + tc::sw128_f32(pt, h2 * 32 + i, D)) =
+                                make_float4(tc::round_tf32(u[i]), tc::round_tf32(u[i + 1]),
+                                            tc::round_tf32(u[i + 2]), tc::round_tf32(u[i + 3]));
+                    }
+                }
+                tc::fence_async_smem();
+                tc::fence_before();
+                tc::bar_sync(BAR_PREP, 128);
+                if (pt == 0) tc::mbar_arrive(bar(B_UTREADY));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 0-3)
+        const int m = tid;  // row of Xt / Pt in each half = tensor-memory lane
+        const float *wv = nullptr;
+        int n = 0;
+        bool ok = true;
+        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
+            const Item it = decode_item(itx, dm, tab);
+            const size_t pair = ((size_t)it.l * tab.n_seg + it.s) * dm.H + it.h;
+            float *To = a.T_out + pair * D * D + m;
+            float *So = a.S_out + pair * D * D + m;
+            if (it.nch == 0) {
+                for (int i = 0; i < D; ++i) {
+                    To[(size_t)i * D] = (i == m) ? 1.f : 0.f;
+                    So[(size_t)i * D] = 0.f;
+                }
+                continue;
+            }
+            if (CK > 0) wv = a.tok.conv_w + (((size_t)it.l * 3 + 2) * dm.H + it.h) * D * CK;
+            // Xt = [I | 0]^T
+            {
+                float v[32];
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = (c + i == m) ? 1.f : 0.f;
+                    tc::tmem_st32(my + TM_XT + c, v);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < D; c += 32) tc::tmem_st32(my + TM_XS + c, v);
+            }
+            tc::fence_before();
+            tc::bar_sync(BAR_EPI, 128);
+            if (m == 0) tc::mbar_arrive(bar(B_XREADY));
+            for (int c = 0; c < it.nch; ++c, ++n) {
+                const int s = n % RS;
+                const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
+                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (n & 1) * 1024);
+                const int nc = min(C, (int)(it.n - c * C));
+                // ---- T half
+                bool w = true;
+                if (m == 0) w = wait_bar(bar(B_PTDONE), n & 1, abort_flag);
+                if (!tc::bar_and(BAR_EPI, 128, w)) { ok = false; break; }
+                tc::fence_after();
+                const float gC = G.eg[C - 1];
+                {
+                    float p[32];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        tc::tmem_ld32(my + TM_PT + h2 * 32, p);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) p[i] = tc::round_tf32(-G.eg[h2 * 32 + i] * p[i]);
+                        tc::tmem_st32(my + TM_PT + h2 * 32, p);
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        tc::tmem_ld32(my + TM_XT + cc, p);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) p[i] *= gC;
+                        tc::tmem_st32(my + TM_XT + cc, p);
+                    }
+                }
+                tc::fence_before();
+                tc::bar_sync(BAR_EPI, 128);
+                if (m == 0) tc::mbar_arrive(bar(B_RTREADY));
+                // ---- S half
+                if (m == 0) {
+                    w = wait_bar(bar(B_PSDONE), n & 1, abort_flag);
+                    if (w) w = wait_bar(bar(B_FULL + s), (n / RS) & 1, abort_flag);
+                }
+                if (!tc::bar_and(BAR_EPI, 128, w)) { ok = false; break; }
+                tc::fence_after();
+                {
+                    float p[32];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        tc::tmem_ld32(my + TM_PS + h2 * 32, p);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int t = h2 * 32 + i;
+                            float vv = 0.f;
+                            if (t < nc) {
+                                if (CK == 0) {
+                                    vv = bf16_at(stg + ST_V, t, m);
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < CK; ++j)
+                                        vv = fmaf(__ldg(wv + m * CK + j), bf16_at(stg + ST_V, t + HIST - j, m), vv);
                                 }
                             }
+                            p[i] = tc::round_tf32(fmaf(-G.eg[t], p[i], vv));
                         }
+                        tc::tmem_st32(my + TM_PS + h2 * 32, p);
                     }
-                } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) kx[i] = vx[i] = 0.f;
-                }
-                if (CK > 0) {
-                    // per-token L2 normalisation of k over the 16 lanes holding the row
-                    float ss = 0.f;
+                    for (int cc = 0; cc < D; cc += 32) {
+                        tc::tmem_ld32(my + TM_XS + cc, p);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) ss = fmaf(kx[i], kx[i], ss);
-#pragma unroll
-                    for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                    const float inv = 1.f / sqrtf(ss + kL2Eps);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) kx[i] *= inv;
-                }
-                float kr[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) kr[i] = tc::round_tf32(kx[i]);
-                *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(t, c0, C)) =
-                    make_float4(kr[0], kr[1], kr[2], kr[3]);
-                *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(t, c0 + 4, C)) =
-                    make_float4(kr[4], kr[5], kr[6], kr[7]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    *reinterpret_cast<float *>(sm + SM_KT + tc::sw128_f32(c0 + i, t, D)) = kr[i];
-                *reinterpret_cast<float4 *>(Vs + t * D + c0) = make_float4(vx[0], vx[1], vx[2], vx[3]);
-                *reinterpret_cast<float4 *>(Vs + t * D + c0 + 4) = make_float4(vx[4], vx[5], vx[6], vx[7]);
-            }
-            tc::fence_async_smem();
-            tc::fence_before();
-            __syncthreads();
-            // ---- Gram K K^T (M = 64)
-            if (tid == 0) {
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks),
-                               tc::idesc_tf32(64, 64), ks > 0);
-                tc::commit(mb);
-            }
-            if (!mma_done()) { failed = true; break; }
-            // ---- L from the Gram rows (M = 64 layout: row 16w + i in lane 32w + i)
-            {
-                float gr[64];
-                tc::tmem_ld32(my + TM_G, gr);
-                tc::tmem_ld32(my + TM_G + 32, gr + 32);
-                if (lane < 16) {
-                    const int t = 16 * warp + lane;
-                    const float gt_t = gt.g[t];
-#pragma unroll
-                    for (int j = 0; j < C; ++j)
-                        Ls[t * LP + j] = (j < t) ? gt.b[j] * expf(gt_t - gt.g[j]) * gr[j] : 0.f;
-                }
-            }
-            __syncthreads();
-            unit_lower_inverse(Ls, Ms, Qs, tid);
-            // ---- B operand of U~^T: element (t, j) = dc_j M[j][t]
-            for (int e = tid; e < C * C; e += NT) {
-                const int t = e >> 6, j = e & 63;
-                *reinterpret_cast<float *>(sm + SM_MT + tc::sw128_f32(t, j, C)) =
-                    tc::round_tf32(gt.dc[j] * Ms[j * LP + t]);
-            }
-            tc::fence_async_smem();
-            tc::fence_before();
-            __syncthreads();
-            // ---- U~^T = K^T (D M)   (M = 128, N = 64, K = 64)
-            if (tid == 0) {
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    tc::mma_ss(tb + TM_U, tc::sdesc_kstep(sKT, D, ks), tc::sdesc_kstep(sMT, C, ks),
-                               tc::idesc_tf32(128, 64), ks > 0);
-                tc::commit(mb);
-            }
-            if (!mma_done()) { failed = true; break; }
-            {
-                float u[32];
-#pragma unroll
-                for (int c = 0; c < C; c += 32) {
-                    tc::tmem_ld32(my + TM_U + c, u);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4 *>(sm + SM_UT + tc::sw128_f32(tid, c + i, D)) =
-                            make_float4(tc::round_tf32(u[i]), tc::round_tf32(u[i + 1]),
-                                        tc::round_tf32(u[i + 2]), tc::round_tf32(u[i + 3]));
-                }
-            }
-            tc::fence_async_smem();
-            tc::fence_before();
-            __syncthreads();
-            // ---- Pt = Xt K^T for both halves (A from tensor memory)
-            if (tid == 0) {
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK32, C, ks),
-                               tc::idesc_tf32(128, 64), ks > 0);
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks),
-                               tc::idesc_tf32(128, 64), ks > 0);
-                tc::commit(mb);
-            }
-            if (!mma_done()) { failed = true; break; }
-            // ---- Rt = [0 | V]^T - Pt diag(Gamma); Xt *= Gamma_C
-            {
-                float p[32];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint32_t src = my + (half ? TM_PS : TM_PT);
-                    const uint32_t dst = SM_RT + half * 32768;
-#pragma unroll
-                    for (int c = 0; c < C; c += 32) {
-                        tc::tmem_ld32(src + c, p);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            float r4[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int t = c + i + q;
-                                const float vb = half ? Vs[t * D + tid] : 0.f;
-                                r4[q] = tc::round_tf32(fmaf(-gt.eg[t], p[i + q], vb));
-                            }
-                            *reinterpret_cast<float4 *>(sm + dst + tc::sw128_f32(tid, c + i, D)) =
-                                make_float4(r4[0], r4[1], r4[2], r4[3]);
-                        }
+                        for (int i = 0; i < 32; ++i) p[i] *= gC;
+                        tc::tmem_st32(my + TM_XS + cc, p);
                     }
                 }
-                const float gC = gt.eg[C - 1];
-#pragma unroll
-                for (int c = 0; c < 2 * D; c += 32) {
-                    tc::tmem_ld32(my + TM_XT + c, p);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) p[i] *= gC;
-                    tc::tmem_st32(my + TM_XT + c, p);
+                tc::fence_before();
+                tc::bar_sync(BAR_EPI, 128);
+                if (m == 0) {
+                    tc::mbar_arrive(bar(B_RSREADY));
+                    tc::mbar_arrive(bar(B_EMPTY + s));  // V rows consumed
                 }
             }
-            tc::fence_async_smem();
-            tc::fence_before();
-            __syncthreads();
-            // ---- Xt += Rt U~   (M = 128, N = 128, K = 64) per half
-            if (tid == 0) {
-                tc::fence_after();
+            if (!ok) break;
+            // ---- emit the finished pair: T[i][m] = Xt_T[m][i], S[i][m] = Xt_S[m][i]
+            bool w = true;
+            if (m == 0) w = wait_bar(bar(B_DSDONE), (n - 1) & 1, abort_flag);
+            if (!tc::bar_and(BAR_EPI, 128, w)) { ok = false; break; }
+            tc::fence_after();
+            {
+                float x[32];
 #pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    tc::mma_ss(tb + TM_XT, tc::sdesc_kstep(sRT, D, ks), tc::sdesc_kstep(sUT, D, ks),
-                               tc::idesc_tf32(128, 128), 1);
+                for (int cc = 0; cc < D; cc += 32) {
+                    tc::tmem_ld32(my + TM_XT + cc, x);
 #pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    tc::mma_ss(tb + TM_XS, tc::sdesc_kstep(sRT + 32768, D, ks), tc::sdesc_kstep(sUT, D, ks),
-                               tc::idesc_tf32(128, 128), 1);
-                tc::commit(mb);
-            }
-            if (!mma_done()) { failed = true; break; }
-        }
-        if (failed) break;
-        // ---- emit: T[i][m] = Xt_T[m][i], S[i][m] = Xt_S[m][i]; thread m owns column m
-        {
-            const size_t pair = ((size_t)l * tab.n_seg + s) * dm.H + h;
-            float *To = a.T_out + pair * D * D + tid;
-            float *So = a.S_out + pair * D * D + tid;
-            float x[32];
+                    for (int i = 0; i < 32; ++i) To[(size_t)(cc + i) * D] = x[i];
+                    tc::tmem_ld32(my + TM_XS + cc, x);
 #pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                tc::tmem_ld32(my + TM_XT + c, x);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) To[(size_t)(c + i) * D] = x[i];
-                tc::tmem_ld32(my + TM_XS + c, x);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) So[(size_t)(c + i) * D] = x[i];
+                    for (int i = 0; i < 32; ++i) So[(size_t)(cc + i) * D] = x[i];
+                }
             }
         }
-        tc::fence_before();
-        __syncthreads();
     }
-    if (failed && tid == 0) atomicOr(a.status, 1);
+
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (tid == 0 && *abort_flag) atomicOr(a.status, 1);
     if (warp == 0) tc::tmem_dealloc(tb, TM_COLS);
 }
 
 int g_num_sms = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t make_token_map(CUtensorMap *map, const void *base, const Dims &dm, int32_t N, int rows)
+{
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)dm.H, (cuuint64_t)N, (cuuint64_t)dm.L};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)dm.H * D * 2, (cuuint64_t)N * dm.H * D * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)rows, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 }  // namespace
 
@@ -465,24 +731,34 @@ cudaError_t launch_build_tc(const BuildArgs &a, const SegTable &tab, cudaStream_
 {
     const int n_items = tab.n_seg * a.dm.L * a.dm.H;
     if (n_items == 0) return cudaSuccess;
+    cudaError_t e;
     if (g_num_sms == 0) {
         int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     }
-    cudaError_t e = cudaMemsetAsync(a.work_counter, 0, 256, st);
-    if (e != cudaSuccess) return e;
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const int rows = C + (a.dm.conv_k > 0 ? a.dm.conv_k - 1 : 0);
+    CUtensorMap tmK, tmV;
+    if ((e = make_token_map(&tmK, a.tok.k, a.dm, a.tok.N, rows)) != cudaSuccess) return e;
+    if ((e = make_token_map(&tmV, a.tok.v, a.dm, a.tok.N, rows)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.status, 0, sizeof(int), st)) != cudaSuccess) return e;
     const int grid = n_items < g_num_sms ? n_items : g_num_sms;
     if (a.dm.conv_k == 0) {
-        e = cudaFuncSetAttribute(build_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
-        if (e != cudaSuccess) return e;
-        build_tc_kernel<0><<<grid, NT, SMEM_DYN, st>>>(a, tab);
+        if ((e = cudaFuncSetAttribute(build_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)))
+            return e;
+        build_tc_kernel<0><<<grid, NT, SMEM_DYN, st>>>(a, tab, tmK, tmV);
     } else {
-        e = cudaFuncSetAttribute(build_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
-        if (e != cudaSuccess) return e;
-        build_tc_kernel<4><<<grid, NT, SMEM_DYN, st>>>(a, tab);
+        if ((e = cudaFuncSetAttribute(build_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)))
+            return e;
+        build_tc_kernel<4><<<grid, NT, SMEM_DYN, st>>>(a, tab, tmK, tmV);
     }
     return cudaGetLastError();
 }

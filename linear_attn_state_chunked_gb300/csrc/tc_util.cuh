@@ -145,3 +145,56 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v)
 
 }  // namespace tc
 }  // namespace hypic
+
+namespace hypic {
+namespace tc {
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(mbar), "r"(bytes) : "memory");
+}
+
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 "selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// 4-D tiled TMA load global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+                 "[%0], [%1, {%2, %3, %4, %5}], [%6];"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+                    "r"(mbar)
+                 : "memory");
+}
+
+// Named barrier over `count` threads that also returns whether every
+// participating thread passed a true predicate.
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred)
+{
+    uint32_t out;
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\n"
+                 "bar.red.and.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(out) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+    return out != 0;
+}
+
+__device__ __forceinline__ void bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
+}  // namespace tc
+}  // namespace hypic
