@@ -172,6 +172,28 @@ int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok,
                         hypic_stream stream);
 
 /*
+ * Segment build without a caller-provided workspace (the HYPIC pages have no
+ * counterpart; this is a library convenience).  For callers that cannot
+ * allocate device memory -- e.g. a plugin inside a host inference engine that
+ * owns all device memory and hands its kernels only input and output buffers,
+ * or a latency-critical path where cudaMalloc's possible device
+ * synchronisation is not allowed.  Computes exactly what hypic_segment_build
+ * computes, with the same arguments minus the workspace.
+ *
+ * The scratch is a 256-byte block compiled into the library (a static device
+ * array that every GPU loading the library keeps until process exit); a
+ * request needing more scratch than that is rejected with
+ * HYPIC_ERR_WORKSPACE.  The first call on a device looks up the block's
+ * device address (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture.  All calls share the block and it
+ * keeps the last call's contents (the build clears what must start at zero):
+ * calls whose work overlaps on the GPU race on it.  Nothing is allocated.
+ */
+int hypic_segment_build_noalloc(const hypic_desc *desc, const hypic_tokens *tok,
+                                const int64_t *seg_off, int32_t n_seg,
+                                float *T_out, float *S_out, hypic_stream stream);
+
+/*
  * Compose: the running state of every (layer, head) over the request
  * order[0..n_order), starting from S_init (NULL = zero):
  *     for e in 0..n_order-1, s = order[e]:

@@ -135,6 +135,10 @@ int cuda_fail(cudaError_t e, const char *what)
 
 }  // namespace
 
+namespace hypic {
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+}  // namespace hypic
+
 extern "C" {
 
 int hypic_version(void) { return HYPIC_ABI_VERSION; }

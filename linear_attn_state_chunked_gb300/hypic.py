@@ -23,8 +23,8 @@ STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_INVALID_ARG", 2: "HYPIC_ERR_SHAPE", 3: "H
 
 # Every symbol include/hypic.h declares.
 EXPORTS = ("hypic_version", "hypic_last_error", "hypic_workspace_size",
-           "hypic_workspace_status", "hypic_segment_build", "hypic_compose",
-           "hypic_seam_advance")
+           "hypic_workspace_status", "hypic_segment_build", "hypic_segment_build_noalloc",
+           "hypic_compose", "hypic_seam_advance")
 
 
 class HypicError(RuntimeError):
@@ -67,6 +67,9 @@ def lib():
         L.hypic_segment_build.restype = ctypes.c_int
         L.hypic_segment_build.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p, i32,
                                           fp, fp, vp, ctypes.c_size_t, vp]
+        L.hypic_segment_build_noalloc.restype = ctypes.c_int
+        L.hypic_segment_build_noalloc.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p,
+                                                  i32, fp, fp, vp]
         L.hypic_compose.restype = ctypes.c_int
         L.hypic_compose.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p, i32,
                                     i32p, i32, fp, fp, fp, fp, fp, fp, vp]
@@ -158,6 +161,16 @@ def segment_build(desc, tok, seg_off, T_out, S_out, workspace, stream=None, n_to
     _check(lib().hypic_segment_build(ctypes.byref(d), ctypes.byref(t), offp, len(off) - 1,
                                      _p(T_out), _p(S_out), _p(workspace), ws_bytes,
                                      _stream(stream)))
+
+
+def segment_build_noalloc(desc, tok, seg_off, T_out, S_out, stream=None, n_tokens=None):
+    """segment_build for callers that cannot allocate device memory: uses the
+    library's own static scratch instead of a workspace (see include/hypic.h)."""
+    d = make_desc(desc)
+    t = make_tokens(tok, _tok_n(tok, n_tokens))
+    off, offp = _i64(seg_off)
+    _check(lib().hypic_segment_build_noalloc(ctypes.byref(d), ctypes.byref(t), offp, len(off) - 1,
+                                             _p(T_out), _p(S_out), _stream(stream)))
 
 
 def compose(desc, tok, seg_off, order, T, S, S_final, S_init=None, S_prefix_out=None,
