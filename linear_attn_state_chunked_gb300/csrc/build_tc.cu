@@ -76,9 +76,9 @@ constexpr uint32_t SM_MT = SM_UT + 32768;      // (D M)^T [64][64] tf32, sw128 (
 constexpr int LP = C + 1;
 constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][65]
 constexpr uint32_t SM_M = SM_L + C * LP * 4;   // (I + L)^-1 [64][65]
-constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // block products [3][16][17]
+constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // per-warp 16 x 8 block products (4 x 16 x 9 used)
 constexpr uint32_t SM_GATE = SM_Q + 3 * 16 * 17 * 4;  // 2 x Gates
-constexpr uint32_t SM_BAR = SM_GATE + 2 * 1024;
+constexpr uint32_t SM_BAR = SM_GATE + 2 * 1280;
 constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
@@ -91,6 +91,7 @@ struct Gates {
     float eg[C];  // exp(g_t)
     float dc[C];  // beta_j exp(g_C - g_j)
     float b[C];   // beta
+    float fb[C];  // beta_j exp(g_m - g_j), g_m = (g_0 + g_C) / 2
 };
 
 // mbarriers
@@ -150,7 +151,7 @@ __device__ __forceinline__ float bf16_at(const uint8_t *tile, int row, int col)
 __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
 {
     const long long t0 = clock64();
-    while (!tc::mbar_test(mbar, parity)) {
+    while (!tc::mbar_try(mbar, parity)) {
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitCycles) {
             *abort_flag = 1;
@@ -160,13 +161,51 @@ __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatil
     return true;
 }
 
+// Warp-level tf32 MMA, 16 x 8 x 8, accumulate into c.
+__device__ __forceinline__ void mma16x8x8(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
+{
+    const float h = tc::round_tf32(x);
+    hi = __float_as_uint(h);
+    lo = __float_as_uint(tc::round_tf32(x - h));
+}
+
+// c (16 x 8) += X[r0 .. r0+16)[k0 .. k0+8) * Y[k0y .. k0y+8)[c0 .. c0+8), with
+// each operand split into two tf32 terms (three products: fp32-level accuracy).
+__device__ __forceinline__ void mma3(float (&c)[4], const float *X, int ldx, int r0, int k0, const float *Y,
+                                     int ldy, int k0y, int c0, int lane)
+{
+    const int g = lane >> 2, t4 = lane & 3;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    split_tf32(X[(r0 + g) * ldx + k0 + t4], ah[0], al[0]);
+    split_tf32(X[(r0 + g + 8) * ldx + k0 + t4], ah[1], al[1]);
+    split_tf32(X[(r0 + g) * ldx + k0 + t4 + 4], ah[2], al[2]);
+    split_tf32(X[(r0 + g + 8) * ldx + k0 + t4 + 4], ah[3], al[3]);
+    split_tf32(Y[(k0y + t4) * ldy + c0 + g], bh[0], bl[0]);
+    split_tf32(Y[(k0y + t4 + 4) * ldy + c0 + g], bh[1], bl[1]);
+    mma16x8x8(c, al, bh);
+    mma16x8x8(c, ah, bl);
+    mma16x8x8(c, ah, bh);
+}
+
 // Blocked inverse of the unit lower triangular (I + L), 64 = 4 x 16 blocks,
-// by the 128 preparation threads (pt = 0..127): diagonal blocks by
-// substitution, then M_ij = -M_ii sum_{k=j}^{i-1} L_ik M_kj level by level.
+// by the 4 preparation warps.  Diagonal blocks by substitution (warp q solves
+// block q, one column per lane, every lane reading the same L element); then
+// level by level (i - j = 1, 2, 3) M_ij = -M_ii sum_{k=j}^{i-1} L_ik M_kj, each
+// warp taking (block, 8-column half) tasks whose 16 x 16 products run on the
+// warp-level tensor-core MMA.
 __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt)
 {
-    if (pt < 64) {
-        const int b = pt >> 4, cc = pt & 15, base = 16 * b;
+    const int wq = pt >> 5, ln = pt & 31;
+    if (ln < 16) {
+        const int base = 16 * wq, cc = ln;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -185,28 +224,31 @@ __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt
         Ms[(16 * bi + r) * LP + 16 * bj + cc] = 0.f;
     }
     tc::bar_sync(BAR_PREP, 128);
+    float *Qw = Qs + wq * 16 * 9;  // this warp's 16 x 8 product, padded rows
+    const int g = ln >> 2, t4 = ln & 3;
     for (int delta = 1; delta <= 3; ++delta) {
-        const int nblk = 4 - delta;
-        for (int e = pt; e < nblk * 256; e += 128) {
-            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int bj = blk, bi = blk + delta;
-            float acc = 0.f;
-            for (int bk = bj; bk < bi; ++bk) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    acc = fmaf(Ls[(16 * bi + r) * LP + 16 * bk + q], Ms[(16 * bk + q) * LP + 16 * bj + cc], acc);
+        const int ntask = 2 * (4 - delta);
+        for (int task = wq; task < ntask; task += 4) {
+            const int bj = task >> 1, nh = task & 1, bi = bj + delta;
+            float q[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int ks = 0; ks < 2 * delta; ++ks) {
+                const int kc = 16 * bj + 8 * ks;
+                mma3(q, Ls, LP, 16 * bi, kc, Ms, LP, kc, 16 * bj + 8 * nh, ln);
             }
-            Qs[(blk * 16 + r) * 17 + cc] = acc;
-        }
-        tc::bar_sync(BAR_PREP, 128);
-        for (int e = pt; e < nblk * 256; e += 128) {
-            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int bj = blk, bi = blk + delta;
-            float acc = 0.f;
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                acc = fmaf(Ms[(16 * bi + r) * LP + 16 * bi + q], Qs[(blk * 16 + q) * 17 + cc], acc);
-            Ms[(16 * bi + r) * LP + 16 * bj + cc] = -acc;
+            Qw[g * 9 + 2 * t4] = q[0];
+            Qw[g * 9 + 2 * t4 + 1] = q[1];
+            Qw[(g + 8) * 9 + 2 * t4] = q[2];
+            Qw[(g + 8) * 9 + 2 * t4 + 1] = q[3];
+            __syncwarp();
+            float r[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3(r, Ms, LP, 16 * bi, 16 * bi, Qw, 9, 0, 0, ln);
+            mma3(r, Ms, LP, 16 * bi, 16 * bi + 8, Qw, 9, 8, 0, ln);
+            const int col = 16 * bj + 8 * nh + 2 * t4;
+            Ms[(16 * bi + g) * LP + col] = -r[0];
+            Ms[(16 * bi + g) * LP + col + 1] = -r[1];
+            Ms[(16 * bi + g + 8) * LP + col] = -r[2];
+            Ms[(16 * bi + g + 8) * LP + col + 1] = -r[3];
+            __syncwarp();
         }
         tc::bar_sync(BAR_PREP, 128);
     }
@@ -332,97 +374,78 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         }
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
+        // Per chunk n: Gram(n), Pt(n) (both halves), U~(n), Xt_T update,
+        // Xt_S update -- each as soon as its inputs are ready, waiting with
+        // hardware-suspended bounded waits.  Chunk n+1's preparation runs on
+        // the CUDA cores while Pt(n) .. Xt_S(n) run on the tensor core.
         if (lane == 0) {
-            Cursor pc{static_cast<int>(blockIdx.x), 0, 0, 0, 0};
-            cursor_seek(pc, n_items, dm, tab);
-            Cursor mc = pc;
-            int pstep = 0, mstep = 0;
-            long long idle_since = clock64();
-            while ((pc.item < n_items || mc.item < n_items) && !*abort_flag) {
-                bool progressed = false;
-                if (pc.item < n_items) {
-                    if (pstep == 0 && tc::mbar_test(bar(B_KREADY), pc.n & 1)) {
-                        tc::fence_after();
+            Cursor mc{static_cast<int>(blockIdx.x), 0, 0, 0, 0};
+            cursor_seek(mc, n_items, dm, tab);
+            while (mc.item < n_items) {
+                const uint32_t par = mc.n & 1;
+                if (!wait_bar(bar(B_KREADY), par, abort_flag)) break;
+                tc::fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < D / 8; ++ks)
-                            tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks),
-                                       tc::idesc_tf32(64, 64), ks > 0);
-                        tc::commit(bar(B_GRAM));
-                        pstep = 1;
-                        progressed = true;
-                    } else if (pstep == 1 && tc::mbar_test(bar(B_KTREADY), pc.n & 1)) {
-                        tc::fence_after();
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks),
+                               tc::idesc_tf32(64, 64), ks > 0);
+                tc::commit(bar(B_GRAM));
+                if (mc.c == 0 && !wait_bar(bar(B_XREADY), mc.xi & 1, abort_flag)) break;
+                tc::fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < C / 8; ++ks)
-                            tc::mma_ts(tb + TM_U, tb + TM_G + ks * 8, tc::sdesc_kstep(sMT, C, ks),
-                                       tc::idesc_tf32(128, 64), ks > 0);
-                        tc::commit(bar(B_UDONE));
-                        pstep = 0;
-                        cursor_next(pc, n_items, dm, tab);
-                        progressed = true;
-                    }
-                }
-                if (mc.item < n_items) {
-                    // Gram(n) issued <=> the prep cursor passed step 0 of chunk n
-                    const bool gram_issued = pc.n > mc.n || (pc.n == mc.n && pstep == 1);
-                    const bool u_issued = pc.n > mc.n;
-                    if (mstep == 0 && gram_issued &&
-                        (mc.c != 0 || tc::mbar_test(bar(B_XREADY), mc.xi & 1))) {
-                        tc::fence_after();
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK32, C, ks),
+                               tc::idesc_tf32(128, 64), ks > 0);
+                tc::commit(bar(B_PTDONE));
 #pragma unroll
-                        for (int ks = 0; ks < D / 8; ++ks)
-                            tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK32, C, ks),
-                                       tc::idesc_tf32(128, 64), ks > 0);
-                        tc::commit(bar(B_PTDONE));
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks),
+                               tc::idesc_tf32(128, 64), ks > 0);
+                tc::commit(bar(B_PSDONE));
+                if (!wait_bar(bar(B_KTREADY), par, abort_flag)) break;
+                tc::fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < D / 8; ++ks)
-                            tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks),
-                                       tc::idesc_tf32(128, 64), ks > 0);
-                        tc::commit(bar(B_PSDONE));
-                        mstep = 1;
-                        progressed = true;
-                    } else if (mstep == 1 && u_issued && tc::mbar_test(bar(B_UTREADY), mc.n & 1) &&
-                               tc::mbar_test(bar(B_RTREADY), mc.n & 1)) {
-                        tc::fence_after();
+                for (int ks = 0; ks < C / 8; ++ks)
+                    tc::mma_ts(tb + TM_U, tb + TM_G + ks * 8, tc::sdesc_kstep(sMT, C, ks),
+                               tc::idesc_tf32(128, 64), ks > 0);
+                tc::commit(bar(B_UDONE));
+                if (!wait_bar(bar(B_UTREADY), par, abort_flag)) break;
+                if (!wait_bar(bar(B_RTREADY), par, abort_flag)) break;
+                tc::fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < C / 8; ++ks)
-                            tc::mma_ts(tb + TM_XT, tb + TM_PT + ks * 8, tc::sdesc_kstep(sUT, D, ks),
-                                       tc::idesc_tf32(128, 128), 1);
-                        mstep = 2;
-                        progressed = true;
-                    } else if (mstep == 2 && tc::mbar_test(bar(B_RSREADY), mc.n & 1)) {
-                        tc::fence_after();
+                for (int ks = 0; ks < C / 8; ++ks)
+                    tc::mma_ts(tb + TM_XT, tb + TM_PT + ks * 8, tc::sdesc_kstep(sUT, D, ks),
+                               tc::idesc_tf32(128, 128), 1);
+                if (!wait_bar(bar(B_RSREADY), par, abort_flag)) break;
+                tc::fence_after();
 #pragma unroll
-                        for (int ks = 0; ks < C / 8; ++ks)
-                            tc::mma_ts(tb + TM_XS, tb + TM_PS + ks * 8, tc::sdesc_kstep(sUT, D, ks),
-                                       tc::idesc_tf32(128, 128), 1);
-                        tc::commit(bar(B_DSDONE));
-                        mstep = 0;
-                        cursor_next(mc, n_items, dm, tab);
-                        progressed = true;
-                    }
-                }
-                if (progressed) {
-                    idle_since = clock64();
-                } else {
-                    if (clock64() - idle_since > kWaitCycles) *abort_flag = 1;
-                    __nanosleep(32);
-                }
+                for (int ks = 0; ks < C / 8; ++ks)
+                    tc::mma_ts(tb + TM_XS, tb + TM_PS + ks * 8, tc::sdesc_kstep(sUT, D, ks),
+                               tc::idesc_tf32(128, 128), 1);
+                tc::commit(bar(B_DSDONE));
+                cursor_next(mc, n_items, dm, tab);
             }
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ preparation
         const int pt = tid - 128;
-        const float *wk = nullptr;
+        const int c0 = (pt & 15) * 8;  // the 8 channels this thread converts
+        float wkr[8][CK > 0 ? CK : 1];
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
             const Item it = decode_item(itx, dm, tab);
-            if (CK > 0) wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
+            if (CK > 0 && it.nch > 0) {
+                const float *wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < (CK > 0 ? CK : 1); ++j) wkr[i][j] = __ldg(wk + (c0 + i) * CK + j);
+            }
             for (int c = 0; c < it.nch; ++c, ++n) {
                 const int s = n % RS;
                 const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (n & 1) * 1024);
+                Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (n & 1) * 1280);
                 const int nc = min(C, (int)(it.n - c * C));
                 bool w = true;
                 if (pt == 0) {
@@ -452,12 +475,14 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     G.b[2 * lane + 1] = B[2 * lane + 1];
                     G.dc[2 * lane] = B[2 * lane] * expf(total - g0);
                     G.dc[2 * lane + 1] = B[2 * lane + 1] * expf(total - g1);
+                    const float gm = 0.5f * (__shfl_sync(0xffffffffu, x0, 0) + total);
+                    G.fb[2 * lane] = B[2 * lane] * __expf(fmaxf(gm - g0, -87.f));
+                    G.fb[2 * lane + 1] = B[2 * lane + 1] * __expf(fmaxf(gm - g1, -87.f));
                 }
                 // K -> tf32 (conv + L2 normalisation first when present)
 #pragma unroll 2
                 for (int iter = 0; iter < (C * D / 8) / 128; ++iter) {
                     const int t = iter * 8 + (pt >> 4);
-                    const int c0 = (pt & 15) * 8;
                     float kx[8];
                     if (t < nc) {
                         if (CK == 0) {
@@ -471,7 +496,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                                 unpack8(*reinterpret_cast<const uint4 *>(stg + ST_K + ((t + HIST - j) * D + c0) * 2),
                                         rk);
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) kx[i] = fmaf(__ldg(wk + (c0 + i) * CK + j), rk[i], kx[i]);
+                                for (int i = 0; i < 8; ++i) kx[i] = fmaf(wkr[i][j], rk[i], kx[i]);
                             }
                         }
                     } else {
@@ -506,15 +531,31 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 if (!tc::bar_and(BAR_PREP, 128, w)) { ok = false; break; }
                 tc::fence_after();
                 {
-                    float gr[64];
+                    // Gram row t sits in lane 16q + ... of warp q (lanes 0-15); lanes 16-31
+                    // take the row's upper 32 columns from their partner lane.
+                    float gr[32], up[32];
                     tc::tmem_ld32(my + TM_G, gr);
-                    tc::tmem_ld32(my + TM_G + 32, gr + 32);
-                    if (lane < 16) {
-                        const int t = 16 * (warp & 3) + lane;
-                        const float gt_t = G.g[t];
+                    tc::tmem_ld32(my + TM_G + 32, up);
 #pragma unroll
-                        for (int j = 0; j < C; ++j)
-                            Ls[t * LP + j] = (j < t) ? G.b[j] * expf(gt_t - G.g[j]) * gr[j] : 0.f;
+                    for (int j = 0; j < 32; ++j) {
+                        const float o = __shfl_up_sync(0xffffffffu, up[j], 16);
+                        if (lane >= 16) gr[j] = o;
+                    }
+                    const int t = 16 * (warp & 3) + (lane & 15);
+                    const int j0 = (lane >= 16) ? 32 : 0;
+                    const float gt_t = G.g[t];
+                    if (G.g[0] - G.g[C - 1] < 80.f) {
+                        // exp(g_t - g_j) = exp(g_t - g_m) exp(g_m - g_j), g_m the chunk midpoint:
+                        // both factors stay within e^{+-40}, one exp per row
+                        const float gm = 0.5f * (G.g[0] + G.g[C - 1]);
+                        const float et = __expf(gt_t - gm);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            Ls[t * LP + j0 + j] = (j0 + j < t) ? G.fb[j0 + j] * et * gr[j] : 0.f;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            Ls[t * LP + j0 + j] = (j0 + j < t) ? G.b[j0 + j] * __expf(gt_t - G.g[j0 + j]) * gr[j] : 0.f;
                     }
                 }
                 tc::bar_sync(BAR_PREP, 128);
@@ -531,10 +572,14 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     }
                 }
                 // B of U~: element (t, j) = dc_j M[j][t]
-                for (int e = pt; e < C * C; e += 128) {
-                    const int t = e >> 6, j = e & 63;
-                    *reinterpret_cast<float *>(sm + SM_MT + tc::sw128_f32(t, j, C)) =
-                        tc::round_tf32(G.dc[j] * Ms[j * LP + t]);
+#pragma unroll 2
+                for (int e = pt; e < C * C / 4; e += 128) {
+                    const int t = e >> 4, j = (e & 15) * 4;
+                    *reinterpret_cast<float4 *>(sm + SM_MT + tc::sw128_f32(t, j, C)) =
+                        make_float4(tc::round_tf32(G.dc[j] * Ms[j * LP + t]),
+                                    tc::round_tf32(G.dc[j + 1] * Ms[(j + 1) * LP + t]),
+                                    tc::round_tf32(G.dc[j + 2] * Ms[(j + 2) * LP + t]),
+                                    tc::round_tf32(G.dc[j + 3] * Ms[(j + 3) * LP + t]));
                 }
                 tc::fence_async_smem();
                 tc::fence_before();
@@ -568,7 +613,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
     } else {
         // ------------------------------------------------------------ epilogue (warps 0-3)
         const int m = tid;  // row of Xt / Pt in each half = tensor-memory lane
-        const float *wv = nullptr;
+        float wvr[CK > 0 ? CK : 1];
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
@@ -583,7 +628,11 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 }
                 continue;
             }
-            if (CK > 0) wv = a.tok.conv_w + (((size_t)it.l * 3 + 2) * dm.H + it.h) * D * CK;
+            if (CK > 0) {
+                const float *wv = a.tok.conv_w + (((size_t)it.l * 3 + 2) * dm.H + it.h) * D * CK;
+#pragma unroll
+                for (int j = 0; j < (CK > 0 ? CK : 1); ++j) wvr[j] = __ldg(wv + m * CK + j);
+            }
             // Xt = [I | 0]^T
             {
                 float v[32];
@@ -604,7 +653,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
             for (int c = 0; c < it.nch; ++c, ++n) {
                 const int s = n % RS;
                 const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (n & 1) * 1024);
+                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (n & 1) * 1280);
                 const int nc = min(C, (int)(it.n - c * C));
                 // ---- T half
                 bool w = true;
@@ -641,23 +690,28 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 tc::fence_after();
                 {
                     float p[32];
+                    // raw V history window for the conv: win[j] = row t + HIST - j
+                    float win[HMAX + 1];
+#pragma unroll
+                    for (int j = 1; j <= HMAX; ++j) win[j] = (j <= HIST) ? bf16_at(stg + ST_V, HIST - j, m) : 0.f;
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         tc::tmem_ld32(my + TM_PS + h2 * 32, p);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int t = h2 * 32 + i;
+                            win[0] = bf16_at(stg + ST_V, t + HIST, m);
                             float vv = 0.f;
-                            if (t < nc) {
-                                if (CK == 0) {
-                                    vv = bf16_at(stg + ST_V, t, m);
-                                } else {
+                            if (CK == 0) {
+                                vv = win[0];
+                            } else {
 #pragma unroll
-                                    for (int j = 0; j < CK; ++j)
-                                        vv = fmaf(__ldg(wv + m * CK + j), bf16_at(stg + ST_V, t + HIST - j, m), vv);
-                                }
+                                for (int j = 0; j < (CK > 0 ? CK : 1); ++j) vv = fmaf(wvr[j], win[j], vv);
                             }
+                            if (t >= nc) vv = 0.f;
                             p[i] = tc::round_tf32(fmaf(-G.eg[t], p[i], vv));
+#pragma unroll
+                            for (int j = HMAX; j > 0; --j) win[j] = win[j - 1];
                         }
                         tc::tmem_st32(my + TM_PS + h2 * 32, p);
                     }
