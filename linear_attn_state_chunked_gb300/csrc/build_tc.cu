@@ -38,6 +38,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_util.cuh"
+#include "tmap.h"
 
 namespace hypic {
 namespace {
@@ -759,18 +760,14 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
 }
 
 int g_num_sms = 0;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 cudaError_t make_token_map(CUtensorMap *map, const void *base, const Dims &dm, int32_t N, int rows)
 {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)dm.H, (cuuint64_t)N, (cuuint64_t)dm.L};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)dm.H * D * 2, (cuuint64_t)N * dm.H * D * 2};
     const cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)rows, 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace
@@ -790,14 +787,6 @@ cudaError_t launch_build_tc(const BuildArgs &a, const SegTable &tab, cudaStream_
         int dev = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    }
-    if (!g_encode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     const int rows = C + (a.dm.conv_k > 0 ? a.dm.conv_k - 1 : 0);
     CUtensorMap tmK, tmV;

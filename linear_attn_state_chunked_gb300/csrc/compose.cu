@@ -353,6 +353,10 @@ HYPIC_DISPATCH(launch_seam, SeamArgs)
 
 cudaError_t launch_compose(const ComposeArgs &a, const SegTable &tab, cudaStream_t st)
 {
+    // Gated delta at d = 128 with bf16 inputs composes on the tensor cores
+    // (tf32 T_C S, 2e-3 class); fp32-input requests (1e-5 class) and the other
+    // modes and widths use the CUDA-core kernel below.
+    if (compose_tc_supported(a.dm)) return launch_compose_tc(a, tab, st);
     return a.dm.dtype == HYPIC_BF16 ? launch_compose_m<__nv_bfloat16>(a, tab, st)
                                     : launch_compose_m<float>(a, tab, st);
 }

@@ -38,6 +38,8 @@ cudaError_t launch_build_rec(const BuildArgs &a, const SegTable &tab, cudaStream
 bool build_tc_supported(const Dims &dm);
 cudaError_t launch_build_tc(const BuildArgs &a, const SegTable &tab, cudaStream_t st);
 cudaError_t launch_compose(const ComposeArgs &a, const SegTable &tab, cudaStream_t st);
+bool compose_tc_supported(const Dims &dm);
+cudaError_t launch_compose_tc(const ComposeArgs &a, const SegTable &tab, cudaStream_t st);
 cudaError_t launch_seam(const SeamArgs &a, const SegTable &tab, cudaStream_t st);
 
 }  // namespace hypic

@@ -192,6 +192,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
                  : "memory");
 }
 
+// 2-D tiled TMA load global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+                 "[%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(mbar)
+                 : "memory");
+}
+
 // Named barrier over `count` threads that also returns whether every
 // participating thread passed a true predicate.
 __device__ __forceinline__ bool bar_and(int id, int count, bool pred)
