@@ -20,13 +20,13 @@
 // truncates).
 //
 // Warp roles (one CTA per SM, persistent over work items):
-//   warp 9      TMA producer: raw bf16 K/V rows (+ conv history) and gates of
+//   warp 13     TMA producer: raw bf16 K/V rows (+ conv history) and gates of
 //               each chunk into a 3-stage ring;
-//   warp 8      one thread issues every tcgen05.mma, interleaving the chunk
-//               pipeline (Pt, Xt updates) with the next chunk's preparation
-//               (Gram, U~) as their inputs become ready;
-//   warps 4-7   preparation of chunk n+1 while chunk n runs: gates, conv +
-//               normalisation, tf32 K, L, the inverse, U~;
+//   warp 12     one thread issues every tcgen05.mma: chunk n's Gram, Pt, U~
+//               and Xt updates, each as soon as its inputs are ready;
+//   warps 4-11  preparation of chunk n+1 while chunk n runs (two warps per
+//               tensor-memory lane quadrant): gates, conv + normalisation,
+//               tf32 K, L, the inverse, U~;
 //   warps 0-3   epilogue of chunk n: Rt and the Gamma_C rescale of Xt, both
 //               halves, and the emission of each finished pair.
 // Work items (segment body, layer, head) arrive longest body first; CTA b
@@ -48,8 +48,9 @@ constexpr int C = 64;    // chunk length
 constexpr int RS = 3;    // raw-input ring stages
 constexpr int HMAX = 3;  // conv history rows kept per chunk (conv_k <= 4)
 constexpr int ROWS = C + HMAX;
-constexpr int NT = 320;  // 10 warps
-constexpr int WARP_MMA = 8, WARP_TMA = 9;
+constexpr int NP = 256;  // preparation threads (warps 4-11, two per tensor-memory lane quadrant)
+constexpr int NT = 448;  // 14 warps
+constexpr int WARP_MMA = 12, WARP_TMA = 13;
 constexpr int BAR_EPI = 1, BAR_PREP = 2;
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds
 
@@ -77,8 +78,8 @@ constexpr uint32_t SM_MT = SM_UT + 32768;      // (D M)^T [64][64] tf32, sw128 (
 constexpr int LP = C + 1;
 constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][65]
 constexpr uint32_t SM_M = SM_L + C * LP * 4;   // (I + L)^-1 [64][65]
-constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // per-warp 16 x 8 block products (4 x 16 x 9 used)
-constexpr uint32_t SM_GATE = SM_Q + 3 * 16 * 17 * 4;  // 2 x Gates
+constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // per-warp 16 x 8 block products [8][16][9]
+constexpr uint32_t SM_GATE = SM_Q + 8 * 16 * 9 * 4;  // 2 x Gates
 constexpr uint32_t SM_BAR = SM_GATE + 2 * 1280;
 constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
@@ -197,7 +198,7 @@ __device__ __forceinline__ void mma3(float (&c)[4], const float *X, int ldx, int
 }
 
 // Blocked inverse of the unit lower triangular (I + L), 64 = 4 x 16 blocks,
-// by the 4 preparation warps.  Diagonal blocks by substitution (warp q solves
+// by the 8 preparation warps (pt = 0 .. NP-1).  Diagonal blocks by substitution (warp q solves
 // block q, one column per lane, every lane reading the same L element); then
 // level by level (i - j = 1, 2, 3) M_ij = -M_ii sum_{k=j}^{i-1} L_ik M_kj, each
 // warp taking (block, 8-column half) tasks whose 16 x 16 products run on the
@@ -205,7 +206,7 @@ __device__ __forceinline__ void mma3(float (&c)[4], const float *X, int ldx, int
 __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt)
 {
     const int wq = pt >> 5, ln = pt & 31;
-    if (ln < 16) {
+    if (wq < 4 && ln < 16) {
         const int base = 16 * wq, cc = ln;
         float x[16];
 #pragma unroll
@@ -218,18 +219,18 @@ __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt
 #pragma unroll
         for (int r = 0; r < 16; ++r) Ms[(base + r) * LP + base + cc] = x[r];
     }
-    for (int e = pt; e < 6 * 256; e += 128) {
+    for (int e = pt; e < 6 * 256; e += NP) {
         const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
         const int bi = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
         const int bj = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
         Ms[(16 * bi + r) * LP + 16 * bj + cc] = 0.f;
     }
-    tc::bar_sync(BAR_PREP, 128);
+    tc::bar_sync(BAR_PREP, NP);
     float *Qw = Qs + wq * 16 * 9;  // this warp's 16 x 8 product, padded rows
     const int g = ln >> 2, t4 = ln & 3;
     for (int delta = 1; delta <= 3; ++delta) {
         const int ntask = 2 * (4 - delta);
-        for (int task = wq; task < ntask; task += 4) {
+        for (int task = wq; task < ntask; task += NP / 32) {
             const int bj = task >> 1, nh = task & 1, bi = bj + delta;
             float q[4] = {0.f, 0.f, 0.f, 0.f};
             for (int ks = 0; ks < 2 * delta; ++ks) {
@@ -251,7 +252,7 @@ __device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt
             Ms[(16 * bi + g + 8) * LP + col + 1] = -r[3];
             __syncwarp();
         }
-        tc::bar_sync(BAR_PREP, 128);
+        tc::bar_sync(BAR_PREP, NP);
     }
 }
 
@@ -429,7 +430,9 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ preparation
-        const int pt = tid - 128;
+        const int pt = tid - 128;      // 0 .. NP-1
+        const int li = pt & 127;       // tensor-memory lane of this thread
+        const int hh = pt >> 7;        // which half of a 64-column operand this warp handles
         const int c0 = (pt & 15) * 8;  // the 8 channels this thread converts
         float wkr[8][CK > 0 ? CK : 1];
         int n = 0;
@@ -453,7 +456,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     w = wait_bar(bar(B_FULL + s), (n / RS) & 1, abort_flag);
                     if (w && n > 0) w = wait_bar(bar(B_PSDONE), (n - 1) & 1, abort_flag);  // K32 free
                 }
-                if (!tc::bar_and(BAR_PREP, 128, w)) { ok = false; break; }
+                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
                 // gates (one warp, two tokens per lane)
                 if (warp == 4) {
                     const float *A = reinterpret_cast<const float *>(stg + ST_A);
@@ -482,8 +485,8 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 }
                 // K -> tf32 (conv + L2 normalisation first when present)
 #pragma unroll 2
-                for (int iter = 0; iter < (C * D / 8) / 128; ++iter) {
-                    const int t = iter * 8 + (pt >> 4);
+                for (int iter = 0; iter < (C * D / 8) / NP; ++iter) {
+                    const int t = iter * (NP / 16) + (pt >> 4);
                     float kx[8];
                     if (t < nc) {
                         if (CK == 0) {
@@ -522,28 +525,28 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                                     tc::round_tf32(kx[7]));
                 }
                 tc::fence_async_smem();
-                tc::bar_sync(BAR_PREP, 128);
+                tc::bar_sync(BAR_PREP, NP);
                 if (pt == 0) {
                     tc::mbar_arrive(bar(B_KREADY));
                     tc::mbar_arrive(bar(B_EMPTY + s));  // K rows and gates consumed
                 }
                 // L from the Gram rows (M = 64 layout: row 16q + i in lane 32q + i)
                 if (pt == 0) w = wait_bar(bar(B_GRAM), n & 1, abort_flag);
-                if (!tc::bar_and(BAR_PREP, 128, w)) { ok = false; break; }
+                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
                 tc::fence_after();
                 {
-                    // Gram row t sits in lane 16q + ... of warp q (lanes 0-15); lanes 16-31
-                    // take the row's upper 32 columns from their partner lane.
-                    float gr[32], up[32];
-                    tc::tmem_ld32(my + TM_G, gr);
-                    tc::tmem_ld32(my + TM_G + 32, up);
+                    // Gram row 16q + i sits in lane 32q + i (i < 16) of quadrant q; this
+                    // warp takes columns 32hh .. 32hh+31 of its 16 rows, lanes 16-31
+                    // the upper 16 of those (shuffled from their partner lane).
+                    float gr[32];
+                    tc::tmem_ld32(my + TM_G + hh * 32, gr);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float o = __shfl_up_sync(0xffffffffu, up[j], 16);
+                    for (int j = 0; j < 16; ++j) {
+                        const float o = __shfl_up_sync(0xffffffffu, gr[16 + j], 16);
                         if (lane >= 16) gr[j] = o;
                     }
                     const int t = 16 * (warp & 3) + (lane & 15);
-                    const int j0 = (lane >= 16) ? 32 : 0;
+                    const int j0 = hh * 32 + ((lane >= 16) ? 16 : 0);
                     const float gt_t = G.g[t];
                     if (G.g[0] - G.g[C - 1] < 80.f) {
                         // exp(g_t - g_j) = exp(g_t - g_m) exp(g_m - g_j), g_m the chunk midpoint:
@@ -551,30 +554,27 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         const float gm = 0.5f * (G.g[0] + G.g[C - 1]);
                         const float et = __expf(gt_t - gm);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
+                        for (int j = 0; j < 16; ++j)
                             Ls[t * LP + j0 + j] = (j0 + j < t) ? G.fb[j0 + j] * et * gr[j] : 0.f;
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
+                        for (int j = 0; j < 16; ++j)
                             Ls[t * LP + j0 + j] = (j0 + j < t) ? G.b[j0 + j] * __expf(gt_t - G.g[j0 + j]) * gr[j] : 0.f;
                     }
                 }
-                tc::bar_sync(BAR_PREP, 128);
+                tc::bar_sync(BAR_PREP, NP);
                 unit_lower_inverse(Ls, Ms, Qs, pt);
-                // K^T into tensor memory (A of U~): lane i holds K[j][i], j = 0..63
+                // K^T into tensor memory (A of U~): lane i holds K[j][i], this warp j = 32hh .. +31
                 {
                     float kt[32];
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            kt[j] = *reinterpret_cast<const float *>(sm + SM_K32 + tc::sw128_f32(h2 * 32 + j, pt, C));
-                        tc::tmem_st32(my + TM_G + h2 * 32, kt);
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        kt[j] = *reinterpret_cast<const float *>(sm + SM_K32 + tc::sw128_f32(hh * 32 + j, li, C));
+                    tc::tmem_st32(my + TM_G + hh * 32, kt);
                 }
                 // B of U~: element (t, j) = dc_j M[j][t]
 #pragma unroll 2
-                for (int e = pt; e < C * C / 4; e += 128) {
+                for (int e = pt; e < C * C / 4; e += NP) {
                     const int t = e >> 4, j = (e & 15) * 4;
                     *reinterpret_cast<float4 *>(sm + SM_MT + tc::sw128_f32(t, j, C)) =
                         make_float4(tc::round_tf32(G.dc[j] * Ms[j * LP + t]),
@@ -584,30 +584,27 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 }
                 tc::fence_async_smem();
                 tc::fence_before();
-                tc::bar_sync(BAR_PREP, 128);
+                tc::bar_sync(BAR_PREP, NP);
                 if (pt == 0) tc::mbar_arrive(bar(B_KTREADY));
                 // U~^T rows into shared memory once the previous chunk's Xt update is done
                 if (pt == 0) {
                     w = wait_bar(bar(B_UDONE), n & 1, abort_flag);
                     if (w && n > 0) w = wait_bar(bar(B_DSDONE), (n - 1) & 1, abort_flag);
                 }
-                if (!tc::bar_and(BAR_PREP, 128, w)) { ok = false; break; }
+                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
                 tc::fence_after();
                 {
                     float u[32];
+                    tc::tmem_ld32(my + TM_U + hh * 32, u);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        tc::tmem_ld32(my + TM_U + h2 * 32, u);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(sm + SM_UT + tc::sw128_f32(pt, h2 * 32 + i, D)) =
-                                make_float4(tc::round_tf32(u[i]), tc::round_tf32(u[i + 1]),
-                                            tc::round_tf32(u[i + 2]), tc::round_tf32(u[i + 3]));
-                    }
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(sm + SM_UT + tc::sw128_f32(li, hh * 32 + i, D)) =
+                            make_float4(tc::round_tf32(u[i]), tc::round_tf32(u[i + 1]), tc::round_tf32(u[i + 2]),
+                                        tc::round_tf32(u[i + 3]));
                 }
                 tc::fence_async_smem();
                 tc::fence_before();
-                tc::bar_sync(BAR_PREP, 128);
+                tc::bar_sync(BAR_PREP, NP);
                 if (pt == 0) tc::mbar_arrive(bar(B_UTREADY));
             }
         }
