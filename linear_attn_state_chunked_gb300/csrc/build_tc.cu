@@ -78,9 +78,9 @@ constexpr uint32_t SM_MT = SM_UT + 32768;      // (D M)^T [64][64] tf32, sw128 (
 constexpr int LP = C + 1;
 constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][65]
 constexpr uint32_t SM_M = SM_L + C * LP * 4;   // (I + L)^-1 [64][65]
-constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // per-warp 16 x 8 block products [8][16][9]
-constexpr uint32_t SM_GATE = SM_Q + 8 * 16 * 9 * 4;  // 2 x Gates
-constexpr uint32_t SM_BAR = SM_GATE + 2 * 1280;
+constexpr uint32_t SM_GATE = SM_M + C * LP * 4;  // 3 x Gates (chunk n uses buffer n % 3)
+constexpr uint32_t SM_WK = SM_GATE + 3 * 1280;  // K conv weights of the current item [4 lags][128]
+constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
@@ -172,88 +172,121 @@ __device__ __forceinline__ void mma16x8x8(float (&c)[4], const uint32_t (&a)[4],
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
-{
-    const float h = tc::round_tf32(x);
-    hi = __float_as_uint(h);
-    lo = __float_as_uint(tc::round_tf32(x - h));
-}
-
-// c (16 x 8) += X[r0 .. r0+16)[k0 .. k0+8) * Y[k0y .. k0y+8)[c0 .. c0+8), with
-// each operand split into two tf32 terms (three products: fp32-level accuracy).
-__device__ __forceinline__ void mma3(float (&c)[4], const float *X, int ldx, int r0, int k0, const float *Y,
+// c (16 x 8) += X[r0 .. r0+16)[k0 .. k0+8) * Y[k0y .. k0y+8)[c0 .. c0+8), operands
+// rounded to tf32.
+__device__ __forceinline__ void mma1(float (&c)[4], const float *X, int ldx, int r0, int k0, const float *Y,
                                      int ldy, int k0y, int c0, int lane)
 {
     const int g = lane >> 2, t4 = lane & 3;
-    uint32_t ah[4], al[4], bh[2], bl[2];
-    split_tf32(X[(r0 + g) * ldx + k0 + t4], ah[0], al[0]);
-    split_tf32(X[(r0 + g + 8) * ldx + k0 + t4], ah[1], al[1]);
-    split_tf32(X[(r0 + g) * ldx + k0 + t4 + 4], ah[2], al[2]);
-    split_tf32(X[(r0 + g + 8) * ldx + k0 + t4 + 4], ah[3], al[3]);
-    split_tf32(Y[(k0y + t4) * ldy + c0 + g], bh[0], bl[0]);
-    split_tf32(Y[(k0y + t4 + 4) * ldy + c0 + g], bh[1], bl[1]);
-    mma16x8x8(c, al, bh);
-    mma16x8x8(c, ah, bl);
-    mma16x8x8(c, ah, bh);
+    uint32_t a[4], b[2];
+    a[0] = __float_as_uint(tc::round_tf32(X[(r0 + g) * ldx + k0 + t4]));
+    a[1] = __float_as_uint(tc::round_tf32(X[(r0 + g + 8) * ldx + k0 + t4]));
+    a[2] = __float_as_uint(tc::round_tf32(X[(r0 + g) * ldx + k0 + t4 + 4]));
+    a[3] = __float_as_uint(tc::round_tf32(X[(r0 + g + 8) * ldx + k0 + t4 + 4]));
+    b[0] = __float_as_uint(tc::round_tf32(Y[(k0y + t4) * ldy + c0 + g]));
+    b[1] = __float_as_uint(tc::round_tf32(Y[(k0y + t4 + 4) * ldy + c0 + g]));
+    mma16x8x8(c, a, b);
 }
 
-// Blocked inverse of the unit lower triangular (I + L), 64 = 4 x 16 blocks,
-// by the 8 preparation warps (pt = 0 .. NP-1).  Diagonal blocks by substitution (warp q solves
-// block q, one column per lane, every lane reading the same L element); then
-// level by level (i - j = 1, 2, 3) M_ij = -M_ii sum_{k=j}^{i-1} L_ik M_kj, each
-// warp taking (block, 8-column half) tasks whose 16 x 16 products run on the
-// warp-level tensor-core MMA.
-__device__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt)
+// Store a 16 x 8 accumulator fragment (times s) at rows r0.., columns c0.. of Y.
+__device__ __forceinline__ void store_frag(float *Y, int ldy, int r0, int c0, const float (&c)[4], float s,
+                                           int lane)
+{
+    const int g = lane >> 2, t4 = lane & 3;
+    Y[(r0 + g) * ldy + c0 + 2 * t4] = s * c[0];
+    Y[(r0 + g) * ldy + c0 + 2 * t4 + 1] = s * c[1];
+    Y[(r0 + g + 8) * ldy + c0 + 2 * t4] = s * c[2];
+    Y[(r0 + g + 8) * ldy + c0 + 2 * t4 + 1] = s * c[3];
+}
+
+// M = (I + L)^{-1} for the unit lower triangular 64 x 64 matrix I + L, by
+// doubling: with I + L = [[A, 0], [B, E]] in equal halves,
+//   M = [[A^{-1}, 0], [-E^{-1} B A^{-1}, E^{-1}]],
+// applied from 8 x 8 diagonal blocks (forward substitution) up to 16, 32
+// and 64.  The 8 -> 16 step runs on CUDA cores inside each of four warps;
+// the 16 -> 32 and 32 -> 64 products on the warp-level tensor-core MMA
+// (tf32 operands, fp32 accumulation).  Only the lower blocks of M are
+// written: its strictly upper 8 x 8 blocks are zeroed once per CTA.  Qs is
+// per-warp scratch (8 x 256 floats); pt = 0 .. NP-1.
+__device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt)
 {
     const int wq = pt >> 5, ln = pt & 31;
-    if (wq < 4 && ln < 16) {
-        const int base = 16 * wq, cc = ln;
-        float x[16];
+    float *Qw = Qs + wq * 256;
+    if (wq < 4) {
+        // 16 x 16 diagonal block wq: its two 8 x 8 diagonal blocks (one column per lane) ...
+        const int B = 16 * wq;
+        if (ln < 16) {
+            const int base = B + 8 * (ln >> 3), cc = ln & 7;
+            float x[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = (r == cc) ? 1.f : 0.f;
+            for (int r = 0; r < 8; ++r) {
+                float acc = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < r; ++j) acc = fmaf(-Ls[(base + r) * LP + base + j], x[j], acc);
-            x[r] = (r < cc) ? 0.f : acc;
+                for (int j = 0; j < r; ++j) acc = fmaf(-Ls[(base + r) * LP + base + j], x[j], acc);
+                x[r] = (r < cc) ? 0.f : acc;
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) Ms[(base + r) * LP + base + cc] = x[r];
         }
+        __syncwarp();
+        // ... then its lower-left 8 x 8: -M_bb (L_ba M_aa), two entries per lane
+        float q[2];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Ms[(base + r) * LP + base + cc] = x[r];
-    }
-    for (int e = pt; e < 6 * 256; e += NP) {
-        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const int bi = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        Ms[(16 * bi + r) * LP + 16 * bj + cc] = 0.f;
+        for (int h = 0; h < 2; ++h) {
+            const int i = (ln >> 3) + 4 * h, j = ln & 7;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k >= j) acc = fmaf(Ls[(B + 8 + i) * LP + B + k], Ms[(B + k) * LP + B + j], acc);
+            q[h] = acc;
+        }
+        Qw[ln] = q[0];
+        Qw[ln + 32] = q[1];
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = (ln >> 3) + 4 * h, j = ln & 7;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k <= i) acc = fmaf(Ms[(B + 8 + i) * LP + B + 8 + k], Qw[k * 8 + j], acc);
+            Ms[(B + 8 + i) * LP + B + j] = -acc;
+        }
     }
     tc::bar_sync(BAR_PREP, NP);
-    float *Qw = Qs + wq * 16 * 9;  // this warp's 16 x 8 product, padded rows
-    const int g = ln >> 2, t4 = ln & 3;
-    for (int delta = 1; delta <= 3; ++delta) {
-        const int ntask = 2 * (4 - delta);
-        for (int task = wq; task < ntask; task += NP / 32) {
-            const int bj = task >> 1, nh = task & 1, bi = bj + delta;
-            float q[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ks = 0; ks < 2 * delta; ++ks) {
-                const int kc = 16 * bj + 8 * ks;
-                mma3(q, Ls, LP, 16 * bi, kc, Ms, LP, kc, 16 * bj + 8 * nh, ln);
-            }
-            Qw[g * 9 + 2 * t4] = q[0];
-            Qw[g * 9 + 2 * t4 + 1] = q[1];
-            Qw[(g + 8) * 9 + 2 * t4] = q[2];
-            Qw[(g + 8) * 9 + 2 * t4 + 1] = q[3];
-            __syncwarp();
-            float r[4] = {0.f, 0.f, 0.f, 0.f};
-            mma3(r, Ms, LP, 16 * bi, 16 * bi, Qw, 9, 0, 0, ln);
-            mma3(r, Ms, LP, 16 * bi, 16 * bi + 8, Qw, 9, 8, 0, ln);
-            const int col = 16 * bj + 8 * nh + 2 * t4;
-            Ms[(16 * bi + g) * LP + col] = -r[0];
-            Ms[(16 * bi + g) * LP + col + 1] = -r[1];
-            Ms[(16 * bi + g + 8) * LP + col] = -r[2];
-            Ms[(16 * bi + g + 8) * LP + col + 1] = -r[3];
-            __syncwarp();
-        }
-        tc::bar_sync(BAR_PREP, NP);
+    if (wq < 4) {
+        // 16 -> 32: M_10 and M_32 (16 x 16), one 8-column half per warp
+        const int bj = 2 * (wq >> 1), bi = bj + 1, c0 = 16 * bj + 8 * (wq & 1);
+        float q[4] = {0.f, 0.f, 0.f, 0.f};
+        // M_jj[k][c0..] vanishes for the first k-step when c0 is the upper half
+        if ((wq & 1) == 0) mma1(q, Ls, LP, 16 * bi, 16 * bj, Ms, LP, 16 * bj, c0, ln);
+        mma1(q, Ls, LP, 16 * bi, 16 * bj + 8, Ms, LP, 16 * bj + 8, c0, ln);
+        store_frag(Qw, 8, 0, 0, q, 1.f, ln);
+        __syncwarp();
+        float r[4] = {0.f, 0.f, 0.f, 0.f};
+        mma1(r, Ms, LP, 16 * bi, 16 * bi, Qw, 8, 0, 0, ln);
+        mma1(r, Ms, LP, 16 * bi, 16 * bi + 8, Qw, 8, 8, 0, ln);
+        store_frag(Ms, LP, 16 * bi, c0, r, -1.f, ln);
     }
+    tc::bar_sync(BAR_PREP, NP);
+    {
+        // 32 -> 64: rows 32..63 x columns 0..31; warp wq takes row block
+        // 32 + 16 rb and the 8-column strip cs.  Q = L[32.., 0..32) M[0..32, strip]
+        // (M[k][strip] = 0 for k < 8 cs), then -M[rows, 32..64) Q.
+        const int rb = wq >> 2, cs = wq & 3, c0 = 8 * cs;
+        float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ks = cs; ks < 4; ++ks) {
+            mma1(q0, Ls, LP, 32, 8 * ks, Ms, LP, 8 * ks, c0, ln);
+            if (rb) mma1(q1, Ls, LP, 48, 8 * ks, Ms, LP, 8 * ks, c0, ln);
+        }
+        store_frag(Qw, 8, 0, 0, q0, 1.f, ln);
+        if (rb) store_frag(Qw, 8, 16, 0, q1, 1.f, ln);
+        __syncwarp();
+        float r[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ks = 0; ks < 2 * (rb + 1); ++ks) mma1(r, Ms, LP, 32 + 16 * rb, 32 + 8 * ks, Qw, 8, 8 * ks, 0, ln);
+        store_frag(Ms, LP, 32 + 16 * rb, c0, r, -1.f, ln);
+    }
+    tc::bar_sync(BAR_PREP, NP);
 }
 
 // Cursor over this CTA's chunks (non-empty items only), used by the MMA issuer.
@@ -288,6 +321,27 @@ __device__ __forceinline__ void cursor_next(Cursor &cu, int n_items, const Dims 
     }
 }
 
+// The three K32-operand MMA groups of a chunk (issued by one thread).
+__device__ __forceinline__ void issue_gram(uint32_t tb, uint32_t sK32)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks)
+        tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(64, 64),
+                   ks > 0);
+}
+__device__ __forceinline__ void issue_pt(uint32_t tb, uint32_t sK32)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks)
+        tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(128, 64), ks > 0);
+}
+__device__ __forceinline__ void issue_ps(uint32_t tb, uint32_t sK32)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks)
+        tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(128, 64), ks > 0);
+}
+
 template <int CK>
 __global__ void __launch_bounds__(NT, 1)
 build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ SegTable tab,
@@ -303,7 +357,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
     uint32_t *tmem_base_sh = reinterpret_cast<uint32_t *>(sm + SM_MISC + 16);
     float *Ls = reinterpret_cast<float *>(sm + SM_L);
     float *Ms = reinterpret_cast<float *>(sm + SM_M);
-    float *Qs = reinterpret_cast<float *>(sm + SM_Q);
+    float *Qs = reinterpret_cast<float *>(sm + SM_MT);  // inverse scratch; (D M)^T is written after it
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Dims dm = a.dm;
@@ -319,6 +373,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         }
         tc::fence_mbar_init();
     }
+    for (int i = tid; i < C * LP; i += NT) Ms[i] = 0.f;  // the upper blocks of M stay zero
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_base_sh), TM_COLS);
     tc::fence_before();
     __syncthreads();
@@ -376,34 +431,30 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         }
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
-        // Per chunk n: Gram(n), Pt(n) (both halves), U~(n), Xt_T update,
-        // Xt_S update -- each as soon as its inputs are ready, waiting with
-        // hardware-suspended bounded waits.  Chunk n+1's preparation runs on
-        // the CUDA cores while Pt(n) .. Xt_S(n) run on the tensor core.
+        // Issue order: Gram(0), Pt(0); then per chunk n: U~(n), Gram(n+1),
+        // Xt_T update (n), Xt_S update (n), Pt(n+1) -- each as soon as its
+        // inputs are ready (hardware-suspended bounded waits).  Gram(n+1)
+        // runs ahead of chunk n's Xt updates so that the preparation warps
+        // find it done; tcgen05.mma from one thread execute in issue order, so
+        // a later MMA never overwrites tensor memory that an earlier one reads.
         if (lane == 0) {
             Cursor mc{static_cast<int>(blockIdx.x), 0, 0, 0, 0};
             cursor_seek(mc, n_items, dm, tab);
-            while (mc.item < n_items) {
+            bool go = mc.item < n_items;
+            if (go) {
+                go = wait_bar(bar(B_KREADY), 0, abort_flag) && wait_bar(bar(B_XREADY), 0, abort_flag);
+                tc::fence_after();
+                if (go) {
+                    issue_gram(tb, sK32);
+                    tc::commit(bar(B_GRAM));
+                    issue_pt(tb, sK32);
+                    tc::commit(bar(B_PTDONE));
+                    issue_ps(tb, sK32);
+                    tc::commit(bar(B_PSDONE));
+                }
+            }
+            while (go && mc.item < n_items) {
                 const uint32_t par = mc.n & 1;
-                if (!wait_bar(bar(B_KREADY), par, abort_flag)) break;
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks),
-                               tc::idesc_tf32(64, 64), ks > 0);
-                tc::commit(bar(B_GRAM));
-                if (mc.c == 0 && !wait_bar(bar(B_XREADY), mc.xi & 1, abort_flag)) break;
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK32, C, ks),
-                               tc::idesc_tf32(128, 64), ks > 0);
-                tc::commit(bar(B_PTDONE));
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks),
-                               tc::idesc_tf32(128, 64), ks > 0);
-                tc::commit(bar(B_PSDONE));
                 if (!wait_bar(bar(B_KTREADY), par, abort_flag)) break;
                 tc::fence_after();
 #pragma unroll
@@ -411,6 +462,15 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     tc::mma_ts(tb + TM_U, tb + TM_G + ks * 8, tc::sdesc_kstep(sMT, C, ks),
                                tc::idesc_tf32(128, 64), ks > 0);
                 tc::commit(bar(B_UDONE));
+                Cursor nx = mc;
+                cursor_next(nx, n_items, dm, tab);
+                const bool more = nx.item < n_items;
+                if (more) {
+                    if (!wait_bar(bar(B_KREADY), par ^ 1u, abort_flag)) break;
+                    tc::fence_after();
+                    issue_gram(tb, sK32);
+                    tc::commit(bar(B_GRAM));
+                }
                 if (!wait_bar(bar(B_UTREADY), par, abort_flag)) break;
                 if (!wait_bar(bar(B_RTREADY), par, abort_flag)) break;
                 tc::fence_after();
@@ -425,113 +485,39 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     tc::mma_ts(tb + TM_XS, tb + TM_PS + ks * 8, tc::sdesc_kstep(sUT, D, ks),
                                tc::idesc_tf32(128, 128), 1);
                 tc::commit(bar(B_DSDONE));
-                cursor_next(mc, n_items, dm, tab);
+                if (more) {
+                    if (nx.c == 0 && !wait_bar(bar(B_XREADY), nx.xi & 1, abort_flag)) break;
+                    tc::fence_after();
+                    issue_pt(tb, sK32);
+                    tc::commit(bar(B_PTDONE));
+                    issue_ps(tb, sK32);
+                    tc::commit(bar(B_PSDONE));
+                }
+                mc = nx;
             }
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ preparation
+        // Step k: finish chunk k-1 up to its U~ operands (L, inverse, K^T,
+        // (D M)^T), convert chunk k (gates, conv + normalisation, tf32 K)
+        // while U~(k-1) runs, then copy U~(k-1)^T to shared memory.
         const int pt = tid - 128;      // 0 .. NP-1
         const int li = pt & 127;       // tensor-memory lane of this thread
         const int hh = pt >> 7;        // which half of a 64-column operand this warp handles
-        const int c0 = (pt & 15) * 8;  // the 8 channels this thread converts
-        float wkr[8][CK > 0 ? CK : 1];
-        int n = 0;
+        const int c0 = (pt & 15) * 8;  // the 8 channels this thread converts ...
+        const int r0 = 4 * (pt >> 4);  // ... in chunk rows r0 .. r0+3
+        int wk_item = -1;  // item whose conv weights are in shared memory
+        Cursor cv{static_cast<int>(blockIdx.x), 0, 0, 0, 0};
+        cursor_seek(cv, n_items, dm, tab);
         bool ok = true;
-        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
-            const Item it = decode_item(itx, dm, tab);
-            if (CK > 0 && it.nch > 0) {
-                const float *wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int j = 0; j < (CK > 0 ? CK : 1); ++j) wkr[i][j] = __ldg(wk + (c0 + i) * CK + j);
-            }
-            for (int c = 0; c < it.nch; ++c, ++n) {
-                const int s = n % RS;
-                const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (n & 1) * 1280);
-                const int nc = min(C, (int)(it.n - c * C));
+        for (int k = 0; ok; ++k) {
+            const bool conv_k = cv.item < n_items;  // chunk k exists
+            if (k > 0) {
+                // ---- chunk m = k-1: L from the Gram rows (M = 64 layout: row 16q + i in lane 32q + i)
+                const int m = k - 1;
+                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (m % 3) * 1280);
                 bool w = true;
-                if (pt == 0) {
-                    w = wait_bar(bar(B_FULL + s), (n / RS) & 1, abort_flag);
-                    if (w && n > 0) w = wait_bar(bar(B_PSDONE), (n - 1) & 1, abort_flag);  // K32 free
-                }
-                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
-                // gates (one warp, two tokens per lane)
-                if (warp == 4) {
-                    const float *A = reinterpret_cast<const float *>(stg + ST_A);
-                    const float *B = reinterpret_cast<const float *>(stg + ST_B);
-                    const float x0 = fmaxf(logf(A[2 * lane]), -88.f);  // alpha = 0 -> exp(-88)
-                    const float x1 = fmaxf(logf(A[2 * lane + 1]), -88.f);
-                    float sum = x0 + x1;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, sum, o);
-                        if (lane >= o) sum += y;
-                    }
-                    const float total = __shfl_sync(0xffffffffu, sum, 31);
-                    const float g1 = sum, g0 = sum - x1;
-                    G.g[2 * lane] = g0;
-                    G.g[2 * lane + 1] = g1;
-                    G.eg[2 * lane] = expf(g0);
-                    G.eg[2 * lane + 1] = expf(g1);
-                    G.b[2 * lane] = B[2 * lane];
-                    G.b[2 * lane + 1] = B[2 * lane + 1];
-                    G.dc[2 * lane] = B[2 * lane] * expf(total - g0);
-                    G.dc[2 * lane + 1] = B[2 * lane + 1] * expf(total - g1);
-                    const float gm = 0.5f * (__shfl_sync(0xffffffffu, x0, 0) + total);
-                    G.fb[2 * lane] = B[2 * lane] * __expf(fmaxf(gm - g0, -87.f));
-                    G.fb[2 * lane + 1] = B[2 * lane + 1] * __expf(fmaxf(gm - g1, -87.f));
-                }
-                // K -> tf32 (conv + L2 normalisation first when present)
-#pragma unroll 2
-                for (int iter = 0; iter < (C * D / 8) / NP; ++iter) {
-                    const int t = iter * (NP / 16) + (pt >> 4);
-                    float kx[8];
-                    if (t < nc) {
-                        if (CK == 0) {
-                            unpack8(*reinterpret_cast<const uint4 *>(stg + ST_K + (t * D + c0) * 2), kx);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) kx[i] = 0.f;
-#pragma unroll
-                            for (int j = 0; j < CK; ++j) {
-                                float rk[8];
-                                unpack8(*reinterpret_cast<const uint4 *>(stg + ST_K + ((t + HIST - j) * D + c0) * 2),
-                                        rk);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) kx[i] = fmaf(wkr[i][j], rk[i], kx[i]);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) kx[i] = 0.f;
-                    }
-                    if (CK > 0) {
-                        float ss = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) ss = fmaf(kx[i], kx[i], ss);
-#pragma unroll
-                        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                        const float inv = 1.f / sqrtf(ss + kL2Eps);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) kx[i] *= inv;
-                    }
-                    *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(t, c0, C)) =
-                        make_float4(tc::round_tf32(kx[0]), tc::round_tf32(kx[1]), tc::round_tf32(kx[2]),
-                                    tc::round_tf32(kx[3]));
-                    *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(t, c0 + 4, C)) =
-                        make_float4(tc::round_tf32(kx[4]), tc::round_tf32(kx[5]), tc::round_tf32(kx[6]),
-                                    tc::round_tf32(kx[7]));
-                }
-                tc::fence_async_smem();
-                tc::bar_sync(BAR_PREP, NP);
-                if (pt == 0) {
-                    tc::mbar_arrive(bar(B_KREADY));
-                    tc::mbar_arrive(bar(B_EMPTY + s));  // K rows and gates consumed
-                }
-                // L from the Gram rows (M = 64 layout: row 16q + i in lane 32q + i)
-                if (pt == 0) w = wait_bar(bar(B_GRAM), n & 1, abort_flag);
+                if (pt == 0) w = wait_bar(bar(B_GRAM), m & 1, abort_flag);
                 if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
                 tc::fence_after();
                 {
@@ -572,10 +558,10 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         kt[j] = *reinterpret_cast<const float *>(sm + SM_K32 + tc::sw128_f32(hh * 32 + j, li, C));
                     tc::tmem_st32(my + TM_G + hh * 32, kt);
                 }
-                // B of U~: element (t, j) = dc_j M[j][t]
-#pragma unroll 2
+                // B of U~: element (t, j) = dc_j M[j][t]; consecutive lanes take consecutive t
+#pragma unroll
                 for (int e = pt; e < C * C / 4; e += NP) {
-                    const int t = e >> 4, j = (e & 15) * 4;
+                    const int t = e & (C - 1), j = (e >> 6) * 4;
                     *reinterpret_cast<float4 *>(sm + SM_MT + tc::sw128_f32(t, j, C)) =
                         make_float4(tc::round_tf32(G.dc[j] * Ms[j * LP + t]),
                                     tc::round_tf32(G.dc[j + 1] * Ms[(j + 1) * LP + t]),
@@ -586,10 +572,140 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 tc::fence_before();
                 tc::bar_sync(BAR_PREP, NP);
                 if (pt == 0) tc::mbar_arrive(bar(B_KTREADY));
-                // U~^T rows into shared memory once the previous chunk's Xt update is done
+            }
+            if (conv_k) {
+                // ---- chunk k: gates and K -> tf32 (conv + L2 normalisation first when present)
+                const Item it = decode_item(cv.item, dm, tab);
+                if (CK > 0 && cv.item != wk_item) {
+                    // visible to all preparation threads after the barrier below
+                    const float *wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
+                    if (pt < D) {
+                        const float4 w4 = *reinterpret_cast<const float4 *>(wk + pt * CK);
+                        float *ws = reinterpret_cast<float *>(sm + SM_WK);
+                        ws[pt] = w4.x;
+                        ws[D + pt] = w4.y;
+                        ws[2 * D + pt] = w4.z;
+                        ws[3 * D + pt] = w4.w;
+                    }
+                    wk_item = cv.item;
+                }
+                const int s = k % RS;
+                const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
+                Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (k % 3) * 1280);
+                const int nc = min(C, (int)(it.n - cv.c * C));
+                bool w = true;
                 if (pt == 0) {
-                    w = wait_bar(bar(B_UDONE), n & 1, abort_flag);
-                    if (w && n > 0) w = wait_bar(bar(B_DSDONE), (n - 1) & 1, abort_flag);
+                    w = wait_bar(bar(B_FULL + s), (k / RS) & 1, abort_flag);
+                    if (w && k > 0) w = wait_bar(bar(B_PSDONE), (k - 1) & 1, abort_flag);  // K32 free
+                }
+                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
+                if (warp == 4) {
+                    // gates (one warp, two tokens per lane)
+                    const float *A = reinterpret_cast<const float *>(stg + ST_A);
+                    const float *B = reinterpret_cast<const float *>(stg + ST_B);
+                    const float x0 = fmaxf(logf(A[2 * lane]), -88.f);  // alpha = 0 -> exp(-88)
+                    const float x1 = fmaxf(logf(A[2 * lane + 1]), -88.f);
+                    float sum = x0 + x1;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, sum, o);
+                        if (lane >= o) sum += y;
+                    }
+                    const float total = __shfl_sync(0xffffffffu, sum, 31);
+                    const float g1 = sum, g0 = sum - x1;
+                    G.g[2 * lane] = g0;
+                    G.g[2 * lane + 1] = g1;
+                    G.eg[2 * lane] = expf(g0);
+                    G.eg[2 * lane + 1] = expf(g1);
+                    G.b[2 * lane] = B[2 * lane];
+                    G.b[2 * lane + 1] = B[2 * lane + 1];
+                    G.dc[2 * lane] = B[2 * lane] * expf(total - g0);
+                    G.dc[2 * lane + 1] = B[2 * lane + 1] * expf(total - g1);
+                    const float gm = 0.5f * (__shfl_sync(0xffffffffu, x0, 0) + total);
+                    G.fb[2 * lane] = B[2 * lane] * __expf(fmaxf(gm - g0, -87.f));
+                    G.fb[2 * lane + 1] = B[2 * lane + 1] * __expf(fmaxf(gm - g1, -87.f));
+                }
+                {
+                    // rows r0 .. r0+3 use staged rows r0 .. r0+3+HIST (row t + HIST - j is lag j)
+                    uint4 raw[4 + HIST];
+#pragma unroll
+                    for (int i = 0; i < 4 + HIST; ++i)
+                        raw[i] = *reinterpret_cast<const uint4 *>(stg + ST_K + ((r0 + i) * D + c0) * 2);
+                    float kx[4][8];
+                    if (CK == 0) {
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) unpack8(raw[r], kx[r]);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) kx[r][i] = 0.f;
+#pragma unroll
+                        for (int j = 0; j < (CK > 0 ? CK : 1); ++j) {
+                            // lag-j weights of channels c0 .. c0+7
+                            const float4 wa = *reinterpret_cast<const float4 *>(sm + SM_WK + (j * D + c0) * 4);
+                            const float4 wb = *reinterpret_cast<const float4 *>(sm + SM_WK + (j * D + c0 + 4) * 4);
+                            const float wj[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                float rk[8];
+                                unpack8(raw[r + HIST - j], rk);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) kx[r][i] = fmaf(wj[i], rk[i], kx[r][i]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        if (r0 + r >= nc) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) kx[r][i] = 0.f;
+                        }
+                    }
+                    if (CK > 0) {
+                        float ss[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            ss[r] = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) ss[r] = fmaf(kx[r][i], kx[r][i], ss[r]);
+                        }
+#pragma unroll
+                        for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float inv = 1.f / sqrtf(ss[r] + kL2Eps);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) kx[r][i] *= inv;
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(r0 + r, c0, C)) =
+                            make_float4(tc::round_tf32(kx[r][0]), tc::round_tf32(kx[r][1]),
+                                        tc::round_tf32(kx[r][2]), tc::round_tf32(kx[r][3]));
+                        *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(r0 + r, c0 + 4, C)) =
+                            make_float4(tc::round_tf32(kx[r][4]), tc::round_tf32(kx[r][5]),
+                                        tc::round_tf32(kx[r][6]), tc::round_tf32(kx[r][7]));
+                    }
+                }
+                tc::fence_async_smem();
+                tc::bar_sync(BAR_PREP, NP);
+                if (pt == 0) {
+                    tc::mbar_arrive(bar(B_KREADY));
+                    tc::mbar_arrive(bar(B_EMPTY + s));  // K rows and gates consumed
+                }
+                cursor_next(cv, n_items, dm, tab);
+            }
+            if (k > 0) {
+                // ---- chunk m = k-1: U~^T rows into shared memory once the previous Xt update is done
+                const int m = k - 1;
+                bool w = true;
+                if (pt == 0) {
+                    w = wait_bar(bar(B_UDONE), m & 1, abort_flag);
+                    if (w && m > 0) w = wait_bar(bar(B_DSDONE), (m - 1) & 1, abort_flag);
                 }
                 if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
                 tc::fence_after();
@@ -607,6 +723,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 tc::bar_sync(BAR_PREP, NP);
                 if (pt == 0) tc::mbar_arrive(bar(B_UTREADY));
             }
+            if (!conv_k) break;
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 0-3)
@@ -651,7 +768,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
             for (int c = 0; c < it.nch; ++c, ++n) {
                 const int s = n % RS;
                 const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (n & 1) * 1280);
+                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (n % 3) * 1280);
                 const int nc = min(C, (int)(it.n - c * C));
                 // ---- T half
                 bool w = true;
