@@ -66,20 +66,18 @@ constexpr uint32_t TM_COLS = 512;
 // raw stage: K rows, V rows (bf16 [ROWS][128]), alpha[64], beta[64] (fp32)
 constexpr uint32_t ST_K = 0;
 constexpr uint32_t ST_V = ROWS * D * 2;
-constexpr uint32_t ST_A = 2 * ROWS * D * 2;
-constexpr uint32_t ST_B = ST_A + C * 4;
-constexpr uint32_t ST_BYTES = ST_B + C * 4;
+constexpr uint32_t ST_G = 2 * ROWS * D * 2;  // the chunk's Gates, written by the producer warp
+constexpr uint32_t ST_BYTES = ST_G + 5 * C * 4;
 
 // shared memory (byte offsets from a 1024-aligned base)
 constexpr uint32_t SM_RAW = 0;
-constexpr uint32_t SM_K32 = RS * ST_BYTES;     // K [64][128] tf32, sw128
+constexpr uint32_t SM_K32 = (RS * ST_BYTES + 1023) / 1024 * 1024;  // K [64][128] tf32, sw128
 constexpr uint32_t SM_UT = SM_K32 + 32768;     // U~^T [128][64] tf32, sw128 (B of the Xt update)
 constexpr uint32_t SM_MT = SM_UT + 32768;      // (D M)^T [64][64] tf32, sw128 (B of U~)
 constexpr int LP = C + 1;
 constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][65]
 constexpr uint32_t SM_M = SM_L + C * LP * 4;   // (I + L)^-1 [64][65]
-constexpr uint32_t SM_GATE = SM_M + C * LP * 4;  // 3 x Gates (chunk n uses buffer n % 3)
-constexpr uint32_t SM_WK = SM_GATE + 3 * 1280;  // K conv weights of the current item [4 lags][128]
+constexpr uint32_t SM_WK = SM_M + C * LP * 4;  // K conv weights of the current item [4 lags][128]
 constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
@@ -296,14 +294,15 @@ struct Cursor {
     int nch;
     int n;     // CTA-wide chunk number
     int xi;    // index of the item among this CTA's non-empty items
+    Item it;   // the item, decoded once
 };
 
 __device__ __forceinline__ void cursor_seek(Cursor &cu, int n_items, const Dims &dm, const SegTable &tab)
 {
     while (cu.item < n_items) {
-        const Item it = decode_item(cu.item, dm, tab);
-        if (it.nch > 0) {
-            cu.nch = it.nch;
+        cu.it = decode_item(cu.item, dm, tab);
+        if (cu.it.nch > 0) {
+            cu.nch = cu.it.nch;
             return;
         }
         cu.item += gridDim.x;
@@ -400,15 +399,40 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
                 const int32_t t0 = c * C;
                 const int nc = min(C, (int)(it.n - t0));
-                for (int tt = lane; tt < C; tt += 32) {
-                    float al = 1.f, be = 0.f;
-                    if (tt < nc) {
-                        const size_t gi = gate_index(dm, N, it.l, it.b0 + t0 + tt, it.h);
-                        al = __bfloat162float(ap[gi]);
-                        be = __bfloat162float(bp[gi]);
+                {
+                    // gates of tokens 2 lane, 2 lane + 1 (padding: alpha = 1, beta = 0)
+                    float al[2] = {1.f, 1.f}, be[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int tt = 2 * lane + u;
+                        if (tt < nc) {
+                            const size_t gi = gate_index(dm, N, it.l, it.b0 + t0 + tt, it.h);
+                            al[u] = __bfloat162float(ap[gi]);
+                            be[u] = __bfloat162float(bp[gi]);
+                        }
                     }
-                    reinterpret_cast<float *>(stg + ST_A)[tt] = al;
-                    reinterpret_cast<float *>(stg + ST_B)[tt] = be;
+                    Gates &G = *reinterpret_cast<Gates *>(stg + ST_G);
+                    const float x0 = fmaxf(logf(al[0]), -88.f);  // alpha = 0 -> exp(-88)
+                    const float x1 = fmaxf(logf(al[1]), -88.f);
+                    float sum = x0 + x1;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, sum, o);
+                        if (lane >= o) sum += y;
+                    }
+                    const float total = __shfl_sync(0xffffffffu, sum, 31);
+                    const float g1 = sum, g0 = sum - x1;
+                    G.g[2 * lane] = g0;
+                    G.g[2 * lane + 1] = g1;
+                    G.eg[2 * lane] = expf(g0);
+                    G.eg[2 * lane + 1] = expf(g1);
+                    G.b[2 * lane] = be[0];
+                    G.b[2 * lane + 1] = be[1];
+                    G.dc[2 * lane] = be[0] * expf(total - g0);
+                    G.dc[2 * lane + 1] = be[1] * expf(total - g1);
+                    const float gm = 0.5f * (__shfl_sync(0xffffffffu, x0, 0) + total);
+                    G.fb[2 * lane] = be[0] * __expf(fmaxf(gm - g0, -87.f));
+                    G.fb[2 * lane + 1] = be[1] * __expf(fmaxf(gm - g1, -87.f));
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -438,7 +462,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         // find it done; tcgen05.mma from one thread execute in issue order, so
         // a later MMA never overwrites tensor memory that an earlier one reads.
         if (lane == 0) {
-            Cursor mc{static_cast<int>(blockIdx.x), 0, 0, 0, 0};
+            Cursor mc{static_cast<int>(blockIdx.x), 0, 0, 0, 0, {}};
             cursor_seek(mc, n_items, dm, tab);
             bool go = mc.item < n_items;
             if (go) {
@@ -507,7 +531,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         const int c0 = (pt & 15) * 8;  // the 8 channels this thread converts ...
         const int r0 = 4 * (pt >> 4);  // ... in chunk rows r0 .. r0+3
         int wk_item = -1;  // item whose conv weights are in shared memory
-        Cursor cv{static_cast<int>(blockIdx.x), 0, 0, 0, 0};
+        Cursor cv{static_cast<int>(blockIdx.x), 0, 0, 0, 0, {}};
         cursor_seek(cv, n_items, dm, tab);
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -515,7 +539,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
             if (k > 0) {
                 // ---- chunk m = k-1: L from the Gram rows (M = 64 layout: row 16q + i in lane 32q + i)
                 const int m = k - 1;
-                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (m % 3) * 1280);
+                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_RAW + (m % RS) * ST_BYTES + ST_G);
                 bool w = true;
                 if (pt == 0) w = wait_bar(bar(B_GRAM), m & 1, abort_flag);
                 if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
@@ -571,11 +595,14 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 tc::fence_async_smem();
                 tc::fence_before();
                 tc::bar_sync(BAR_PREP, NP);
-                if (pt == 0) tc::mbar_arrive(bar(B_KTREADY));
+                if (pt == 0) {
+                    tc::mbar_arrive(bar(B_KTREADY));
+                    tc::mbar_arrive(bar(B_EMPTY + m % RS));  // K rows and gates consumed
+                }
             }
             if (conv_k) {
                 // ---- chunk k: gates and K -> tf32 (conv + L2 normalisation first when present)
-                const Item it = decode_item(cv.item, dm, tab);
+                const Item &it = cv.it;
                 if (CK > 0 && cv.item != wk_item) {
                     // visible to all preparation threads after the barrier below
                     const float *wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
@@ -591,40 +618,11 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 }
                 const int s = k % RS;
                 const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (k % 3) * 1280);
                 const int nc = min(C, (int)(it.n - cv.c * C));
                 bool w = true;
-                if (pt == 0) {
-                    w = wait_bar(bar(B_FULL + s), (k / RS) & 1, abort_flag);
-                    if (w && k > 0) w = wait_bar(bar(B_PSDONE), (k - 1) & 1, abort_flag);  // K32 free
-                }
+                if (pt == 0) w = wait_bar(bar(B_FULL + s), (k / RS) & 1, abort_flag);
+                if (pt == 32 && k > 0) w = wait_bar(bar(B_PSDONE), (k - 1) & 1, abort_flag);  // K32 free
                 if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
-                if (warp == 4) {
-                    // gates (one warp, two tokens per lane)
-                    const float *A = reinterpret_cast<const float *>(stg + ST_A);
-                    const float *B = reinterpret_cast<const float *>(stg + ST_B);
-                    const float x0 = fmaxf(logf(A[2 * lane]), -88.f);  // alpha = 0 -> exp(-88)
-                    const float x1 = fmaxf(logf(A[2 * lane + 1]), -88.f);
-                    float sum = x0 + x1;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, sum, o);
-                        if (lane >= o) sum += y;
-                    }
-                    const float total = __shfl_sync(0xffffffffu, sum, 31);
-                    const float g1 = sum, g0 = sum - x1;
-                    G.g[2 * lane] = g0;
-                    G.g[2 * lane + 1] = g1;
-                    G.eg[2 * lane] = expf(g0);
-                    G.eg[2 * lane + 1] = expf(g1);
-                    G.b[2 * lane] = B[2 * lane];
-                    G.b[2 * lane + 1] = B[2 * lane + 1];
-                    G.dc[2 * lane] = B[2 * lane] * expf(total - g0);
-                    G.dc[2 * lane + 1] = B[2 * lane + 1] * expf(total - g1);
-                    const float gm = 0.5f * (__shfl_sync(0xffffffffu, x0, 0) + total);
-                    G.fb[2 * lane] = B[2 * lane] * __expf(fmaxf(gm - g0, -87.f));
-                    G.fb[2 * lane + 1] = B[2 * lane + 1] * __expf(fmaxf(gm - g1, -87.f));
-                }
                 {
                     // rows r0 .. r0+3 use staged rows r0 .. r0+3+HIST (row t + HIST - j is lag j)
                     uint4 raw[4 + HIST];
@@ -693,20 +691,15 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 }
                 tc::fence_async_smem();
                 tc::bar_sync(BAR_PREP, NP);
-                if (pt == 0) {
-                    tc::mbar_arrive(bar(B_KREADY));
-                    tc::mbar_arrive(bar(B_EMPTY + s));  // K rows and gates consumed
-                }
+                if (pt == 0) tc::mbar_arrive(bar(B_KREADY));
                 cursor_next(cv, n_items, dm, tab);
             }
             if (k > 0) {
                 // ---- chunk m = k-1: U~^T rows into shared memory once the previous Xt update is done
                 const int m = k - 1;
                 bool w = true;
-                if (pt == 0) {
-                    w = wait_bar(bar(B_UDONE), m & 1, abort_flag);
-                    if (w && m > 0) w = wait_bar(bar(B_DSDONE), (m - 1) & 1, abort_flag);
-                }
+                if (pt == 0) w = wait_bar(bar(B_UDONE), m & 1, abort_flag);
+                if (pt == 32 && m > 0) w = wait_bar(bar(B_DSDONE), (m - 1) & 1, abort_flag);
                 if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
                 tc::fence_after();
                 {
@@ -768,7 +761,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
             for (int c = 0; c < it.nch; ++c, ++n) {
                 const int s = n % RS;
                 const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_GATE + (n % 3) * 1280);
+                const Gates &G = *reinterpret_cast<const Gates *>(stg + ST_G);
                 const int nc = min(C, (int)(it.n - c * C));
                 // ---- T half
                 bool w = true;
