@@ -234,7 +234,7 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
     peaks = _peaks()
 
-    wl = W.make(WORKLOAD, device=dev)
+    wl = W.make(WORKLOAD, device=dev, layers=args.layers)
     d = wl.desc
     L, H, D, w = d["n_layers"], d["n_heads"], d["d_k"], d["seam_w"]
     n_seg, n_ord = wl.n_seg, len(wl.order)
@@ -355,7 +355,8 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": _config(),
+            "config": dict(_config(), **({"layers": L, "subset": "first %d layers only" % L}
+                                         if args.layers else {})),
             "components": {
                 "build": {"mtok_s_per_layer": build_mtok, "ms": build_ms, "launches_per_step": 1},
                 "compose_with_seams": {"segs_s_per_layer": comp_segs, "ms": comp_ms,
@@ -383,6 +384,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="first N layers of the workload only (small cases for profiling; "
+                         "not a bench line)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -45,7 +45,7 @@ namespace {
 
 constexpr int D = 128;   // head width
 constexpr int C = 64;    // chunk length
-constexpr int RS = 3;    // raw-input ring stages
+constexpr int RS = 2;    // raw-input ring stages
 constexpr int HMAX = 3;  // conv history rows kept per chunk (conv_k <= 4)
 constexpr int ROWS = C + HMAX;
 constexpr int NP = 256;  // preparation threads (warps 4-11, two per tensor-memory lane quadrant)
@@ -74,15 +74,18 @@ constexpr uint32_t SM_RAW = 0;
 constexpr uint32_t SM_K32 = (RS * ST_BYTES + 1023) / 1024 * 1024;  // K [64][128] tf32, sw128
 constexpr uint32_t SM_UT = SM_K32 + 32768;     // U~^T [128][64] tf32, sw128 (B of the Xt update)
 constexpr uint32_t SM_MT = SM_UT + 32768;      // (D M)^T [64][64] tf32, sw128 (B of U~)
-constexpr int LP = C + 1;
-constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][65]
-constexpr uint32_t SM_M = SM_L + C * LP * 4;   // (I + L)^-1 [64][65]
-constexpr uint32_t SM_WK = SM_M + C * LP * 4;  // K conv weights of the current item [4 lags][128]
+constexpr int LP = C + 4;                      // row pitch of L and M: 16-byte rows for ldmatrix
+constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][68], tf32 values
+constexpr uint32_t SM_M = SM_L + C * LP * 4;   // M = (I + L)^-1 [64][68], tf32 values
+constexpr int QP = 36;                         // row pitch of the per-warp Q^T scratch
+constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // per-warp Q^T [8][36] for the inverse
+constexpr uint32_t SM_WK = SM_Q + 8 * 8 * QP * 4;  // K conv weights of the current item [4 lags][128]
 constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
 static_assert(SM_K32 % 1024 == 0 && SM_UT % 1024 == 0 && SM_MT % 1024 == 0, "tile alignment");
+static_assert(SM_L % 16 == 0 && SM_M % 16 == 0 && SM_Q % 16 == 0, "ldmatrix row alignment");
 static_assert(ST_BYTES % 128 == 0 && ST_V % 128 == 0, "TMA destination alignment");
 static_assert(SMEM_DYN <= 232448, "shared memory budget");
 
@@ -170,31 +173,62 @@ __device__ __forceinline__ void mma16x8x8(float (&c)[4], const uint32_t (&a)[4],
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// c (16 x 8) += X[r0 .. r0+16)[k0 .. k0+8) * Y[k0y .. k0y+8)[c0 .. c0+8), operands
-// rounded to tf32.
-__device__ __forceinline__ void mma1(float (&c)[4], const float *X, int ldx, int r0, int k0, const float *Y,
-                                     int ldy, int k0y, int c0, int lane)
+// Warp-level tf32 MMA operands straight from shared memory (ldmatrix of 8 x 4
+// fp32 tiles: lane 4g + t receives element (g, t) of each tile).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
-    const int g = lane >> 2, t4 = lane & 3;
-    uint32_t a[4], b[2];
-    a[0] = __float_as_uint(tc::round_tf32(X[(r0 + g) * ldx + k0 + t4]));
-    a[1] = __float_as_uint(tc::round_tf32(X[(r0 + g + 8) * ldx + k0 + t4]));
-    a[2] = __float_as_uint(tc::round_tf32(X[(r0 + g) * ldx + k0 + t4 + 4]));
-    a[3] = __float_as_uint(tc::round_tf32(X[(r0 + g + 8) * ldx + k0 + t4 + 4]));
-    b[0] = __float_as_uint(tc::round_tf32(Y[(k0y + t4) * ldy + c0 + g]));
-    b[1] = __float_as_uint(tc::round_tf32(Y[(k0y + t4 + 4) * ldy + c0 + g]));
-    mma16x8x8(c, a, b);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr) : "memory");
 }
 
-// Store a 16 x 8 accumulator fragment (times s) at rows r0.., columns c0.. of Y.
-__device__ __forceinline__ void store_frag(float *Y, int ldy, int r0, int c0, const float (&c)[4], float s,
-                                           int lane)
+// Row-major fp32 matrix with pitch LP floats: A fragment of the 16 x 8 tile at (r0, k0).
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], uint32_t base, int r0, int k0, int lane)
+{
+    const int row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8, col = k0 + (lane >> 4) * 4;
+    ldsm_x4(a, base + (row * LP + col) * 4);
+}
+
+// B fragment (k0 .. k0+8) x (n0 .. n0+8) of a matrix stored transposed in the
+// 64 x 64 sw128 tile at base (row n holds column n of the matrix).
+__device__ __forceinline__ void frag_b_sw(uint32_t (&b)[2], uint32_t base, int k0, int n0, int lane)
+{
+    ldsm_x2(b, base + tc::sw128_f32(n0 + (lane & 7), k0 + ((lane >> 3) & 1) * 4, C));
+}
+
+// B fragment of the per-warp Q^T scratch (pitch QP): rows k0 .. k0+8 of Q.
+__device__ __forceinline__ void frag_b_q(uint32_t (&b)[2], uint32_t qt, int k0, int lane)
+{
+    ldsm_x2(b, qt + ((lane & 7) * QP + k0 + ((lane >> 3) & 1) * 4) * 4);
+}
+
+// Store a 16 x 8 accumulator fragment (rows r0.., columns c0..) as tf32 values,
+// negated, into M (row-major) and M^T (sw128 tile).
+__device__ __forceinline__ void store_m(float *Ms, uint8_t *Mt, int r0, int c0, const float (&c)[4], int lane)
 {
     const int g = lane >> 2, t4 = lane & 3;
-    Y[(r0 + g) * ldy + c0 + 2 * t4] = s * c[0];
-    Y[(r0 + g) * ldy + c0 + 2 * t4 + 1] = s * c[1];
-    Y[(r0 + g + 8) * ldy + c0 + 2 * t4] = s * c[2];
-    Y[(r0 + g + 8) * ldy + c0 + 2 * t4 + 1] = s * c[3];
+    const float v0 = tc::round_tf32(-c[0]), v1 = tc::round_tf32(-c[1]);
+    const float v2 = tc::round_tf32(-c[2]), v3 = tc::round_tf32(-c[3]);
+    *reinterpret_cast<float2 *>(Ms + (r0 + g) * LP + c0 + 2 * t4) = make_float2(v0, v1);
+    *reinterpret_cast<float2 *>(Ms + (r0 + g + 8) * LP + c0 + 2 * t4) = make_float2(v2, v3);
+    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4, r0 + g, C)) = v0;
+    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4 + 1, r0 + g, C)) = v1;
+    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4, r0 + g + 8, C)) = v2;
+    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4 + 1, r0 + g + 8, C)) = v3;
+}
+
+// Store a 16 x 8 accumulator fragment as tf32 values into rows r0.. of the Q^T scratch.
+__device__ __forceinline__ void store_q(float *Qt, int r0, const float (&c)[4], int lane)
+{
+    const int g = lane >> 2, t4 = lane & 3;
+    Qt[(2 * t4) * QP + r0 + g] = tc::round_tf32(c[0]);
+    Qt[(2 * t4 + 1) * QP + r0 + g] = tc::round_tf32(c[1]);
+    Qt[(2 * t4) * QP + r0 + g + 8] = tc::round_tf32(c[2]);
+    Qt[(2 * t4 + 1) * QP + r0 + g + 8] = tc::round_tf32(c[3]);
 }
 
 // M = (I + L)^{-1} for the unit lower triangular 64 x 64 matrix I + L, by
@@ -203,13 +237,16 @@ __device__ __forceinline__ void store_frag(float *Y, int ldy, int r0, int c0, co
 // applied from 8 x 8 diagonal blocks (forward substitution) up to 16, 32
 // and 64.  The 8 -> 16 step runs on CUDA cores inside each of four warps;
 // the 16 -> 32 and 32 -> 64 products on the warp-level tensor-core MMA
-// (tf32 operands, fp32 accumulation).  Only the lower blocks of M are
-// written: its strictly upper 8 x 8 blocks are zeroed once per CTA.  Qs is
-// per-warp scratch (8 x 256 floats); pt = 0 .. NP-1.
-__device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, float *Qs, int pt)
+// (tf32 operands, fp32 accumulation).  L holds tf32 values; M is written as
+// tf32 values twice, row-major (Ms, A operands) and transposed into the
+// sw128 tile Mt (B operands, and later (D M)^T in place).  Only the lower
+// blocks are written: the strictly upper 8 x 8 blocks stay zero from the
+// start of the kernel.  pt = 0 .. NP-1.
+__device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, uint8_t *Mt, float *Qs, int pt)
 {
     const int wq = pt >> 5, ln = pt & 31;
-    float *Qw = Qs + wq * 256;
+    float *Qt = Qs + wq * 8 * QP;  // this warp's Q^T
+    const uint32_t sL = tc::smem_u32(Ls), sM = tc::smem_u32(Ms), sMt = tc::smem_u32(Mt), sQ = tc::smem_u32(Qt);
     if (wq < 4) {
         // 16 x 16 diagonal block wq: its two 8 x 8 diagonal blocks (one column per lane) ...
         const int B = 16 * wq;
@@ -221,10 +258,12 @@ __device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, floa
                 float acc = (r == cc) ? 1.f : 0.f;
 #pragma unroll
                 for (int j = 0; j < r; ++j) acc = fmaf(-Ls[(base + r) * LP + base + j], x[j], acc);
-                x[r] = (r < cc) ? 0.f : acc;
+                x[r] = (r < cc) ? 0.f : tc::round_tf32(acc);
             }
 #pragma unroll
             for (int r = 0; r < 8; ++r) Ms[(base + r) * LP + base + cc] = x[r];
+            *reinterpret_cast<float4 *>(Mt + tc::sw128_f32(base + cc, base, C)) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4 *>(Mt + tc::sw128_f32(base + cc, base + 4, C)) = make_float4(x[4], x[5], x[6], x[7]);
         }
         __syncwarp();
         // ... then its lower-left 8 x 8: -M_bb (L_ba M_aa), two entries per lane
@@ -234,21 +273,21 @@ __device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, floa
             const int i = (ln >> 3) + 4 * h, j = ln & 7;
             float acc = 0.f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k >= j) acc = fmaf(Ls[(B + 8 + i) * LP + B + k], Ms[(B + k) * LP + B + j], acc);
+            for (int k = 0; k < 8; ++k) acc = fmaf(Ls[(B + 8 + i) * LP + B + k], Ms[(B + k) * LP + B + j], acc);
             q[h] = acc;
         }
-        Qw[ln] = q[0];
-        Qw[ln + 32] = q[1];
+        Qt[ln] = q[0];
+        Qt[ln + 32] = q[1];
         __syncwarp();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = (ln >> 3) + 4 * h, j = ln & 7;
             float acc = 0.f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k <= i) acc = fmaf(Ms[(B + 8 + i) * LP + B + 8 + k], Qw[k * 8 + j], acc);
-            Ms[(B + 8 + i) * LP + B + j] = -acc;
+            for (int k = 0; k < 8; ++k) acc = fmaf(Ms[(B + 8 + i) * LP + B + 8 + k], Qt[k * 8 + j], acc);
+            const float v = tc::round_tf32(-acc);
+            Ms[(B + 8 + i) * LP + B + j] = v;
+            *reinterpret_cast<float *>(Mt + tc::sw128_f32(B + j, B + 8 + i, C)) = v;
         }
     }
     tc::bar_sync(BAR_PREP, NP);
@@ -256,15 +295,26 @@ __device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, floa
         // 16 -> 32: M_10 and M_32 (16 x 16), one 8-column half per warp
         const int bj = 2 * (wq >> 1), bi = bj + 1, c0 = 16 * bj + 8 * (wq & 1);
         float q[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], b[2];
         // M_jj[k][c0..] vanishes for the first k-step when c0 is the upper half
-        if ((wq & 1) == 0) mma1(q, Ls, LP, 16 * bi, 16 * bj, Ms, LP, 16 * bj, c0, ln);
-        mma1(q, Ls, LP, 16 * bi, 16 * bj + 8, Ms, LP, 16 * bj + 8, c0, ln);
-        store_frag(Qw, 8, 0, 0, q, 1.f, ln);
+        if ((wq & 1) == 0) {
+            frag_a(a, sL, 16 * bi, 16 * bj, ln);
+            frag_b_sw(b, sMt, 16 * bj, c0, ln);
+            mma16x8x8(q, a, b);
+        }
+        frag_a(a, sL, 16 * bi, 16 * bj + 8, ln);
+        frag_b_sw(b, sMt, 16 * bj + 8, c0, ln);
+        mma16x8x8(q, a, b);
+        store_q(Qt, 0, q, ln);
         __syncwarp();
         float r[4] = {0.f, 0.f, 0.f, 0.f};
-        mma1(r, Ms, LP, 16 * bi, 16 * bi, Qw, 8, 0, 0, ln);
-        mma1(r, Ms, LP, 16 * bi, 16 * bi + 8, Qw, 8, 8, 0, ln);
-        store_frag(Ms, LP, 16 * bi, c0, r, -1.f, ln);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            frag_a(a, sM, 16 * bi, 16 * bi + 8 * ks, ln);
+            frag_b_q(b, sQ, 8 * ks, ln);
+            mma16x8x8(r, a, b);
+        }
+        store_m(Ms, Mt, 16 * bi, c0, r, ln);
     }
     tc::bar_sync(BAR_PREP, NP);
     {
@@ -273,16 +323,26 @@ __device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, floa
         // (M[k][strip] = 0 for k < 8 cs), then -M[rows, 32..64) Q.
         const int rb = wq >> 2, cs = wq & 3, c0 = 8 * cs;
         float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], b[2];
         for (int ks = cs; ks < 4; ++ks) {
-            mma1(q0, Ls, LP, 32, 8 * ks, Ms, LP, 8 * ks, c0, ln);
-            if (rb) mma1(q1, Ls, LP, 48, 8 * ks, Ms, LP, 8 * ks, c0, ln);
+            frag_b_sw(b, sMt, 8 * ks, c0, ln);
+            frag_a(a, sL, 32, 8 * ks, ln);
+            mma16x8x8(q0, a, b);
+            if (rb) {
+                frag_a(a, sL, 48, 8 * ks, ln);
+                mma16x8x8(q1, a, b);
+            }
         }
-        store_frag(Qw, 8, 0, 0, q0, 1.f, ln);
-        if (rb) store_frag(Qw, 8, 16, 0, q1, 1.f, ln);
+        store_q(Qt, 0, q0, ln);
+        if (rb) store_q(Qt, 16, q1, ln);
         __syncwarp();
         float r[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int ks = 0; ks < 2 * (rb + 1); ++ks) mma1(r, Ms, LP, 32 + 16 * rb, 32 + 8 * ks, Qw, 8, 8 * ks, 0, ln);
-        store_frag(Ms, LP, 32 + 16 * rb, c0, r, -1.f, ln);
+        for (int ks = 0; ks < 2 * (rb + 1); ++ks) {
+            frag_a(a, sM, 32 + 16 * rb, 32 + 8 * ks, ln);
+            frag_b_q(b, sQ, 8 * ks, ln);
+            mma16x8x8(r, a, b);
+        }
+        store_m(Ms, Mt, 32 + 16 * rb, c0, r, ln);
     }
     tc::bar_sync(BAR_PREP, NP);
 }
@@ -356,7 +416,8 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
     uint32_t *tmem_base_sh = reinterpret_cast<uint32_t *>(sm + SM_MISC + 16);
     float *Ls = reinterpret_cast<float *>(sm + SM_L);
     float *Ms = reinterpret_cast<float *>(sm + SM_M);
-    float *Qs = reinterpret_cast<float *>(sm + SM_MT);  // inverse scratch; (D M)^T is written after it
+    float *Qs = reinterpret_cast<float *>(sm + SM_Q);
+    uint8_t *Mt = sm + SM_MT;  // M^T during the inverse, then (D M)^T in place
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Dims dm = a.dm;
@@ -373,6 +434,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         tc::fence_mbar_init();
     }
     for (int i = tid; i < C * LP; i += NT) Ms[i] = 0.f;  // the upper blocks of M stay zero
+    for (int i = tid; i < C * C; i += NT) reinterpret_cast<float *>(Mt)[i] = 0.f;
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_base_sh), TM_COLS);
     tc::fence_before();
     __syncthreads();
@@ -565,15 +627,18 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         const float et = __expf(gt_t - gm);
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            Ls[t * LP + j0 + j] = (j0 + j < t) ? G.fb[j0 + j] * et * gr[j] : 0.f;
+                            gr[j] = (j0 + j < t) ? tc::round_tf32(G.fb[j0 + j] * et * gr[j]) : 0.f;
                     } else {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            Ls[t * LP + j0 + j] = (j0 + j < t) ? G.b[j0 + j] * __expf(gt_t - G.g[j0 + j]) * gr[j] : 0.f;
+                            gr[j] = (j0 + j < t) ? tc::round_tf32(G.b[j0 + j] * __expf(gt_t - G.g[j0 + j]) * gr[j]) : 0.f;
                     }
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4 *>(Ls + t * LP + j0 + j) = make_float4(gr[j], gr[j + 1], gr[j + 2], gr[j + 3]);
                 }
                 tc::bar_sync(BAR_PREP, NP);
-                unit_lower_inverse(Ls, Ms, Qs, pt);
+                unit_lower_inverse(Ls, Ms, Mt, Qs, pt);
                 // K^T into tensor memory (A of U~): lane i holds K[j][i], this warp j = 32hh .. +31
                 {
                     float kt[32];
@@ -582,15 +647,14 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         kt[j] = *reinterpret_cast<const float *>(sm + SM_K32 + tc::sw128_f32(hh * 32 + j, li, C));
                     tc::tmem_st32(my + TM_G + hh * 32, kt);
                 }
-                // B of U~: element (t, j) = dc_j M[j][t]; consecutive lanes take consecutive t
+                // B of U~: element (t, j) = dc_j M[j][t], scaled in place in the M^T tile
 #pragma unroll
                 for (int e = pt; e < C * C / 4; e += NP) {
                     const int t = e & (C - 1), j = (e >> 6) * 4;
-                    *reinterpret_cast<float4 *>(sm + SM_MT + tc::sw128_f32(t, j, C)) =
-                        make_float4(tc::round_tf32(G.dc[j] * Ms[j * LP + t]),
-                                    tc::round_tf32(G.dc[j + 1] * Ms[(j + 1) * LP + t]),
-                                    tc::round_tf32(G.dc[j + 2] * Ms[(j + 2) * LP + t]),
-                                    tc::round_tf32(G.dc[j + 3] * Ms[(j + 3) * LP + t]));
+                    float4 *p = reinterpret_cast<float4 *>(Mt + tc::sw128_f32(t, j, C));
+                    const float4 mv = *p;
+                    *p = make_float4(tc::round_tf32(G.dc[j] * mv.x), tc::round_tf32(G.dc[j + 1] * mv.y),
+                                     tc::round_tf32(G.dc[j + 2] * mv.z), tc::round_tf32(G.dc[j + 3] * mv.w));
                 }
                 tc::fence_async_smem();
                 tc::fence_before();

@@ -37,8 +37,10 @@ def test_full_size(name):
     for key in ("T", "S", "S_final", "S_prefix", "o"):
         assert torch.isfinite(out[key]).all(), key
     items, chains = _sample(wl, 8, 4, seed=sum(map(ord, name)))
-    check_pairs(wl, out, items, tol)
-    check_request(wl, out, chains, tol)
+    et, es = check_pairs(wl, out, items, tol)
+    r = check_request(wl, out, chains, tol)
+    print("\nparity %s: T %.2e  S %.2e  S_final %.2e  S_prefix %.2e  seam o %.2e  (tol %.0e)"
+          % (name, et, es, r["final"], r["prefix"], r["o"], tol))
     if name == "stress_gdn":
         # the slow gate keeps T_C well away from zero, so composition matters
         assert out["T"].abs().amax().item() > 1e-5

@@ -31,8 +31,10 @@ def test_small_workloads(name):
     wl = W.make(name, device="cuda")
     out = run_pipeline(wl)
     tol = tol_of(wl.desc)
-    check_pairs(wl, out, _all_items(wl), tol)
+    et, es = check_pairs(wl, out, _all_items(wl), tol)
     res = check_request(wl, out, _all_chains(wl), tol)
+    print("\nparity %s: T %.2e  S %.2e  S_final %.2e  S_prefix %.2e  seam o %.2e  (tol %.0e)"
+          % (name, et, es, res["final"], res["prefix"], res["o"], tol))
     if name == "stress_tiny":
         # the composition term is far from negligible here
         T = out["T"].cpu().numpy()
