@@ -53,6 +53,23 @@ def _peaks():
                 source="fallback")
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one build
+# launch on the 1-layer case, and the SHA-256 of the kernel source they were
+# taken on; reported only while the source is unchanged.
+BUILD_TRAFFIC = {"source_sha256": "153a7a493e5a0b82da1a758006ec2c55b786914057c7d8aeef890b1d352a379d",
+                 "bytes_per_layer": 1735469000 + 784953088}
+
+
+def _build_traffic(n_layers):
+    import hashlib
+    src = os.path.join(ROOT, "linear_attn_state_chunked_gb300", "csrc", "build_tc.cu")
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if BUILD_TRAFFIC["source_sha256"] != sha or BUILD_TRAFFIC["bytes_per_layer"] is None:
+        return None
+    return BUILD_TRAFFIC["bytes_per_layer"] * n_layers
+
+
 def _config():
     from linear_attn_state_chunked_gb300 import workloads as W
     d = W.describe(WORKLOAD)
@@ -286,14 +303,22 @@ def run_gpu(args):
     build_mtok = body_tokens * L / (build_ms * 1e-3) / 1e6
     comp_segs = n_ord * L / (comp_ms * 1e-3)
 
-    # roofline of the dominant kernel (the build): algorithmic flops of the
-    # recurrence, 4 d_k (d_k + d_v) per body token and head, on CUDA cores
+    # roofline of the dominant kernel (the build, a tf32 tensor-core
+    # contraction): algorithmic flops of the recurrence, 4 d_k (d_k + d_v) =
+    # 131,072 per body token and head, against the dense tf32 peak taken as
+    # the measured sustained bf16 peak x the nominal tf32/bf16 ratio 1.1/2.25
+    # (the build runs ~70 ms inside a longer step).  DRAM traffic per launch:
+    # from the ncu capture of the 1-layer case scaled by the layer count
+    # (traffic grows in proportion), or null if not supplied.
     flops = body_tokens * L * H * 4.0 * D * (2 * D)
     achieved = flops / (build_ms * 1e-3) / 1e12
-    alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-    roof = {"kernel": "build_rec_kernel", "bound": "alu", "achieved": achieved,
-            "peak": alu_peak, "unit": "TFLOP/s", "frac": achieved / alu_peak, "traffic": None,
-            "peak_source": "152 SMs x 128 fp32 lanes x 2 flop x %d MHz" % peaks["sm_max_mhz"]}
+    tf32_peak = peaks["bf16_sustained"] * 1.1 / 2.25
+    traffic = _build_traffic(L)
+    roof = {"kernel": "build_tc_kernel", "bound": "tensor", "achieved": achieved,
+            "peak": tf32_peak, "unit": "TFLOP/s", "frac": achieved / tf32_peak, "traffic": traffic,
+            "peak_source": "%s sustained bf16 %.1f TFLOP/s x 1.1/2.25 (tf32)"
+                           % (peaks["source"], peaks["bf16_sustained"]),
+            "algorithmic": "131072 flop per body token-head x %d token-heads" % (body_tokens * L * H)}
     # compose + seams: HBM-bound; algorithmic bytes = pairs read + seam inputs + outputs
     pair_bytes = L * n_ord * H * (2 * D * D) * 4
     seam_tok = int(sum(min(w, int(wl.lengths[s])) for s in wl.order))
@@ -343,7 +368,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        heads, segs = 32, 30
+        heads, segs = 32, 120
         dt, lt = oracle_sample(wl, heads, segs)
         cpu = {"value": lt / dt / 1e6, "unit": UNIT, "cores": _cores(), "kind": "oracle",
                "sample": "fp64 oracle on layer 0, all %d heads, first %d segments of the request "
@@ -354,7 +379,7 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "tf32", "data": "synthetic",
             "config": dict(_config(), **({"layers": L, "subset": "first %d layers only" % L}
                                          if args.layers else {})),
             "components": {
