@@ -6,19 +6,27 @@
 // running state advances entry by entry as S <- T_C S + S(C|0), each segment's
 // seam tokens first re-run under the running state, emitting their outputs.
 //
-// One CTA per (layer, head) chain.  Per request entry e:
-//   * T_C and S(C|0) of the entry stream into shared memory by TMA
-//     (128-byte swizzle, the tensor core's operand layout) and D = T_C S runs
-//     as 16 tf32 MMAs (A = T_C, B = S^T from shared memory, D in tensor
-//     memory), both driven by thread 0;
-//   * the 8 warps run the seam column-parallel (a pair of threads owns column
-//     j of S in registers, so u_j = k.S[:, j] needs one shuffle), write the
-//     tf32-rounded state as the MMA's B operand, and after the MMA form
-//     S_new = D + S(C|0) row-parallel (tensor-memory lanes), transposing it
-//     through shared memory back to columns for the next seam.
-// The next entry's T_C loads while this entry's epilogue and the next seam
-// run; its S(C|0) loads while the seam and the MMA run.  The next entry's
-// seam tokens (with their conv warm-up) are staged while the MMA runs.
+// One CTA per (layer, head) chain.  The running state lives in tensor memory
+// transposed, X = S^T (lane j holds column j of S), in fp32, with its tf32
+// split X = Xhi + Xlo beside it for use as an MMA operand.  Per request entry:
+//
+//   seam (w <= 8 tokens, one chunk of the WY form of the recurrence; with
+//   g_t = sum_{r<=t} log alpha_r, Gamma_t = e^{g_t}):
+//     [u_t | z_t]    = S^T [k_t | q_t]                 tensor core, 3xTF32
+//     U              = (I + L)^{-1} (V - diag(Gamma) K S)   per column, CUDA cores
+//                      L_ts = beta_s e^{g_t - g_s} k_t.k_s  (s < t)
+//     o_t            = Gamma_t z_t + sum_{s<=t} e^{g_t - g_s} beta_s (q_t.k_s) U_s
+//     S             <- Gamma_w S + K^T diag(beta_s e^{g_w - g_s}) U
+//                      (X rescaled on CUDA cores, then one K = 8 MMA, 3xTF32)
+//   body:  S <- T_C S + S(C|0)     (tensor core: A = Xhi from tensor memory,
+//                                   B = T_C rows from shared memory)
+//
+// Warp roles: warps 0-3 own the state (thread j = tensor-memory lane j =
+// column j of S); warps 4-7 stage each entry's seam ahead of time (conv warm-up
+// across the segment boundary, L2 normalisation, the seam's 8 x 8 Gram and
+// triangular inverse, all independent of the state) into double buffers;
+// warp 8 issues the MMAs and the T_C copies.  T_C and S(C|0) of the next
+// entry stream in by TMA as soon as their buffers free up.
 #include <cstring>
 
 #include "common.cuh"
@@ -30,30 +38,62 @@ namespace hypic {
 namespace {
 
 constexpr int D = 128;
-constexpr int WMAX = 8;     // seam window served by this kernel
-constexpr int NMAIN = 256;  // 8 warps: seams, epilogue, outputs; thread 0 also drives TMA and the MMA
-constexpr int NT = NMAIN;
-constexpr int BAR_MAIN = 1;
-constexpr long long kWaitCycles = 4000000000LL;
+constexpr int WMAX = 8;       // seam window served by this kernel
+constexpr int HIST = 3;       // conv history rows (taps - 1, taps <= 4)
+constexpr int NS = 128;       // state threads (warps 0-3)
+constexpr int NG = 128;       // staging threads (warps 4-7)
+constexpr int WARP_MMA = 8;   // MMA issue and T_C copies (lane 0)
+constexpr int NT = NS + NG + 32;
+constexpr int BAR_STATE = 1, BAR_STAGE = 2;
+constexpr long long kWaitCycles = 4000000000LL;  // about two seconds
 
-constexpr uint32_t SM_T = 0;           // T_C   [128][128] fp32, sw128 (A)
-constexpr uint32_t SM_SC = 65536;      // S(C|0) [128][128] fp32, sw128
-constexpr uint32_t SM_ST = 131072;     // S^T  [128][128] fp32, sw128 (B; also the transpose buffer)
-constexpr int TOK_F = 3 * D + 4;       // q, k, v, alpha, beta (+pad) per token
-constexpr uint32_t SM_TOK = 196608;    // [WMAX][TOK_F] fp32: the staged seam tokens
-constexpr int HIST = 3;                // conv history rows (taps - 1, taps <= 4)
-constexpr int RAW_ROWS = HIST + WMAX;  // per tensor: history rows, then the seam rows
-constexpr uint32_t RAW_T = RAW_ROWS * D * 2;           // bytes per tensor (bf16)
-constexpr uint32_t SM_RAW = SM_TOK + WMAX * TOK_F * 4;  // 2 buffers x {q, k, v} raw rows (TMA)
-constexpr uint32_t SM_RED = SM_RAW + 2 * 3 * RAW_T;     // [8 warps][WMAX][2] partial sums
-constexpr uint32_t SM_BAR = SM_RED + 8 * WMAX * 2 * 4;
-constexpr uint32_t SM_MISC = SM_BAR + 8 * 8;
+// tensor-memory columns
+constexpr uint32_t TM_X = 0;      // S^T, fp32
+constexpr uint32_t TM_XHI = 128;  // tf32(S^T)
+constexpr uint32_t TM_XLO = 256;  // tf32(S^T - Xhi)
+constexpr uint32_t TM_Y = 384;    // T_C S (transposed); during the seam: [u | z] and W
+constexpr uint32_t TM_D2 = TM_Y;       // 16 columns: u_t (t < 8), z_t
+constexpr uint32_t TM_W = TM_Y + 32;   // 24 columns: Whi, Wlo, Whi
+constexpr uint32_t TM_COLS = 512;
+
+// shared memory
+constexpr uint32_t SM_T = 0;         // T_C    [128][128] fp32, sw128 (B of the body MMA)
+constexpr uint32_t SM_SC = 65536;    // S(C|0) [128][128] fp32, sw128
+constexpr uint32_t SM_BUF = 131072;  // 2 x staged seam
+constexpr uint32_t BF_KQH = 0;       //   [k_t ; q_t] tf32 hi [16][128], sw128 (B of the seam MMA)
+constexpr uint32_t BF_KQL = 8192;    //   lo parts
+constexpr uint32_t BF_KP = 16384;    //   K^T [128][32] sw128: columns t, 8 + t = hi(k_t), 16 + t = lo(k_t)
+constexpr uint32_t BF_V = 32768;     //   v_t [8][128] fp32
+constexpr uint32_t BF_SMALL = 36864; //   M [8][8], AQ [8][8], Gamma [8], d [8], Gamma_w, beta [8], g [8]
+constexpr uint32_t BUF_BYTES = 37888;
+constexpr int SMALL_M = 0, SMALL_AQ = 64, SMALL_G = 128, SMALL_D = 136, SMALL_GL = 144, SMALL_B = 152,
+              SMALL_LG = 160;
+constexpr uint32_t RAW_T = (HIST + WMAX) * D * 2;           // raw rows per tensor (bf16)
+constexpr uint32_t SM_RAW = SM_BUF + 2 * BUF_BYTES;         // 2 x {q, k, v} raw rows (TMA)
+constexpr uint32_t SM_RED = SM_RAW + 2 * 3 * RAW_T;         // [4 warps][8 tokens][2] + dots [64]
+constexpr uint32_t SM_BAR = SM_RED + (4 * WMAX * 2 + 64) * 4;
+constexpr uint32_t SM_MISC = SM_BAR + 16 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
 static_assert(SMEM_DYN <= 232448, "shared memory budget");
+static_assert(SM_BUF % 1024 == 0 && BUF_BYTES % 1024 == 0 && BF_KP % 1024 == 0 && BF_KQL % 1024 == 0,
+              "operand tile alignment");
 static_assert(SM_RAW % 128 == 0 && RAW_T % 128 == 0 && (HIST * D * 2) % 128 == 0, "TMA alignment");
 
-enum { B_FULLT = 0, B_FULLSC, B_MMADONE, B_FULLR0, B_FULLR1, B_COUNT };
+enum {
+    B_FULLT = 0,   // T_C of the entry landed                     TMA -> mma
+    B_FULLSC,      // S(C|0) of the entry landed                  TMA -> state
+    B_FULLR0,      // [2] raw seam rows landed                    TMA -> staging
+    B_STAGED0 = B_FULLR0 + 2,  // [2] seam staged                 staging -> mma
+    B_BUFFREE0 = B_STAGED0 + 2,  // [2] staged buffer consumed    mma -> staging
+    B_XREADY = B_BUFFREE0 + 2,   // X, Xhi, Xlo hold the state before the entry   state -> mma
+    B_SEAMDONE,    // [u | z] in tensor memory                    mma -> state
+    B_WREADY,      // W written, X rescaled                       state -> mma
+    B_UPDDONE,     // seam update of X done                       mma -> state
+    B_XHIREADY,    // Xhi of the state after the seam             state -> mma
+    B_BODYDONE,    // T_C S in tensor memory                      mma -> state
+    B_COUNT
+};
 
 __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
 {
@@ -83,105 +123,29 @@ __device__ __forceinline__ bool hist_by_tma(const SegTable &tab, int e)
     return tab.off[sp + 1] - tab.off[sp] >= HIST;
 }
 
-// Stage seam tokens t < sw of request entry e from the raw rows the TMA
-// brought in (the 256 main threads; thread = channel c of tokens
-// th*WMAX/2 .. th*WMAX/2 + WMAX/2 - 1): q, k, v (convolved along the request
-// stream when CK > 0, then q and k L2-normalised per token).  alpha and beta
-// come in registers from threads 0 .. 2*WMAX-1 (gab: thread t < WMAX holds
-// alpha of token t, thread WMAX + t beta).
-template <int CK>
-__device__ void stage_seam(float *tok, float *red, const uint8_t *raw, const Dims &dm, const TokPtrs &tk,
-                           const SegTable &tab, int l, int h, int e, int sw, int tid, float gab)
+__device__ __forceinline__ int seam_len(const SegTable &tab, int e, int w)
 {
-    constexpr int TH = WMAX / 2;
-    constexpr int NL = CK > 0 ? CK : 1;
-    const int c = tid & (D - 1), th = tid >> 7;
-    const bool htma = CK > 0 && hist_by_tma(tab, e);
-    float wq[NL], wk[NL], wv[NL];
-    if (CK > 0) {
-        const float *w0 = tk.conv_w + (((size_t)l * 3 + 0) * dm.H + h) * D * CK + c * CK;
-#pragma unroll
-        for (int j = 0; j < NL; ++j) {
-            wq[j] = __ldg(w0 + j);
-            wk[j] = __ldg(w0 + (size_t)dm.H * D * CK + j);
-            wv[j] = __ldg(w0 + 2 * (size_t)dm.H * D * CK + j);
-        }
-    }
-    auto raw_at = [&](int tensor, int row) {
-        const uint16_t u = *reinterpret_cast<const uint16_t *>(raw + tensor * RAW_T + (row * D + c) * 2);
-        return __uint_as_float(static_cast<uint32_t>(u) << 16);
-    };
-    float sq[TH], sk[TH];
-#pragma unroll
-    for (int tt = 0; tt < TH; ++tt) {
-        const int t = th * TH + tt;
-        sq[tt] = sk[tt] = 0.f;
-        if (t >= sw) continue;
-        float qv = 0.f, kv = 0.f, vv = 0.f;
-#pragma unroll
-        for (int lag = 0; lag < NL; ++lag) {
-            float rq, rk, rv;
-            if (t - lag >= 0 || htma) {
-                const int row = HIST + t - lag;
-                rq = raw_at(0, row);
-                rk = raw_at(1, row);
-                rv = raw_at(2, row);
-            } else {
-                // history across short segments or before the request start
-                const int32_t tb = stream_back(tab, e, t, lag);
-                rq = rk = rv = 0.f;
-                if (tb >= 0) {
-                    const size_t ix = tok_index(dm, tk.N, l, tb, h, c);
-                    rq = __bfloat162float(static_cast<const __nv_bfloat16 *>(tk.q)[ix]);
-                    rk = __bfloat162float(static_cast<const __nv_bfloat16 *>(tk.k)[ix]);
-                    rv = __bfloat162float(static_cast<const __nv_bfloat16 *>(tk.v)[ix]);
-                }
-            }
-            if (CK == 0) {
-                qv = rq; kv = rk; vv = rv;
-            } else {
-                qv = fmaf(wq[lag], rq, qv);
-                kv = fmaf(wk[lag], rk, kv);
-                vv = fmaf(wv[lag], rv, vv);
-            }
-        }
-        float *row = tok + t * TOK_F;
-        row[c] = qv;
-        row[D + c] = kv;
-        row[2 * D + c] = vv;
-        sq[tt] = qv * qv;
-        sk[tt] = kv * kv;
-    }
-    if (tid < 2 * WMAX && (tid & (WMAX - 1)) < sw) tok[(tid & (WMAX - 1)) * TOK_F + 3 * D + (tid >= WMAX)] = gab;
-    if (CK > 0) {
-        const int warp = tid >> 5, lane = tid & 31;
-#pragma unroll
-        for (int tt = 0; tt < TH; ++tt) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sq[tt] += __shfl_xor_sync(0xffffffffu, sq[tt], o);
-                sk[tt] += __shfl_xor_sync(0xffffffffu, sk[tt], o);
-            }
-            if (lane == 0) {
-                red[(warp * WMAX + tt) * 2] = sq[tt];
-                red[(warp * WMAX + tt) * 2 + 1] = sk[tt];
-            }
-        }
-        tc::bar_sync(BAR_MAIN, NMAIN);
-#pragma unroll
-        for (int tt = 0; tt < TH; ++tt) {
-            const int t = th * TH + tt;
-            if (t >= sw) continue;
-            float a = 0.f, b = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                a += red[((4 * th + w) * WMAX + tt) * 2];
-                b += red[((4 * th + w) * WMAX + tt) * 2 + 1];
-            }
-            float *row = tok + t * TOK_F;
-            row[c] *= 1.f / sqrtf(a + kL2Eps);
-            row[D + c] *= 1.f / sqrtf(b + kL2Eps);
-        }
+    const int s = tab.perm[e];
+    return min(w, tab.off[s + 1] - tab.off[s]);
+}
+
+// Dot product index p (0..63) of the staged seam: 28 k_t.k_s (s < t), then
+// 36 q_t.k_s (s <= t).  Rows of the [k ; q] tile: k_t in row t, q_t in row 8 + t.
+__device__ __forceinline__ void dot_rows(int p, int &ra, int &rb, int &t, int &s)
+{
+    if (p < 28) {
+        t = 1;
+        while (p >= t) { p -= t; ++t; }
+        s = p;
+        ra = t;
+        rb = s;
+    } else {
+        p -= 28;
+        t = 0;
+        while (p > t) { p -= t + 1; ++t; }
+        s = p;
+        ra = WMAX + t;
+        rb = s;
     }
 }
 
@@ -197,7 +161,6 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
     auto bar = [&](int i) { return s_base + SM_BAR + 8u * i; };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM_MISC);
     uint32_t *tmem_base_sh = reinterpret_cast<uint32_t *>(sm + SM_MISC + 16);
-    float *red = reinterpret_cast<float *>(sm + SM_RED);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Dims dm = a.dm;
@@ -210,230 +173,478 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
         for (int i = 0; i < B_COUNT; ++i) tc::mbar_init(bar(i), 1);
         tc::fence_mbar_init();
     }
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_base_sh), 128);
+    // K^T tiles: columns 24..31 stay zero
+    for (int i = tid; i < 2 * D * 32; i += NT)
+        reinterpret_cast<float *>(sm + SM_BUF + (i >> 12) * BUF_BYTES + BF_KP)[i & 4095] = 0.f;
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_base_sh), TM_COLS);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tb = *tmem_base_sh;
 
-    {
-        // ------------------------------------------------ main warps: seams, epilogue, outputs
-        // Seam / state layout: the thread pair (tid, tid ^ 1) owns column
-        // j = tid / 2; thread hf = tid % 2 holds rows 8m + 4hf .. 8m + 4hf + 3
-        // (m = 0..15) in x[4m .. 4m + 3], so a warp's 16-byte reads of k and q
-        // hit two adjacent chunks (no bank conflict); the pair's partial dot
-        // products meet by a shuffle.  Epilogue layout: tensor-memory lane
-        // i = 32 (warp % 4) + lane, columns 64 (warp / 4) .. + 63.
-        constexpr int HR = D / 2;
-        const int j = tid >> 1, hf = tid & 1;
-        auto RW = [&](int r) { return 8 * (r >> 2) + 4 * hf + (r & 3); };
-        const int lane_i = 32 * (warp & 3) + lane, cbase = 64 * (warp >> 2);
-        const uint32_t my = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const size_t st_base = ((size_t)l * dm.H + h) * D * D;
-        float *toks = reinterpret_cast<float *>(sm + SM_TOK);
-        // thread 0 drives the copies and the MMA
-        auto pair_row = [&](int e) {
-            return (int)((((size_t)l * tab.n_seg + tab.perm[e]) * dm.H + h) * D);
-        };
-        auto load_T = [&](int e) {
-            tc::mbar_arrive_expect_tx(bar(B_FULLT), D * D * 4);
+    auto pair_row = [&](int e) { return (int)((((size_t)l * tab.n_seg + tab.perm[e]) * dm.H + h) * D); };
+    auto load_T = [&](int e) {
+        tc::mbar_arrive_expect_tx(bar(B_FULLT), D * D * 4);
 #pragma unroll
-            for (int at = 0; at < 4; ++at)
-                tc::tma_load_2d(s_base + SM_T + at * 16384, &tmT, 32 * at, pair_row(e), bar(B_FULLT));
-        };
-        auto load_SC = [&](int e) {
-            tc::mbar_arrive_expect_tx(bar(B_FULLSC), D * D * 4);
+        for (int at = 0; at < 4; ++at)
+            tc::tma_load_2d(s_base + SM_T + at * 16384, &tmT, 32 * at, pair_row(e), bar(B_FULLT));
+    };
+    auto load_SC = [&](int e) {
+        tc::mbar_arrive_expect_tx(bar(B_FULLSC), D * D * 4);
 #pragma unroll
-            for (int at = 0; at < 4; ++at)
-                tc::tma_load_2d(s_base + SM_SC + at * 16384, &tmS, 32 * at, pair_row(e), bar(B_FULLSC));
-        };
-        // raw seam rows of entry e (and the conv history rows when they are the
-        // previous entry's last tokens) into raw buffer e & 1
-        auto load_raw = [&](int e) {
-            const int s = tab.perm[e];
-            const uint32_t fb = bar(B_FULLR0 + (e & 1));
-            const int sw = min(w, tab.off[s + 1] - tab.off[s]);
-            if (sw == 0) {
-                tc::mbar_arrive(fb);
-                return;
-            }
-            const bool htma = CK > 0 && hist_by_tma(tab, e);
-            tc::mbar_arrive_expect_tx(fb, 3 * WMAX * D * 2 + (htma ? 3 * HIST * D * 2 : 0));
-            const uint32_t rb = s_base + SM_RAW + (e & 1) * 3 * RAW_T;
-#pragma unroll
-            for (int x3 = 0; x3 < 3; ++x3) {
-                tc::tma_load_4d(rb + x3 * RAW_T + HIST * D * 2, &tmX.rows8[x3], 0, h, tab.off[s], l, fb);
-                if (htma)
-                    tc::tma_load_4d(rb + x3 * RAW_T, &tmX.rows3[x3], 0, h, tab.off[tab.perm[e - 1] + 1] - HIST, l, fb);
-            }
-        };
-        auto load_gates = [&](int e) {  // threads 0 .. 2*WMAX-1: alpha / beta of token tid % WMAX
-            float v = 0.f;
-            const int s = tab.perm[e];
-            const int t = tid & (WMAX - 1);
-            if (tid < 2 * WMAX && t < min(w, tab.off[s + 1] - tab.off[s])) {
-                const size_t gi = gate_index(dm, a.tok.N, l, tab.off[s] + t, h);
-                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(tid < WMAX ? a.tok.alpha : a.tok.beta);
-                v = __bfloat162float(src[gi]);
-            }
-            return v;
-        };
-        auto stage = [&](int e, float gab) -> bool {
-            bool wr = true;
-            if (tid == 0) wr = wait_bar(bar(B_FULLR0 + (e & 1)), (e >> 1) & 1, abort_flag);
-            if (!tc::bar_and(BAR_MAIN, NMAIN, wr)) return false;
-            const int s = tab.perm[e];
-            stage_seam<CK>(toks, red, sm + SM_RAW + (e & 1) * 3 * RAW_T, dm, a.tok, tab, l, h, e,
-                           min(w, tab.off[s + 1] - tab.off[s]), tid, gab);
-            return true;
-        };
-        int armed = 0;  // entries whose copies were issued
-        if (tid == 0 && n_ent > 0) {
-            load_T(0);
-            load_SC(0);
-            armed = 1;
-            if (w > 0) load_raw(0);
+        for (int at = 0; at < 4; ++at)
+            tc::tma_load_2d(s_base + SM_SC + at * 16384, &tmS, 32 * at, pair_row(e), bar(B_FULLSC));
+    };
+    // raw seam rows of entry e (and the conv history rows when they are the
+    // previous entry's last tokens) into raw buffer e & 1
+    auto load_raw = [&](int e) {
+        const int s = tab.perm[e];
+        const uint32_t fb = bar(B_FULLR0 + (e & 1));
+        const int sw = seam_len(tab, e, w);
+        if (sw == 0) {
+            tc::mbar_arrive(fb);
+            return;
         }
-        float x[HR];
+        const bool htma = CK > 0 && hist_by_tma(tab, e);
+        tc::mbar_arrive_expect_tx(fb, 3 * WMAX * D * 2 + (htma ? 3 * HIST * D * 2 : 0));
+        const uint32_t rb = s_base + SM_RAW + (e & 1) * 3 * RAW_T;
 #pragma unroll
-        for (int r = 0; r < HR; ++r) x[r] = a.S_init ? a.S_init[st_base + (size_t)RW(r) * D + j] : 0.f;
+        for (int x3 = 0; x3 < 3; ++x3) {
+            tc::tma_load_4d(rb + x3 * RAW_T + HIST * D * 2, &tmX.rows8[x3], 0, h, tab.off[s], l, fb);
+            if (htma)
+                tc::tma_load_4d(rb + x3 * RAW_T, &tmX.rows3[x3], 0, h, tab.off[tab.perm[e - 1] + 1] - HIST, l, fb);
+        }
+    };
+
+    const size_t st_base = ((size_t)l * dm.H + h) * D * D;
+    if (warp < 4) {
+        // ================================================= state warps
+        const int j = tid;
+        const uint32_t my = tb + (static_cast<uint32_t>(warp * 32) << 16);
+        int sc_armed = 0;  // S(C|0) copies issued
+        if (tid == 0 && n_ent > 0) {
+            load_SC(0);
+            sc_armed = 1;
+        }
+        // X = S_init^T (or 0); S_prefix[0] = S_init
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float xv[32], hv[32], lv[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const float x = a.S_init ? a.S_init[st_base + (size_t)(c0 + q) * D + j] : 0.f;
+                xv[q] = x;
+                hv[q] = tc::round_tf32(x);
+                lv[q] = tc::round_tf32(x - hv[q]);
+                if (n_ent > 0 && a.S_prefix) a.S_prefix[(((size_t)l * n_ent) * dm.H + h) * D * D + (size_t)(c0 + q) * D + j] = x;
+                if (n_ent == 0) a.S_final[st_base + (size_t)(c0 + q) * D + j] = x;
+            }
+            tc::tmem_st32(my + TM_X + c0, xv);
+            tc::tmem_st32(my + TM_XHI + c0, hv);
+            tc::tmem_st32(my + TM_XLO + c0, lv);
+        }
+        tc::fence_before();
+        tc::bar_sync(BAR_STATE, NS);
+        if (tid == 0 && n_ent > 0) tc::mbar_arrive(bar(B_XREADY));
         bool ok = true;
-        if (w > 0 && n_ent > 0) ok = stage(0, load_gates(0));
         for (int e = 0; e < n_ent && ok; ++e) {
-            const int s = tab.perm[e];
-            const int sw = min(w, tab.off[s + 1] - tab.off[s]);
-            // next entry's raw seam rows and gates start loading now
-            float gab = 0.f;
-            if (w > 0 && e + 1 < n_ent) {
-                if (tid == 0) load_raw(e + 1);
-                gab = load_gates(e + 1);
-            }
-            if (a.S_prefix) {
-                float *dst = a.S_prefix + (((size_t)l * n_ent + e) * dm.H + h) * D * D + j;
-#pragma unroll
-                for (int r = 0; r < HR; ++r) dst[(size_t)RW(r) * D] = x[r];
-            }
-            // ---- seam of entry e (tokens staged in buffer e & 1)
+            const uint8_t *buf = sm + SM_BUF + (e & 1) * BUF_BYTES;
             if (w > 0) {
-                tc::bar_sync(BAR_MAIN, NMAIN);  // staged tokens visible
-                const float *tok = toks;
+                // ---- seam outputs and the update operand W
+                const int sw = seam_len(tab, e, w);
+                bool wt = true;
+                if (tid == 0) wt = wait_bar(bar(B_SEAMDONE), e & 1, abort_flag);
+                if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
+                tc::fence_after();
+                const float *smf = reinterpret_cast<const float *>(buf + BF_SMALL);
+                const float *Vr = reinterpret_cast<const float *>(buf + BF_V);
+                float uz[32];
+                tc::tmem_ld32(my + TM_D2, uz);
+                float U[WMAX];
+#pragma unroll
+                for (int t = 0; t < WMAX; ++t) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int s = 0; s <= t; ++s)
+                        acc = fmaf(smf[SMALL_M + t * WMAX + s], Vr[s * D + j] - smf[SMALL_G + s] * uz[s], acc);
+                    U[t] = acc;
+                }
                 float *o_dst = a.o_out + (((size_t)l * n_ent + e) * w) * dm.H * D + (size_t)h * D + j;
-                for (int t = 0; t < w; ++t) {
-                    float o = 0.f;
-                    if (t < sw) {
-                        const float *row = tok + t * TOK_F;
-                        const float al = row[3 * D], be = row[3 * D + 1];
-                        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
 #pragma unroll
-                        for (int r = 0; r < HR; r += 4) {
-                            const float4 k4 = *reinterpret_cast<const float4 *>(row + D + RW(r));
-                            u0 = fmaf(k4.x, x[r], u0);
-                            u1 = fmaf(k4.y, x[r + 1], u1);
-                            u2 = fmaf(k4.z, x[r + 2], u2);
-                            u3 = fmaf(k4.w, x[r + 3], u3);
-                        }
-                        float u = (u0 + u1) + (u2 + u3);
-                        u += __shfl_xor_sync(0xffffffffu, u, 1);
-                        const float coef = be * (row[2 * D + j] - al * u);
-                        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+                for (int t = 0; t < WMAX; ++t) {
+                    if (t < w) {
+                        float o = smf[SMALL_G + t] * uz[WMAX + t];
 #pragma unroll
-                        for (int r = 0; r < HR; r += 4) {
-                            const float4 k4 = *reinterpret_cast<const float4 *>(row + D + RW(r));
-                            const float4 q4 = *reinterpret_cast<const float4 *>(row + RW(r));
-                            x[r] = fmaf(k4.x, coef, al * x[r]);
-                            x[r + 1] = fmaf(k4.y, coef, al * x[r + 1]);
-                            x[r + 2] = fmaf(k4.z, coef, al * x[r + 2]);
-                            x[r + 3] = fmaf(k4.w, coef, al * x[r + 3]);
-                            o0 = fmaf(q4.x, x[r], o0);
-                            o1 = fmaf(q4.y, x[r + 1], o1);
-                            o2 = fmaf(q4.z, x[r + 2], o2);
-                            o3 = fmaf(q4.w, x[r + 3], o3);
-                        }
-                        o = (o0 + o1) + (o2 + o3);
+                        for (int s = 0; s <= t; ++s) o = fmaf(smf[SMALL_AQ + t * WMAX + s], U[s], o);
+                        o_dst[(size_t)t * dm.H * D] = (t < sw) ? o : 0.f;
                     }
-                    o += __shfl_xor_sync(0xffffffffu, o, 1);
-                    if (hf == 0) o_dst[(size_t)t * dm.H * D] = o;
                 }
-            }
-            // ---- B operand: S^T row j = column j of S, rounded to tf32
+                float wv[32];
 #pragma unroll
-            for (int r = 0; r < HR; r += 4)
-                *reinterpret_cast<float4 *>(sm + SM_ST + tc::sw128_f32(j, RW(r), D)) =
-                    make_float4(tc::round_tf32(x[r]), tc::round_tf32(x[r + 1]), tc::round_tf32(x[r + 2]),
-                                tc::round_tf32(x[r + 3]));
-            tc::fence_async_smem();
-            tc::bar_sync(BAR_MAIN, NMAIN);
-            bool wm = true;
+                for (int s = 0; s < WMAX; ++s) {
+                    const float x = smf[SMALL_D + s] * U[s];
+                    const float hi = tc::round_tf32(x);
+                    wv[s] = hi;
+                    wv[WMAX + s] = tc::round_tf32(x - hi);
+                    wv[2 * WMAX + s] = hi;
+                    wv[3 * WMAX + s] = 0.f;
+                }
+                tc::tmem_st32(my + TM_W, wv);
+                const float gl = smf[SMALL_GL];
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float xv[32];
+                    tc::tmem_ld32(my + TM_X + c0, xv);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) xv[q] *= gl;
+                    tc::tmem_st32(my + TM_X + c0, xv);
+                }
+                tc::fence_before();
+                tc::bar_sync(BAR_STATE, NS);
+                if (tid == 0) tc::mbar_arrive(bar(B_WREADY));
+                // ---- Xhi of the state after the seam (operand of the body MMA)
+                if (tid == 0) wt = wait_bar(bar(B_UPDDONE), e & 1, abort_flag);
+                if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
+                tc::fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float xv[32];
+                    tc::tmem_ld32(my + TM_X + c0, xv);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) xv[q] = tc::round_tf32(xv[q]);
+                    tc::tmem_st32(my + TM_XHI + c0, xv);
+                }
+                tc::fence_before();
+                tc::bar_sync(BAR_STATE, NS);
+                if (tid == 0) tc::mbar_arrive(bar(B_XHIREADY));
+            }
+            // ---- body: S = T_C S + S(C|0), back into X / Xhi / Xlo
+            bool wb = true;
             if (tid == 0) {
-                wm = wait_bar(bar(B_FULLT), e & 1, abort_flag);
-                if (wm) {
-                    tc::fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < D / 8; ++ks)
-                        tc::mma_ss(tb, tc::sdesc_kstep(s_base + SM_T, D, ks),
-                                   tc::sdesc_kstep(s_base + SM_ST, D, ks), tc::idesc_tf32(128, 128), ks > 0);
-                    tc::commit(bar(B_MMADONE));
-                }
+                wb = wait_bar(bar(B_BODYDONE), e & 1, abort_flag);
+                if (wb) wb = wait_bar(bar(B_FULLSC), e & 1, abort_flag);
             }
-            // ---- stage the next entry's seam tokens while the MMA runs
-            if (w > 0 && e + 1 < n_ent && !stage(e + 1, gab)) { ok = false; break; }
-            // ---- epilogue: S_new row i = (T_C S)[i][:] + S(C|0)[i][:], transposed into S^T
-            bool wt = wm;
-            if (tid == 0 && wt) {
-                wt = wait_bar(bar(B_MMADONE), e & 1, abort_flag);
-                if (wt && e + 1 < n_ent) load_T(e + 1);  // T buffer free once the MMA is done
-                if (wt) wt = wait_bar(bar(B_FULLSC), e & 1, abort_flag);
-            }
-            if (!tc::bar_and(BAR_MAIN, NMAIN, wt)) { ok = false; break; }
+            if (!tc::bar_and(BAR_STATE, NS, wb)) { ok = false; break; }
             tc::fence_after();
-            {
-                float dv[32];
+            const bool last = e + 1 == n_ent;
+            float *out = last ? a.S_final + st_base
+                              : (a.S_prefix ? a.S_prefix + (((size_t)l * n_ent + e + 1) * dm.H + h) * D * D : nullptr);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float xv[32], hv[32];
+                tc::tmem_ld32(my + TM_Y + c0, xv);
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    const int cc = cbase + c0;
-                    tc::tmem_ld32(my + cc, dv);
+                for (int q = 0; q < 32; ++q)
+                    xv[q] += *reinterpret_cast<const float *>(sm + SM_SC + tc::sw128_f32(c0 + q, j, D));
+                tc::tmem_st32(my + TM_X + c0, xv);
 #pragma unroll
-                    for (int q = 0; q < 32; q += 4) {
-                        const float4 s4 =
-                            *reinterpret_cast<const float4 *>(sm + SM_SC + tc::sw128_f32(lane_i, cc + q, D));
-                        *reinterpret_cast<float *>(sm + SM_ST + tc::sw128_f32(cc + q, lane_i, D)) = dv[q] + s4.x;
-                        *reinterpret_cast<float *>(sm + SM_ST + tc::sw128_f32(cc + q + 1, lane_i, D)) = dv[q + 1] + s4.y;
-                        *reinterpret_cast<float *>(sm + SM_ST + tc::sw128_f32(cc + q + 2, lane_i, D)) = dv[q + 2] + s4.z;
-                        *reinterpret_cast<float *>(sm + SM_ST + tc::sw128_f32(cc + q + 3, lane_i, D)) = dv[q + 3] + s4.w;
-                    }
+                for (int q = 0; q < 32; ++q) hv[q] = tc::round_tf32(xv[q]);
+                tc::tmem_st32(my + TM_XHI + c0, hv);
+                if (out) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) out[(size_t)(c0 + q) * D + j] = xv[q];
                 }
+#pragma unroll
+                for (int q = 0; q < 32; ++q) hv[q] = tc::round_tf32(xv[q] - hv[q]);
+                tc::tmem_st32(my + TM_XLO + c0, hv);
             }
             tc::fence_before();
-            tc::bar_sync(BAR_MAIN, NMAIN);
-            if (tid == 0 && e + 1 < n_ent) {  // S(C|0) buffer consumed
-                load_SC(e + 1);
-                armed = e + 2;
-            }
-            // ---- back to columns
-#pragma unroll
-            for (int r = 0; r < HR; r += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(sm + SM_ST + tc::sw128_f32(j, RW(r), D));
-                x[r] = v4.x;
-                x[r + 1] = v4.y;
-                x[r + 2] = v4.z;
-                x[r + 3] = v4.w;
+            tc::bar_sync(BAR_STATE, NS);
+            if (tid == 0 && !last) {
+                load_SC(e + 1);  // S(C|0) buffer consumed
+                sc_armed = e + 2;
+                tc::mbar_arrive(bar(B_XREADY));
             }
         }
-        if (ok) {
-#pragma unroll
-            for (int r = 0; r < HR; ++r) a.S_final[st_base + (size_t)RW(r) * D + j] = x[r];
-        } else if (tid == 0 && armed > 0) {
-            // aborted: let the copies in flight land before the CTA exits
+        if (!ok && tid == 0 && sc_armed > 0) {
+            // aborted: let the copy in flight land before the CTA exits
             const long long t0 = clock64();
-            while ((!tc::mbar_test(bar(B_FULLT), (armed - 1) & 1) || !tc::mbar_test(bar(B_FULLSC), (armed - 1) & 1)) &&
-                   clock64() - t0 < kWaitCycles) {
+            while (!tc::mbar_test(bar(B_FULLSC), (sc_armed - 1) & 1) && clock64() - t0 < kWaitCycles) {
+            }
+        }
+    } else if (warp < 8) {
+        // ================================================= staging warps
+        const int c = tid - NS;  // channel
+        const int gw = warp - 4;
+        constexpr int NL = CK > 0 ? CK : 1;
+        float wq[NL], wk[NL], wvv[NL];
+        if (CK > 0) {
+            const float *w0 = a.tok.conv_w + (((size_t)l * 3 + 0) * dm.H + h) * D * CK + c * CK;
+#pragma unroll
+            for (int jj = 0; jj < NL; ++jj) {
+                wq[jj] = __ldg(w0 + jj);
+                wk[jj] = __ldg(w0 + (size_t)dm.H * D * CK + jj);
+                wvv[jj] = __ldg(w0 + 2 * (size_t)dm.H * D * CK + jj);
+            }
+        }
+        float *red = reinterpret_cast<float *>(sm + SM_RED);
+        float *dots = red + 4 * WMAX * 2;
+        int raw_armed = 0;
+        if (w > 0 && c == 0) {
+            for (int e = 0; e < 2 && e < n_ent; ++e) load_raw(e);
+            raw_armed = min(2, n_ent);
+        }
+        bool ok = true;
+        for (int e = 0; w > 0 && e < n_ent && ok; ++e) {
+            const int b = e & 1;
+            uint8_t *buf = sm + SM_BUF + b * BUF_BYTES;
+            const uint8_t *raw = sm + SM_RAW + b * 3 * RAW_T;
+            const int s = tab.perm[e];
+            const int sw = seam_len(tab, e, w);
+            // gates of the seam tokens (lanes 0-7 of the first staging warp: alpha, 8-15: beta)
+            float gab = 0.f;
+            if (c < 2 * WMAX && (c & (WMAX - 1)) < sw) {
+                const size_t gi = gate_index(dm, a.tok.N, l, tab.off[s] + (c & (WMAX - 1)), h);
+                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(c < WMAX ? a.tok.alpha : a.tok.beta);
+                gab = __bfloat162float(src[gi]);
+            } else if (c < WMAX) {
+                gab = 1.f;  // padding token: alpha = 1, beta = 0
+            }
+            bool wt = true;
+            if (c == 0) {
+                if (e >= 2) wt = wait_bar(bar(B_BUFFREE0 + b), ((e - 2) >> 1) & 1, abort_flag);
+                if (wt) wt = wait_bar(bar(B_FULLR0 + b), (e >> 1) & 1, abort_flag);
+            }
+            if (!tc::bar_and(BAR_STAGE, NG, wt)) { ok = false; break; }
+            // ---- conv (along the request stream) and L2 normalisation of q, k
+            const bool htma = CK > 0 && hist_by_tma(tab, e);
+            auto raw_at = [&](int tensor, int row) {
+                const uint16_t u = *reinterpret_cast<const uint16_t *>(raw + tensor * RAW_T + (row * D + c) * 2);
+                return __uint_as_float(static_cast<uint32_t>(u) << 16);
+            };
+            float qv[WMAX], kv[WMAX], vv[WMAX];
+#pragma unroll
+            for (int t = 0; t < WMAX; ++t) {
+                qv[t] = kv[t] = vv[t] = 0.f;
+                if (t >= sw) continue;
+#pragma unroll
+                for (int lag = 0; lag < NL; ++lag) {
+                    float rq, rk, rv;
+                    if (t - lag >= 0 || htma) {
+                        const int row = HIST + t - lag;
+                        rq = raw_at(0, row);
+                        rk = raw_at(1, row);
+                        rv = raw_at(2, row);
+                    } else {
+                        // history across short segments or before the request start
+                        const int32_t tbk = stream_back(tab, e, t, lag);
+                        rq = rk = rv = 0.f;
+                        if (tbk >= 0) {
+                            const size_t ix = tok_index(dm, a.tok.N, l, tbk, h, c);
+                            rq = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.tok.q)[ix]);
+                            rk = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.tok.k)[ix]);
+                            rv = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.tok.v)[ix]);
+                        }
+                    }
+                    if (CK == 0) {
+                        qv[t] = rq;
+                        kv[t] = rk;
+                        vv[t] = rv;
+                    } else {
+                        qv[t] = fmaf(wq[lag], rq, qv[t]);
+                        kv[t] = fmaf(wk[lag], rk, kv[t]);
+                        vv[t] = fmaf(wvv[lag], rv, vv[t]);
+                    }
+                }
+            }
+            if (CK > 0) {
+                float sq[WMAX], sk[WMAX];
+#pragma unroll
+                for (int t = 0; t < WMAX; ++t) {
+                    sq[t] = qv[t] * qv[t];
+                    sk[t] = kv[t] * kv[t];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int t = 0; t < WMAX; ++t) {
+                        sq[t] += __shfl_xor_sync(0xffffffffu, sq[t], o);
+                        sk[t] += __shfl_xor_sync(0xffffffffu, sk[t], o);
+                    }
+                if (lane == 0) {
+#pragma unroll
+                    for (int t = 0; t < WMAX; ++t) {
+                        red[(gw * WMAX + t) * 2] = sq[t];
+                        red[(gw * WMAX + t) * 2 + 1] = sk[t];
+                    }
+                }
+                tc::bar_sync(BAR_STAGE, NG);
+#pragma unroll
+                for (int t = 0; t < WMAX; ++t) {
+                    float aa = 0.f, bb = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < 4; ++ww) {
+                        aa += red[(ww * WMAX + t) * 2];
+                        bb += red[(ww * WMAX + t) * 2 + 1];
+                    }
+                    qv[t] *= 1.f / sqrtf(aa + kL2Eps);
+                    kv[t] *= 1.f / sqrtf(bb + kL2Eps);
+                }
+            }
+            // raw buffer b consumed: the rows of entry e + 2 may load into it
+            tc::bar_sync(BAR_STAGE, NG);
+            if (c == 0 && e + 2 < n_ent) {
+                load_raw(e + 2);
+                raw_armed = e + 3;
+            }
+            // ---- operand tiles: [k ; q] split in tf32 hi / lo, K^T, V
+#pragma unroll
+            for (int t = 0; t < WMAX; ++t) {
+                const float kh = tc::round_tf32(kv[t]), kl = tc::round_tf32(kv[t] - kh);
+                const float qh = tc::round_tf32(qv[t]), ql = tc::round_tf32(qv[t] - qh);
+                *reinterpret_cast<float *>(buf + BF_KQH + tc::sw128_f32(t, c, 2 * WMAX)) = kh;
+                *reinterpret_cast<float *>(buf + BF_KQL + tc::sw128_f32(t, c, 2 * WMAX)) = kl;
+                *reinterpret_cast<float *>(buf + BF_KQH + tc::sw128_f32(WMAX + t, c, 2 * WMAX)) = qh;
+                *reinterpret_cast<float *>(buf + BF_KQL + tc::sw128_f32(WMAX + t, c, 2 * WMAX)) = ql;
+                *reinterpret_cast<float *>(buf + BF_KP + tc::sw128_f32(c, t, D)) = kh;
+                *reinterpret_cast<float *>(buf + BF_KP + tc::sw128_f32(c, WMAX + t, D)) = kh;
+                *reinterpret_cast<float *>(buf + BF_KP + tc::sw128_f32(c, 2 * WMAX + t, D)) = kl;
+                reinterpret_cast<float *>(buf + BF_V)[t * D + c] = vv[t];
+            }
+            // ---- gates: g_t, Gamma_t, d_s = beta_s e^{g_w - g_s}
+            float *smf = reinterpret_cast<float *>(buf + BF_SMALL);
+            if (gw == 0) {
+                // lanes 0-7 hold alpha_t, lanes 8-15 beta_t
+                const float la = (lane < WMAX) ? fmaxf(logf(gab), -88.f) : 0.f;
+                float g = la;
+#pragma unroll
+                for (int o = 1; o < WMAX; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, g, o);
+                    if (lane >= o && lane < WMAX) g += y;
+                }
+                const float gw7 = __shfl_sync(0xffffffffu, g, WMAX - 1);
+                const float be = __shfl_sync(0xffffffffu, gab, (lane & (WMAX - 1)) + WMAX);
+                if (lane < WMAX) {
+                    smf[SMALL_LG + lane] = g;
+                    smf[SMALL_B + lane] = be;
+                    smf[SMALL_G + lane] = expf(g);
+                    smf[SMALL_D + lane] = be * expf(gw7 - g);
+                    if (lane == 0) smf[SMALL_GL] = expf(gw7);
+                }
+            }
+            tc::fence_async_smem();
+            tc::bar_sync(BAR_STAGE, NG);
+            // ---- the 64 dot products k_t.k_s (s < t) and q_t.k_s (s <= t), fp32 from hi + lo
+            {
+                const int p = c >> 1, half = c & 1;
+                int ra, rb, tt, ss;
+                dot_rows(p, ra, rb, tt, ss);
+                float acc = 0.f;
+#pragma unroll 8
+                for (int cc = 64 * half; cc < 64 * half + 64; cc += 4) {
+                    const float4 ah = *reinterpret_cast<const float4 *>(buf + BF_KQH + tc::sw128_f32(ra, cc, 2 * WMAX));
+                    const float4 al = *reinterpret_cast<const float4 *>(buf + BF_KQL + tc::sw128_f32(ra, cc, 2 * WMAX));
+                    const float4 bh = *reinterpret_cast<const float4 *>(buf + BF_KQH + tc::sw128_f32(rb, cc, 2 * WMAX));
+                    const float4 bl = *reinterpret_cast<const float4 *>(buf + BF_KQL + tc::sw128_f32(rb, cc, 2 * WMAX));
+                    acc = fmaf(ah.x + al.x, bh.x + bl.x, acc);
+                    acc = fmaf(ah.y + al.y, bh.y + bl.y, acc);
+                    acc = fmaf(ah.z + al.z, bh.z + bl.z, acc);
+                    acc = fmaf(ah.w + al.w, bh.w + bl.w, acc);
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                if (half == 0) dots[p] = acc;
+            }
+            tc::bar_sync(BAR_STAGE, NG);
+            // ---- M = (I + L)^{-1}, L_tr = beta_r e^{g_t - g_r} k_t.k_r (r < t): one column per
+            // thread (threads 0-7); AQ_ts = beta_s e^{g_t - g_s} q_t.k_s (s <= t): one row per thread (8-15)
+            if (c < WMAX) {
+                const int col = c;
+                float x[WMAX];
+#pragma unroll
+                for (int t = 0; t < WMAX; ++t) {
+                    float acc = (t == col) ? 1.f : 0.f;
+#pragma unroll
+                    for (int r = 0; r < t; ++r)
+                        acc = fmaf(-dots[t * (t - 1) / 2 + r] * smf[SMALL_B + r] *
+                                       expf(smf[SMALL_LG + t] - smf[SMALL_LG + r]),
+                                   x[r], acc);
+                    x[t] = (t < col) ? 0.f : acc;
+                }
+#pragma unroll
+                for (int t = 0; t < WMAX; ++t) smf[SMALL_M + t * WMAX + col] = x[t];
+            } else if (c < 2 * WMAX) {
+                const int t = c - WMAX;
+#pragma unroll
+                for (int s2 = 0; s2 < WMAX; ++s2) {
+                    float v = 0.f;
+                    if (s2 <= t)
+                        v = dots[28 + t * (t + 1) / 2 + s2] * smf[SMALL_B + s2] *
+                            expf(smf[SMALL_LG + t] - smf[SMALL_LG + s2]);
+                    smf[SMALL_AQ + t * WMAX + s2] = v;
+                }
+            }
+            tc::bar_sync(BAR_STAGE, NG);
+            if (c == 0) tc::mbar_arrive(bar(B_STAGED0 + b));
+        }
+        if (!ok && c == 0 && raw_armed > 0) {
+            const long long t0 = clock64();
+            for (int k = (raw_armed > 2 ? raw_armed - 2 : 0); k < raw_armed; ++k)
+                while (!tc::mbar_test(bar(B_FULLR0 + (k & 1)), (k >> 1) & 1) && clock64() - t0 < kWaitCycles) {
+                }
+        }
+    } else if (warp == WARP_MMA && lane == 0) {
+        // ================================================= MMA issue and T_C copies
+        int t_armed = 0;
+        if (n_ent > 0) {
+            load_T(0);
+            t_armed = 1;
+        }
+        for (int e = 0; e < n_ent; ++e) {
+            const int b = e & 1;
+            const uint32_t buf = s_base + SM_BUF + b * BUF_BYTES;
+            if (!wait_bar(bar(B_XREADY), e & 1, abort_flag)) break;
+            if (w > 0) {
+                if (!wait_bar(bar(B_STAGED0 + b), (e >> 1) & 1, abort_flag)) break;
+                tc::fence_after();
+                // [u | z] = X [k | q]^T, 3xTF32: Xhi khi + Xlo khi + Xhi klo
+#pragma unroll 1
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ts(tb + TM_D2, tb + TM_XHI + ks * 8, tc::sdesc_kstep(buf + BF_KQH, 2 * WMAX, ks),
+                               tc::idesc_tf32(128, 2 * WMAX), ks > 0);
+#pragma unroll 1
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ts(tb + TM_D2, tb + TM_XLO + ks * 8, tc::sdesc_kstep(buf + BF_KQH, 2 * WMAX, ks),
+                               tc::idesc_tf32(128, 2 * WMAX), 1);
+#pragma unroll 1
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ts(tb + TM_D2, tb + TM_XHI + ks * 8, tc::sdesc_kstep(buf + BF_KQL, 2 * WMAX, ks),
+                               tc::idesc_tf32(128, 2 * WMAX), 1);
+                tc::commit(bar(B_SEAMDONE));
+                if (!wait_bar(bar(B_WREADY), e & 1, abort_flag)) break;
+                tc::fence_after();
+                // X += W K: [Whi | Wlo | Whi] against K^T columns [hi | hi | lo]
+#pragma unroll 1
+                for (int ks = 0; ks < 3; ++ks)
+                    tc::mma_ts(tb + TM_X, tb + TM_W + ks * 8, tc::sdesc_kstep(buf + BF_KP, D, ks),
+                               tc::idesc_tf32(128, 128), 1);
+                tc::commit(bar(B_UPDDONE));
+                tc::commit(bar(B_BUFFREE0 + b));
+                if (!wait_bar(bar(B_XHIREADY), e & 1, abort_flag)) break;
+            }
+            if (!wait_bar(bar(B_FULLT), e & 1, abort_flag)) break;
+            tc::fence_after();
+            // Y = Xhi T_C^T, i.e. (T_C S)^T
+#pragma unroll 1
+            for (int ks = 0; ks < D / 8; ++ks)
+                tc::mma_ts(tb + TM_Y, tb + TM_XHI + ks * 8, tc::sdesc_kstep(s_base + SM_T, D, ks),
+                           tc::idesc_tf32(128, 128), ks > 0);
+            tc::commit(bar(B_BODYDONE));
+            if (e + 1 < n_ent) {
+                // T_C buffer free once the body MMA is done
+                if (!wait_bar(bar(B_BODYDONE), e & 1, abort_flag)) break;
+                load_T(e + 1);
+                t_armed = e + 2;
+            }
+        }
+        if (*abort_flag && t_armed > 0) {
+            const long long t0 = clock64();
+            while (!tc::mbar_test(bar(B_FULLT), (t_armed - 1) & 1) && clock64() - t0 < kWaitCycles) {
             }
         }
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    if (warp == 0) tc::tmem_dealloc(tb, 128);
+    if (warp == 0) tc::tmem_dealloc(tb, TM_COLS);
 }
 
 }  // namespace
