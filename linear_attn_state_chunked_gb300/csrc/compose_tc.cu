@@ -8,24 +8,26 @@
 //
 // One CTA per (layer, head) chain.  The running state lives in tensor memory
 // transposed, X = S^T (lane j holds column j of S), in fp32, with its tf32
-// split X = Xhi + Xlo beside it for use as an MMA operand.  Per request entry:
+// rounding Xhi beside it for use as an MMA operand.  Per request entry:
 //
 //   seam (w <= 8 tokens, one chunk of the WY form of the recurrence; with
 //   g_t = sum_{r<=t} log alpha_r, Gamma_t = e^{g_t}):
-//     [u_t | z_t]    = S^T [k_t | q_t]                 tensor core, 3xTF32
+//     [u_t | z_t]    = S^T [k_t | q_t]                 tensor core, tf32
 //     U              = (I + L)^{-1} (V - diag(Gamma) K S)   per column, CUDA cores
 //                      L_ts = beta_s e^{g_t - g_s} k_t.k_s  (s < t)
 //     o_t            = Gamma_t z_t + sum_{s<=t} e^{g_t - g_s} beta_s (q_t.k_s) U_s
 //     S             <- Gamma_w S + K^T diag(beta_s e^{g_w - g_s}) U
-//                      (X rescaled on CUDA cores, then one K = 8 MMA, 3xTF32)
+//                      (X pre-scaled by Gamma_w when the previous entry's
+//                      state is formed, then one K = 8 MMA, 3xTF32)
 //   body:  S <- T_C S + S(C|0)     (tensor core: A = Xhi from tensor memory,
 //                                   B = T_C rows from shared memory)
 //
-// Warp roles: warps 0-3 own the state (thread j = tensor-memory lane j =
-// column j of S); warps 4-7 stage each entry's seam ahead of time (conv warm-up
-// across the segment boundary, L2 normalisation, the seam's 8 x 8 Gram and
-// triangular inverse, all independent of the state) into double buffers;
-// warp 8 issues the MMAs and the T_C copies.  T_C and S(C|0) of the next
+// Warp roles: warps 0-7 own the state (two warps per tensor-memory lane
+// quadrant, each half of the columns; lane j = column j of S), thread 0 also
+// issuing the MMAs and the T_C / S(C|0) copies; warps 8-11 stage each
+// entry's seam ahead of time (conv warm-up across the segment boundary, L2
+// normalisation, the seam's 8 x 8 Gram and triangular inverse, all
+// independent of the state) into double buffers.  T_C and S(C|0) of the next
 // entry stream in by TMA as soon as their buffers free up.
 #include <cstring>
 
@@ -40,20 +42,18 @@ namespace {
 constexpr int D = 128;
 constexpr int WMAX = 8;       // seam window served by this kernel
 constexpr int HIST = 3;       // conv history rows (taps - 1, taps <= 4)
-constexpr int NS = 128;       // state threads (warps 0-3)
-constexpr int NG = 128;       // staging threads (warps 4-7)
-constexpr int WARP_MMA = 8;   // MMA issue and T_C copies (lane 0)
-constexpr int NT = NS + NG + 32;
+constexpr int NS = 256;       // state threads (warps 0-7, two per tensor-memory lane quadrant)
+constexpr int NG = 128;       // staging threads (warps 8-11)
+constexpr int NT = NS + NG;
 constexpr int BAR_STATE = 1, BAR_STAGE = 2;
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds
 
 // tensor-memory columns
-constexpr uint32_t TM_X = 0;      // S^T, fp32
-constexpr uint32_t TM_XHI = 128;  // tf32(S^T)
-constexpr uint32_t TM_XLO = 256;  // tf32(S^T - Xhi)
-constexpr uint32_t TM_Y = 384;    // T_C S (transposed); during the seam: [u | z] and W
-constexpr uint32_t TM_D2 = TM_Y;       // 16 columns: u_t (t < 8), z_t
-constexpr uint32_t TM_W = TM_Y + 32;   // 24 columns: Whi, Wlo, Whi
+constexpr uint32_t TM_X = 0;      // S^T, fp32 (pre-scaled by Gamma_w of the next seam)
+constexpr uint32_t TM_XHI = 128;  // tf32(S^T), unscaled
+constexpr uint32_t TM_Y = 256;    // T_C S (transposed); during the seam: [u | z] and W
+constexpr uint32_t TM_D2 = TM_Y;       // 4 x 16 columns: partial [u_t | z_t] over quarters of k
+constexpr uint32_t TM_W = TM_Y + 64;   // 24 columns: Whi, Wlo, Whi
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory
@@ -61,7 +61,7 @@ constexpr uint32_t SM_T = 0;         // T_C    [128][128] fp32, sw128 (B of the 
 constexpr uint32_t SM_SC = 65536;    // S(C|0) [128][128] fp32, sw128
 constexpr uint32_t SM_BUF = 131072;  // 2 x staged seam
 constexpr uint32_t BF_KQH = 0;       //   [k_t ; q_t] tf32 hi [16][128], sw128 (B of the seam MMA)
-constexpr uint32_t BF_KQL = 8192;    //   lo parts
+constexpr uint32_t BF_KQF = 8192;    //   the same in fp32 (for the seam's Gram)
 constexpr uint32_t BF_KP = 16384;    //   K^T [128][32] sw128: columns t, 8 + t = hi(k_t), 16 + t = lo(k_t)
 constexpr uint32_t BF_V = 32768;     //   v_t [8][128] fp32
 constexpr uint32_t BF_SMALL = 36864; //   M [8][8], AQ [8][8], Gamma [8], d [8], Gamma_w, beta [8], g [8]
@@ -70,28 +70,27 @@ constexpr int SMALL_M = 0, SMALL_AQ = 64, SMALL_G = 128, SMALL_D = 136, SMALL_GL
               SMALL_LG = 160;
 constexpr uint32_t RAW_T = (HIST + WMAX) * D * 2;           // raw rows per tensor (bf16)
 constexpr uint32_t SM_RAW = SM_BUF + 2 * BUF_BYTES;         // 2 x {q, k, v} raw rows (TMA)
-constexpr uint32_t SM_RED = SM_RAW + 2 * 3 * RAW_T;         // [4 warps][8 tokens][2] + dots [64]
-constexpr uint32_t SM_BAR = SM_RED + (4 * WMAX * 2 + 64) * 4;
+constexpr uint32_t SM_RED = SM_RAW + 2 * 3 * RAW_T;         // staging scratch (below)
+constexpr int RED_DOTS = 4 * WMAX * 2;                      //   after [4 warps][8 tokens][2] norms: dots [64]
+constexpr int RED_SCR = RED_DOTS + 64;                      //   beta_s e^{g_t - g_s} [64], L [64]
+constexpr uint32_t SM_BAR = SM_RED + (RED_SCR + 128) * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 16 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
 static_assert(SMEM_DYN <= 232448, "shared memory budget");
-static_assert(SM_BUF % 1024 == 0 && BUF_BYTES % 1024 == 0 && BF_KP % 1024 == 0 && BF_KQL % 1024 == 0,
+static_assert(SM_BUF % 1024 == 0 && BUF_BYTES % 1024 == 0 && BF_KP % 1024 == 0 && BF_KQF % 1024 == 0,
               "operand tile alignment");
 static_assert(SM_RAW % 128 == 0 && RAW_T % 128 == 0 && (HIST * D * 2) % 128 == 0, "TMA alignment");
 
 enum {
-    B_FULLT = 0,   // T_C of the entry landed                     TMA -> mma
+    B_FULLT = 0,   // T_C of the entry landed                     TMA -> state
     B_FULLSC,      // S(C|0) of the entry landed                  TMA -> state
     B_FULLR0,      // [2] raw seam rows landed                    TMA -> staging
-    B_STAGED0 = B_FULLR0 + 2,  // [2] seam staged                 staging -> mma
-    B_BUFFREE0 = B_STAGED0 + 2,  // [2] staged buffer consumed    mma -> staging
-    B_XREADY = B_BUFFREE0 + 2,   // X, Xhi, Xlo hold the state before the entry   state -> mma
-    B_SEAMDONE,    // [u | z] in tensor memory                    mma -> state
-    B_WREADY,      // W written, X rescaled                       state -> mma
-    B_UPDDONE,     // seam update of X done                       mma -> state
-    B_XHIREADY,    // Xhi of the state after the seam             state -> mma
-    B_BODYDONE,    // T_C S in tensor memory                      mma -> state
+    B_STAGED0 = B_FULLR0 + 2,    // [2] seam staged               staging -> state
+    B_BUFFREE0 = B_STAGED0 + 2,  // [2] staged buffer consumed    MMA -> staging
+    B_SEAMDONE = B_BUFFREE0 + 2, // [u | z] in tensor memory      MMA -> state
+    B_UPDDONE,     // seam update of X done                       MMA -> state
+    B_BODYDONE,    // T_C S in tensor memory                      MMA -> state
     B_COUNT
 };
 
@@ -217,48 +216,92 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
     };
 
     const size_t st_base = ((size_t)l * dm.H + h) * D * D;
-    if (warp < 4) {
+    if (warp < NS / 32) {
         // ================================================= state warps
-        const int j = tid;
-        const uint32_t my = tb + (static_cast<uint32_t>(warp * 32) << 16);
-        int sc_armed = 0;  // S(C|0) copies issued
+        // lane j = 32 (warp % 4) + lane of tensor memory = column j of S;
+        // this thread's columns of X are 64 hf .. 64 hf + 63.  Thread 0 also
+        // issues every MMA and the T_C / S(C|0) copies.
+        const int j = 32 * (warp & 3) + lane, hf = warp >> 2;
+        const uint32_t my = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        int t_armed = 0, sc_armed = 0;  // copies issued
+        auto issue_seam = [&](int e) {
+            const uint32_t buf = s_base + SM_BUF + (e & 1) * BUF_BYTES;
+            tc::fence_after();
+            // [u | z] = Xhi [k | q]^T in tf32, as four independent partial sums
+            // over quarters of k (columns 16 p .. 16 p + 15) so the MMAs overlap
+#pragma unroll 1
+            for (int ks = 0; ks < D / 8; ++ks)
+                tc::mma_ts(tb + TM_D2 + 16 * (ks & 3), tb + TM_XHI + ks * 8,
+                           tc::sdesc_kstep(buf + BF_KQH, 2 * WMAX, ks), tc::idesc_tf32(128, 2 * WMAX), ks >= 4);
+            tc::commit(bar(B_SEAMDONE));
+        };
+        auto issue_body = [&](int e) -> bool {
+            if (!wait_bar(bar(B_FULLT), e & 1, abort_flag)) return false;
+            tc::fence_after();
+            // Y = Xhi T_C^T, i.e. (T_C S)^T
+#pragma unroll 1
+            for (int ks = 0; ks < D / 8; ++ks)
+                tc::mma_ts(tb + TM_Y, tb + TM_XHI + ks * 8, tc::sdesc_kstep(s_base + SM_T, D, ks),
+                           tc::idesc_tf32(128, 128), ks > 0);
+            tc::commit(bar(B_BODYDONE));
+            return true;
+        };
+        // Gamma_w of entry e's seam (1 without seams); waits for the staging of
+        // entry e, which runs ahead
+        auto seam_scale = [&](int e, bool &okw) -> float {
+            if (w == 0) return 1.f;
+            bool wt = true;
+            if (tid == 0) wt = wait_bar(bar(B_STAGED0 + (e & 1)), (e >> 1) & 1, abort_flag);
+            okw = tc::bar_and(BAR_STATE, NS, wt);
+            return reinterpret_cast<const float *>(sm + SM_BUF + (e & 1) * BUF_BYTES + BF_SMALL)[SMALL_GL];
+        };
         if (tid == 0 && n_ent > 0) {
+            load_T(0);
             load_SC(0);
-            sc_armed = 1;
+            t_armed = sc_armed = 1;
         }
-        // X = S_init^T (or 0); S_prefix[0] = S_init
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float xv[32], hv[32], lv[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const float x = a.S_init ? a.S_init[st_base + (size_t)(c0 + q) * D + j] : 0.f;
-                xv[q] = x;
-                hv[q] = tc::round_tf32(x);
-                lv[q] = tc::round_tf32(x - hv[q]);
-                if (n_ent > 0 && a.S_prefix) a.S_prefix[(((size_t)l * n_ent) * dm.H + h) * D * D + (size_t)(c0 + q) * D + j] = x;
-                if (n_ent == 0) a.S_final[st_base + (size_t)(c0 + q) * D + j] = x;
-            }
-            tc::tmem_st32(my + TM_X + c0, xv);
-            tc::tmem_st32(my + TM_XHI + c0, hv);
-            tc::tmem_st32(my + TM_XLO + c0, lv);
-        }
-        tc::fence_before();
-        tc::bar_sync(BAR_STATE, NS);
-        if (tid == 0 && n_ent > 0) tc::mbar_arrive(bar(B_XREADY));
         bool ok = true;
+        // X = Gamma_w S_init^T (or 0), Xhi = tf32(S_init^T); S_prefix[0] = S_init
+        {
+            const float g0 = n_ent > 0 ? seam_scale(0, ok) : 1.f;
+            for (int c0 = 64 * hf; ok && c0 < 64 * hf + 64; c0 += 32) {
+                float xv[32], hv[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const float x = a.S_init ? a.S_init[st_base + (size_t)(c0 + q) * D + j] : 0.f;
+                    xv[q] = g0 * x;
+                    hv[q] = tc::round_tf32(x);
+                    if (n_ent > 0 && a.S_prefix)
+                        a.S_prefix[(((size_t)l * n_ent) * dm.H + h) * D * D + (size_t)(c0 + q) * D + j] = x;
+                    if (n_ent == 0) a.S_final[st_base + (size_t)(c0 + q) * D + j] = x;
+                }
+                tc::tmem_st32_async(my + TM_X + c0, xv);
+                tc::tmem_st32_async(my + TM_XHI + c0, hv);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before();
+            tc::bar_sync(BAR_STATE, NS);
+            if (tid == 0 && ok && n_ent > 0 && w > 0) issue_seam(0);
+        }
         for (int e = 0; e < n_ent && ok; ++e) {
             const uint8_t *buf = sm + SM_BUF + (e & 1) * BUF_BYTES;
+            bool wt = true;
             if (w > 0) {
                 // ---- seam outputs and the update operand W
                 const int sw = seam_len(tab, e, w);
-                bool wt = true;
                 if (tid == 0) wt = wait_bar(bar(B_SEAMDONE), e & 1, abort_flag);
                 if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
                 tc::fence_after();
                 const float *smf = reinterpret_cast<const float *>(buf + BF_SMALL);
                 const float *Vr = reinterpret_cast<const float *>(buf + BF_V);
-                float uz[32];
-                tc::tmem_ld32(my + TM_D2, uz);
+                float uz[2 * WMAX];
+                {
+                    float p0[32], p1[32];
+                    tc::tmem_ld32(my + TM_D2, p0);
+                    tc::tmem_ld32(my + TM_D2 + 32, p1);
+#pragma unroll
+                    for (int cc = 0; cc < 2 * WMAX; ++cc) uz[cc] = (p0[cc] + p0[16 + cc]) + (p1[cc] + p1[16 + cc]);
+                }
                 float U[WMAX];
 #pragma unroll
                 for (int t = 0; t < WMAX; ++t) {
@@ -268,103 +311,117 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                         acc = fmaf(smf[SMALL_M + t * WMAX + s], Vr[s * D + j] - smf[SMALL_G + s] * uz[s], acc);
                     U[t] = acc;
                 }
-                float *o_dst = a.o_out + (((size_t)l * n_ent + e) * w) * dm.H * D + (size_t)h * D + j;
+                if (hf == 0) {
+                    float wv[32];
 #pragma unroll
-                for (int t = 0; t < WMAX; ++t) {
-                    if (t < w) {
-                        float o = smf[SMALL_G + t] * uz[WMAX + t];
+                    for (int s = 0; s < WMAX; ++s) {
+                        const float x = smf[SMALL_D + s] * U[s];
+                        const float hi = tc::round_tf32(x);
+                        wv[s] = hi;
+                        wv[WMAX + s] = tc::round_tf32(x - hi);
+                        wv[2 * WMAX + s] = hi;
+                        wv[3 * WMAX + s] = 0.f;
+                    }
+                    tc::tmem_st32(my + TM_W, wv);
+                    tc::fence_before();
+                }
+                tc::bar_sync(BAR_STATE, NS);
+                if (tid == 0) {
+                    tc::fence_after();
+                    // X += W K: [Whi | Wlo | Whi] against K^T columns [hi | hi | lo]
+                    const uint32_t bufa = s_base + SM_BUF + (e & 1) * BUF_BYTES;
+#pragma unroll 1
+                    for (int ks = 0; ks < 3; ++ks)
+                        tc::mma_ts(tb + TM_X, tb + TM_W + ks * 8, tc::sdesc_kstep(bufa + BF_KP, D, ks),
+                                   tc::idesc_tf32(128, 128), 1);
+                    tc::commit(bar(B_UPDDONE));
+                    tc::commit(bar(B_BUFFREE0 + (e & 1)));
+                }
+                if (hf == 1) {
+                    // outputs while the update MMA runs
+                    float *o_dst = a.o_out + (((size_t)l * n_ent + e) * w) * dm.H * D + (size_t)h * D + j;
 #pragma unroll
-                        for (int s = 0; s <= t; ++s) o = fmaf(smf[SMALL_AQ + t * WMAX + s], U[s], o);
-                        o_dst[(size_t)t * dm.H * D] = (t < sw) ? o : 0.f;
+                    for (int t = 0; t < WMAX; ++t) {
+                        if (t < w) {
+                            float o = smf[SMALL_G + t] * uz[WMAX + t];
+#pragma unroll
+                            for (int s = 0; s <= t; ++s) o = fmaf(smf[SMALL_AQ + t * WMAX + s], U[s], o);
+                            o_dst[(size_t)t * dm.H * D] = (t < sw) ? o : 0.f;
+                        }
                     }
                 }
-                float wv[32];
-#pragma unroll
-                for (int s = 0; s < WMAX; ++s) {
-                    const float x = smf[SMALL_D + s] * U[s];
-                    const float hi = tc::round_tf32(x);
-                    wv[s] = hi;
-                    wv[WMAX + s] = tc::round_tf32(x - hi);
-                    wv[2 * WMAX + s] = hi;
-                    wv[3 * WMAX + s] = 0.f;
-                }
-                tc::tmem_st32(my + TM_W, wv);
-                const float gl = smf[SMALL_GL];
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float xv[32];
-                    tc::tmem_ld32(my + TM_X + c0, xv);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) xv[q] *= gl;
-                    tc::tmem_st32(my + TM_X + c0, xv);
-                }
-                tc::fence_before();
-                tc::bar_sync(BAR_STATE, NS);
-                if (tid == 0) tc::mbar_arrive(bar(B_WREADY));
                 // ---- Xhi of the state after the seam (operand of the body MMA)
                 if (tid == 0) wt = wait_bar(bar(B_UPDDONE), e & 1, abort_flag);
                 if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
                 tc::fence_after();
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
                     float xv[32];
                     tc::tmem_ld32(my + TM_X + c0, xv);
 #pragma unroll
                     for (int q = 0; q < 32; ++q) xv[q] = tc::round_tf32(xv[q]);
-                    tc::tmem_st32(my + TM_XHI + c0, xv);
+                    tc::tmem_st32_async(my + TM_XHI + c0, xv);
                 }
+                tc::tmem_wait_st();
                 tc::fence_before();
                 tc::bar_sync(BAR_STATE, NS);
-                if (tid == 0) tc::mbar_arrive(bar(B_XHIREADY));
             }
-            // ---- body: S = T_C S + S(C|0), back into X / Xhi / Xlo
-            bool wb = true;
-            if (tid == 0) {
-                wb = wait_bar(bar(B_BODYDONE), e & 1, abort_flag);
-                if (wb) wb = wait_bar(bar(B_FULLSC), e & 1, abort_flag);
-            }
-            if (!tc::bar_and(BAR_STATE, NS, wb)) { ok = false; break; }
-            tc::fence_after();
+            if (tid == 0) wt = issue_body(e);
+            // ---- body: S = T_C S + S(C|0); X takes the next seam's Gamma_w
             const bool last = e + 1 == n_ent;
+            const float gn = last ? 1.f : seam_scale(e + 1, ok);
+            if (!ok) break;
+            if (tid == 0 && wt) {
+                wt = wait_bar(bar(B_BODYDONE), e & 1, abort_flag);
+                if (wt) wt = wait_bar(bar(B_FULLSC), e & 1, abort_flag);
+            }
+            if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
+            tc::fence_after();
+            if (tid == 0 && !last) {
+                load_T(e + 1);  // T_C buffer free: the body MMA is done
+                t_armed = e + 2;
+            }
             float *out = last ? a.S_final + st_base
                               : (a.S_prefix ? a.S_prefix + (((size_t)l * n_ent + e + 1) * dm.H + h) * D * D : nullptr);
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+#pragma unroll
+            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
                 float xv[32], hv[32];
                 tc::tmem_ld32(my + TM_Y + c0, xv);
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
+                for (int q = 0; q < 32; ++q) {
                     xv[q] += *reinterpret_cast<const float *>(sm + SM_SC + tc::sw128_f32(c0 + q, j, D));
-                tc::tmem_st32(my + TM_X + c0, xv);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) hv[q] = tc::round_tf32(xv[q]);
-                tc::tmem_st32(my + TM_XHI + c0, hv);
+                    hv[q] = tc::round_tf32(xv[q]);
+                }
+                tc::tmem_st32_async(my + TM_XHI + c0, hv);
                 if (out) {
 #pragma unroll
                     for (int q = 0; q < 32; ++q) out[(size_t)(c0 + q) * D + j] = xv[q];
                 }
 #pragma unroll
-                for (int q = 0; q < 32; ++q) hv[q] = tc::round_tf32(xv[q] - hv[q]);
-                tc::tmem_st32(my + TM_XLO + c0, hv);
+                for (int q = 0; q < 32; ++q) xv[q] *= gn;
+                tc::tmem_st32_async(my + TM_X + c0, xv);
             }
+            tc::tmem_wait_st();
             tc::fence_before();
             tc::bar_sync(BAR_STATE, NS);
             if (tid == 0 && !last) {
                 load_SC(e + 1);  // S(C|0) buffer consumed
                 sc_armed = e + 2;
-                tc::mbar_arrive(bar(B_XREADY));
+                if (w > 0) issue_seam(e + 1);
             }
         }
-        if (!ok && tid == 0 && sc_armed > 0) {
-            // aborted: let the copy in flight land before the CTA exits
+        if (!ok && tid == 0) {
+            // aborted: let the copies in flight land before the CTA exits
             const long long t0 = clock64();
-            while (!tc::mbar_test(bar(B_FULLSC), (sc_armed - 1) & 1) && clock64() - t0 < kWaitCycles) {
+            while (((t_armed > 0 && !tc::mbar_test(bar(B_FULLT), (t_armed - 1) & 1)) ||
+                    (sc_armed > 0 && !tc::mbar_test(bar(B_FULLSC), (sc_armed - 1) & 1))) &&
+                   clock64() - t0 < kWaitCycles) {
             }
         }
-    } else if (warp < 8) {
+    } else {
         // ================================================= staging warps
         const int c = tid - NS;  // channel
-        const int gw = warp - 4;
+        const int gw = warp - NS / 32;
         constexpr int NL = CK > 0 ? CK : 1;
         float wq[NL], wk[NL], wvv[NL];
         if (CK > 0) {
@@ -377,28 +434,33 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             }
         }
         float *red = reinterpret_cast<float *>(sm + SM_RED);
-        float *dots = red + 4 * WMAX * 2;
+        float *dots = red + RED_DOTS;
+        float *scr = red + RED_SCR;
+        // gates of entry e's seam tokens: threads 0-7 alpha_t (1 past the
+        // segment), 8-15 beta_t (0 past the segment)
+        auto gate = [&](int e) {
+            float v = (c < WMAX) ? 1.f : 0.f;
+            if (c < 2 * WMAX && e < n_ent && (c & (WMAX - 1)) < seam_len(tab, e, w)) {
+                const size_t gi = gate_index(dm, a.tok.N, l, tab.off[tab.perm[e]] + (c & (WMAX - 1)), h);
+                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(c < WMAX ? a.tok.alpha : a.tok.beta);
+                v = __bfloat162float(src[gi]);
+            }
+            return v;
+        };
         int raw_armed = 0;
         if (w > 0 && c == 0) {
             for (int e = 0; e < 2 && e < n_ent; ++e) load_raw(e);
             raw_armed = min(2, n_ent);
         }
+        float gab_next = (w > 0) ? gate(0) : 0.f;
         bool ok = true;
         for (int e = 0; w > 0 && e < n_ent && ok; ++e) {
             const int b = e & 1;
             uint8_t *buf = sm + SM_BUF + b * BUF_BYTES;
             const uint8_t *raw = sm + SM_RAW + b * 3 * RAW_T;
-            const int s = tab.perm[e];
             const int sw = seam_len(tab, e, w);
-            // gates of the seam tokens (lanes 0-7 of the first staging warp: alpha, 8-15: beta)
-            float gab = 0.f;
-            if (c < 2 * WMAX && (c & (WMAX - 1)) < sw) {
-                const size_t gi = gate_index(dm, a.tok.N, l, tab.off[s] + (c & (WMAX - 1)), h);
-                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(c < WMAX ? a.tok.alpha : a.tok.beta);
-                gab = __bfloat162float(src[gi]);
-            } else if (c < WMAX) {
-                gab = 1.f;  // padding token: alpha = 1, beta = 0
-            }
+            const float gab = gab_next;
+            gab_next = gate(e + 1);  // in flight while this entry is staged
             bool wt = true;
             if (c == 0) {
                 if (e >= 2) wt = wait_bar(bar(B_BUFFREE0 + b), ((e - 2) >> 1) & 1, abort_flag);
@@ -486,15 +548,14 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                 load_raw(e + 2);
                 raw_armed = e + 3;
             }
-            // ---- operand tiles: [k ; q] split in tf32 hi / lo, K^T, V
+            // ---- operand tiles: [k ; q] in tf32 and in fp32, K^T split hi / lo, V
 #pragma unroll
             for (int t = 0; t < WMAX; ++t) {
                 const float kh = tc::round_tf32(kv[t]), kl = tc::round_tf32(kv[t] - kh);
-                const float qh = tc::round_tf32(qv[t]), ql = tc::round_tf32(qv[t] - qh);
                 *reinterpret_cast<float *>(buf + BF_KQH + tc::sw128_f32(t, c, 2 * WMAX)) = kh;
-                *reinterpret_cast<float *>(buf + BF_KQL + tc::sw128_f32(t, c, 2 * WMAX)) = kl;
-                *reinterpret_cast<float *>(buf + BF_KQH + tc::sw128_f32(WMAX + t, c, 2 * WMAX)) = qh;
-                *reinterpret_cast<float *>(buf + BF_KQL + tc::sw128_f32(WMAX + t, c, 2 * WMAX)) = ql;
+                *reinterpret_cast<float *>(buf + BF_KQH + tc::sw128_f32(WMAX + t, c, 2 * WMAX)) = tc::round_tf32(qv[t]);
+                *reinterpret_cast<float *>(buf + BF_KQF + tc::sw128_f32(t, c, 2 * WMAX)) = kv[t];
+                *reinterpret_cast<float *>(buf + BF_KQF + tc::sw128_f32(WMAX + t, c, 2 * WMAX)) = qv[t];
                 *reinterpret_cast<float *>(buf + BF_KP + tc::sw128_f32(c, t, D)) = kh;
                 *reinterpret_cast<float *>(buf + BF_KP + tc::sw128_f32(c, WMAX + t, D)) = kh;
                 *reinterpret_cast<float *>(buf + BF_KP + tc::sw128_f32(c, 2 * WMAX + t, D)) = kl;
@@ -523,54 +584,51 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             }
             tc::fence_async_smem();
             tc::bar_sync(BAR_STAGE, NG);
-            // ---- the 64 dot products k_t.k_s (s < t) and q_t.k_s (s <= t), fp32 from hi + lo
+            // ---- the 64 dot products k_t.k_s (s < t), q_t.k_s (s <= t) (two threads each),
+            // and the decays e^{g_t - g_s} (s <= t)
             {
                 const int p = c >> 1, half = c & 1;
                 int ra, rb, tt, ss;
                 dot_rows(p, ra, rb, tt, ss);
                 float acc = 0.f;
-#pragma unroll 8
+#pragma unroll 4
                 for (int cc = 64 * half; cc < 64 * half + 64; cc += 4) {
-                    const float4 ah = *reinterpret_cast<const float4 *>(buf + BF_KQH + tc::sw128_f32(ra, cc, 2 * WMAX));
-                    const float4 al = *reinterpret_cast<const float4 *>(buf + BF_KQL + tc::sw128_f32(ra, cc, 2 * WMAX));
-                    const float4 bh = *reinterpret_cast<const float4 *>(buf + BF_KQH + tc::sw128_f32(rb, cc, 2 * WMAX));
-                    const float4 bl = *reinterpret_cast<const float4 *>(buf + BF_KQL + tc::sw128_f32(rb, cc, 2 * WMAX));
-                    acc = fmaf(ah.x + al.x, bh.x + bl.x, acc);
-                    acc = fmaf(ah.y + al.y, bh.y + bl.y, acc);
-                    acc = fmaf(ah.z + al.z, bh.z + bl.z, acc);
-                    acc = fmaf(ah.w + al.w, bh.w + bl.w, acc);
+                    const float4 av = *reinterpret_cast<const float4 *>(buf + BF_KQF + tc::sw128_f32(ra, cc, 2 * WMAX));
+                    const float4 bv = *reinterpret_cast<const float4 *>(buf + BF_KQF + tc::sw128_f32(rb, cc, 2 * WMAX));
+                    acc = fmaf(av.x, bv.x, acc);
+                    acc = fmaf(av.y, bv.y, acc);
+                    acc = fmaf(av.z, bv.z, acc);
+                    acc = fmaf(av.w, bv.w, acc);
                 }
                 acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                 if (half == 0) dots[p] = acc;
+                if (c >= 64) {
+                    const int t = (c - 64) >> 3, s2 = (c - 64) & 7;
+                    scr[c - 64] = (s2 <= t) ? smf[SMALL_B + s2] * expf(smf[SMALL_LG + t] - smf[SMALL_LG + s2]) : 0.f;
+                }
             }
             tc::bar_sync(BAR_STAGE, NG);
-            // ---- M = (I + L)^{-1}, L_tr = beta_r e^{g_t - g_r} k_t.k_r (r < t): one column per
-            // thread (threads 0-7); AQ_ts = beta_s e^{g_t - g_s} q_t.k_s (s <= t): one row per thread (8-15)
+            // ---- AQ_ts = beta_s e^{g_t - g_s} q_t.k_s, L_ts = beta_s e^{g_t - g_s} k_t.k_s
+            if (c < 64) {
+                const int t = c >> 3, s2 = c & 7;
+                const float be = scr[c];
+                smf[SMALL_AQ + c] = (s2 <= t) ? be * dots[28 + t * (t + 1) / 2 + s2] : 0.f;
+                scr[64 + c] = (s2 < t) ? be * dots[t * (t - 1) / 2 + s2] : 0.f;
+            }
+            tc::bar_sync(BAR_STAGE, NG);
+            // ---- M = (I + L)^{-1}, one column per thread
             if (c < WMAX) {
-                const int col = c;
+                const float *Lm = scr + 64;
                 float x[WMAX];
 #pragma unroll
                 for (int t = 0; t < WMAX; ++t) {
-                    float acc = (t == col) ? 1.f : 0.f;
+                    float acc = (t == c) ? 1.f : 0.f;
 #pragma unroll
-                    for (int r = 0; r < t; ++r)
-                        acc = fmaf(-dots[t * (t - 1) / 2 + r] * smf[SMALL_B + r] *
-                                       expf(smf[SMALL_LG + t] - smf[SMALL_LG + r]),
-                                   x[r], acc);
-                    x[t] = (t < col) ? 0.f : acc;
+                    for (int r = 0; r < t; ++r) acc = fmaf(-Lm[t * WMAX + r], x[r], acc);
+                    x[t] = (t < c) ? 0.f : acc;
                 }
 #pragma unroll
-                for (int t = 0; t < WMAX; ++t) smf[SMALL_M + t * WMAX + col] = x[t];
-            } else if (c < 2 * WMAX) {
-                const int t = c - WMAX;
-#pragma unroll
-                for (int s2 = 0; s2 < WMAX; ++s2) {
-                    float v = 0.f;
-                    if (s2 <= t)
-                        v = dots[28 + t * (t + 1) / 2 + s2] * smf[SMALL_B + s2] *
-                            expf(smf[SMALL_LG + t] - smf[SMALL_LG + s2]);
-                    smf[SMALL_AQ + t * WMAX + s2] = v;
-                }
+                for (int t = 0; t < WMAX; ++t) smf[SMALL_M + t * WMAX + c] = x[t];
             }
             tc::bar_sync(BAR_STAGE, NG);
             if (c == 0) tc::mbar_arrive(bar(B_STAGED0 + b));
@@ -580,65 +638,6 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             for (int k = (raw_armed > 2 ? raw_armed - 2 : 0); k < raw_armed; ++k)
                 while (!tc::mbar_test(bar(B_FULLR0 + (k & 1)), (k >> 1) & 1) && clock64() - t0 < kWaitCycles) {
                 }
-        }
-    } else if (warp == WARP_MMA && lane == 0) {
-        // ================================================= MMA issue and T_C copies
-        int t_armed = 0;
-        if (n_ent > 0) {
-            load_T(0);
-            t_armed = 1;
-        }
-        for (int e = 0; e < n_ent; ++e) {
-            const int b = e & 1;
-            const uint32_t buf = s_base + SM_BUF + b * BUF_BYTES;
-            if (!wait_bar(bar(B_XREADY), e & 1, abort_flag)) break;
-            if (w > 0) {
-                if (!wait_bar(bar(B_STAGED0 + b), (e >> 1) & 1, abort_flag)) break;
-                tc::fence_after();
-                // [u | z] = X [k | q]^T, 3xTF32: Xhi khi + Xlo khi + Xhi klo
-#pragma unroll 1
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ts(tb + TM_D2, tb + TM_XHI + ks * 8, tc::sdesc_kstep(buf + BF_KQH, 2 * WMAX, ks),
-                               tc::idesc_tf32(128, 2 * WMAX), ks > 0);
-#pragma unroll 1
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ts(tb + TM_D2, tb + TM_XLO + ks * 8, tc::sdesc_kstep(buf + BF_KQH, 2 * WMAX, ks),
-                               tc::idesc_tf32(128, 2 * WMAX), 1);
-#pragma unroll 1
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_ts(tb + TM_D2, tb + TM_XHI + ks * 8, tc::sdesc_kstep(buf + BF_KQL, 2 * WMAX, ks),
-                               tc::idesc_tf32(128, 2 * WMAX), 1);
-                tc::commit(bar(B_SEAMDONE));
-                if (!wait_bar(bar(B_WREADY), e & 1, abort_flag)) break;
-                tc::fence_after();
-                // X += W K: [Whi | Wlo | Whi] against K^T columns [hi | hi | lo]
-#pragma unroll 1
-                for (int ks = 0; ks < 3; ++ks)
-                    tc::mma_ts(tb + TM_X, tb + TM_W + ks * 8, tc::sdesc_kstep(buf + BF_KP, D, ks),
-                               tc::idesc_tf32(128, 128), 1);
-                tc::commit(bar(B_UPDDONE));
-                tc::commit(bar(B_BUFFREE0 + b));
-                if (!wait_bar(bar(B_XHIREADY), e & 1, abort_flag)) break;
-            }
-            if (!wait_bar(bar(B_FULLT), e & 1, abort_flag)) break;
-            tc::fence_after();
-            // Y = Xhi T_C^T, i.e. (T_C S)^T
-#pragma unroll 1
-            for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_ts(tb + TM_Y, tb + TM_XHI + ks * 8, tc::sdesc_kstep(s_base + SM_T, D, ks),
-                           tc::idesc_tf32(128, 128), ks > 0);
-            tc::commit(bar(B_BODYDONE));
-            if (e + 1 < n_ent) {
-                // T_C buffer free once the body MMA is done
-                if (!wait_bar(bar(B_BODYDONE), e & 1, abort_flag)) break;
-                load_T(e + 1);
-                t_armed = e + 2;
-            }
-        }
-        if (*abort_flag && t_armed > 0) {
-            const long long t0 = clock64();
-            while (!tc::mbar_test(bar(B_FULLT), (t_armed - 1) & 1) && clock64() - t0 < kWaitCycles) {
-            }
         }
     }
     tc::fence_before();
