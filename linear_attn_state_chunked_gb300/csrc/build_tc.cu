@@ -738,7 +738,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             for (int r = 0; r < 4; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
 #pragma unroll
                         for (int r = 0; r < 4; ++r) {
-                            const float inv = 1.f / sqrtf(ss[r] + kL2Eps);
+                            const float inv = rsqrtf(ss[r] + kL2Eps);  // hardware reciprocal square root
 #pragma unroll
                             for (int i = 0; i < 8; ++i) kx[r][i] *= inv;
                         }

@@ -66,8 +66,8 @@ constexpr uint32_t BF_KP = 16384;    //   K^T [128][32] sw128: columns t, 8 + t 
 constexpr uint32_t BF_V = 32768;     //   v_t [8][128] fp32
 constexpr uint32_t BF_SMALL = 36864; //   M [8][8], AQ [8][8], Gamma [8], d [8], Gamma_w, beta [8], g [8]
 constexpr uint32_t BUF_BYTES = 37888;
-constexpr int SMALL_M = 0, SMALL_AQ = 64, SMALL_G = 128, SMALL_D = 136, SMALL_GL = 144, SMALL_B = 152,
-              SMALL_LG = 160;
+constexpr int SMALL_M = 0, SMALL_AQ = 64, SMALL_G = 128, SMALL_D = 136, SMALL_GL = 144, SMALL_SW = 145,
+              SMALL_B = 152, SMALL_LG = 160;
 constexpr uint32_t RAW_T = (HIST + WMAX) * D * 2;           // raw rows per tensor (bf16)
 constexpr uint32_t SM_RAW = SM_BUF + 2 * BUF_BYTES;         // 2 x {q, k, v} raw rows (TMA)
 constexpr uint32_t SM_RED = SM_RAW + 2 * 3 * RAW_T;         // staging scratch (below)
@@ -181,18 +181,27 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
     tc::fence_after();
     const uint32_t tb = *tmem_base_sh;
 
+    // first row of entry e's pair in the [L * n_seg * H * 128][128] views of T and S
     auto pair_row = [&](int e) { return (int)((((size_t)l * tab.n_seg + tab.perm[e]) * dm.H + h) * D); };
-    auto load_T = [&](int e) {
+    auto load_T = [&](int row) {
         tc::mbar_arrive_expect_tx(bar(B_FULLT), D * D * 4);
 #pragma unroll
         for (int at = 0; at < 4; ++at)
-            tc::tma_load_2d(s_base + SM_T + at * 16384, &tmT, 32 * at, pair_row(e), bar(B_FULLT));
+            tc::tma_load_2d(s_base + SM_T + at * 16384, &tmT, 32 * at, row, bar(B_FULLT));
     };
-    auto load_SC = [&](int e) {
+    // T_C and S(C|0) of a pair into L2 ahead of their copies to shared memory
+    auto prefetch_pair = [&](int row) {
+#pragma unroll
+        for (int at = 0; at < 4; ++at) {
+            tc::tma_prefetch_2d(&tmT, 32 * at, row);
+            tc::tma_prefetch_2d(&tmS, 32 * at, row);
+        }
+    };
+    auto load_SC = [&](int row) {
         tc::mbar_arrive_expect_tx(bar(B_FULLSC), D * D * 4);
 #pragma unroll
         for (int at = 0; at < 4; ++at)
-            tc::tma_load_2d(s_base + SM_SC + at * 16384, &tmS, 32 * at, pair_row(e), bar(B_FULLSC));
+            tc::tma_load_2d(s_base + SM_SC + at * 16384, &tmS, 32 * at, row, bar(B_FULLSC));
     };
     // raw seam rows of entry e (and the conv history rows when they are the
     // previous entry's last tokens) into raw buffer e & 1
@@ -255,10 +264,18 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             okw = tc::bar_and(BAR_STATE, NS, wt);
             return reinterpret_cast<const float *>(sm + SM_BUF + (e & 1) * BUF_BYTES + BF_SMALL)[SMALL_GL];
         };
+        // thread 0 keeps the pair rows of entries e + 1 and e + 2 in registers,
+        // looked up one entry ahead of their use
+        int row1 = 0, row2 = 0;
         if (tid == 0 && n_ent > 0) {
-            load_T(0);
-            load_SC(0);
+            load_T(pair_row(0));
+            load_SC(pair_row(0));
             t_armed = sc_armed = 1;
+            if (n_ent > 1) {
+                row1 = pair_row(1);
+                prefetch_pair(row1);
+            }
+            if (n_ent > 2) row2 = pair_row(2);
         }
         bool ok = true;
         // X = Gamma_w S_init^T (or 0), Xhi = tf32(S_init^T); S_prefix[0] = S_init
@@ -285,15 +302,16 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
         }
         for (int e = 0; e < n_ent && ok; ++e) {
             const uint8_t *buf = sm + SM_BUF + (e & 1) * BUF_BYTES;
+            if (tid == 0 && e + 2 < n_ent) prefetch_pair(row2);
             bool wt = true;
             if (w > 0) {
                 // ---- seam outputs and the update operand W
-                const int sw = seam_len(tab, e, w);
                 if (tid == 0) wt = wait_bar(bar(B_SEAMDONE), e & 1, abort_flag);
                 if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
                 tc::fence_after();
                 const float *smf = reinterpret_cast<const float *>(buf + BF_SMALL);
                 const float *Vr = reinterpret_cast<const float *>(buf + BF_V);
+                const int sw = reinterpret_cast<const int *>(smf)[SMALL_SW];
                 float uz[2 * WMAX];
                 {
                     float p0[32], p1[32];
@@ -378,7 +396,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
             tc::fence_after();
             if (tid == 0 && !last) {
-                load_T(e + 1);  // T_C buffer free: the body MMA is done
+                load_T(row1);  // T_C buffer free: the body MMA is done
                 t_armed = e + 2;
             }
             float *out = last ? a.S_final + st_base
@@ -405,9 +423,11 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             tc::fence_before();
             tc::bar_sync(BAR_STATE, NS);
             if (tid == 0 && !last) {
-                load_SC(e + 1);  // S(C|0) buffer consumed
+                load_SC(row1);  // S(C|0) buffer consumed
                 sc_armed = e + 2;
                 if (w > 0) issue_seam(e + 1);
+                row1 = row2;
+                if (e + 3 < n_ent) row2 = pair_row(e + 3);
             }
         }
         if (!ok && tid == 0) {
@@ -538,8 +558,8 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                         aa += red[(ww * WMAX + t) * 2];
                         bb += red[(ww * WMAX + t) * 2 + 1];
                     }
-                    qv[t] *= 1.f / sqrtf(aa + kL2Eps);
-                    kv[t] *= 1.f / sqrtf(bb + kL2Eps);
+                    qv[t] *= rsqrtf(aa + kL2Eps);  // hardware reciprocal square root
+                    kv[t] *= rsqrtf(bb + kL2Eps);
                 }
             }
             // raw buffer b consumed: the rows of entry e + 2 may load into it
@@ -579,7 +599,10 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                     smf[SMALL_B + lane] = be;
                     smf[SMALL_G + lane] = expf(g);
                     smf[SMALL_D + lane] = be * expf(gw7 - g);
-                    if (lane == 0) smf[SMALL_GL] = expf(gw7);
+                    if (lane == 0) {
+                        smf[SMALL_GL] = expf(gw7);
+                        reinterpret_cast<int *>(smf)[SMALL_SW] = sw;
+                    }
                 }
             }
             tc::fence_async_smem();

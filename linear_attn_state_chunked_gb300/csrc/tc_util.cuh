@@ -212,6 +212,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
                  : "memory");
 }
 
+// Prefetch the box at (c0, c1) of a 2-D tensor map into L2 (no shared-memory
+// destination, no completion signal).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1) : "memory");
+}
+
 // Named barrier over `count` threads that also returns whether every
 // participating thread passed a true predicate.
 __device__ __forceinline__ bool bar_and(int id, int count, bool pred)
