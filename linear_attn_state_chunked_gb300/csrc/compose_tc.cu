@@ -112,20 +112,29 @@ struct TokMaps {
     CUtensorMap rows3[3];  // q, k, v: boxes of HIST token rows (conv history)
 };
 
-// Whether the conv history of entry e's seam is the previous entry's last
-// HIST tokens, fetched by TMA (otherwise the history crosses several short
-// segments or precedes the request, and the staging reads it directly).
-__device__ __forceinline__ bool hist_by_tma(const SegTable &tab, int e)
-{
-    if (e == 0) return false;
-    const int sp = tab.perm[e - 1];
-    return tab.off[sp + 1] - tab.off[sp] >= HIST;
-}
+// What the staging needs of request entry e, read from the request table in
+// one go (the table sits in the constant bank, where misses are slow, so the
+// staging looks entries up ahead of their use).
+struct EntryInfo {
+    int32_t off;   // first token of the segment
+    int sw;        // seam length
+    int htma;      // conv history by TMA (the previous entry has >= HIST tokens)
+    int32_t hrow;  // first conv-history row when htma
+};
 
-__device__ __forceinline__ int seam_len(const SegTable &tab, int e, int w)
+__device__ __forceinline__ EntryInfo entry_info(const SegTable &tab, int e, int w, int ck)
 {
+    EntryInfo r{0, 0, 0, 0};
     const int s = tab.perm[e];
-    return min(w, tab.off[s + 1] - tab.off[s]);
+    r.off = tab.off[s];
+    r.sw = min(w, tab.off[s + 1] - r.off);
+    if (ck > 0 && e > 0) {
+        const int sp = tab.perm[e - 1];
+        const int32_t pend = tab.off[sp + 1];
+        r.htma = (pend - tab.off[sp]) >= HIST;
+        r.hrow = pend - HIST;
+    }
+    return r;
 }
 
 // Dot product index p (0..63) of the staged seam: 28 k_t.k_s (s < t), then
@@ -205,22 +214,19 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
     };
     // raw seam rows of entry e (and the conv history rows when they are the
     // previous entry's last tokens) into raw buffer e & 1
-    auto load_raw = [&](int e) {
-        const int s = tab.perm[e];
+    auto load_raw = [&](int e, const EntryInfo &ei) {
         const uint32_t fb = bar(B_FULLR0 + (e & 1));
-        const int sw = seam_len(tab, e, w);
-        if (sw == 0) {
+        if (ei.sw == 0) {
             tc::mbar_arrive(fb);
             return;
         }
-        const bool htma = CK > 0 && hist_by_tma(tab, e);
+        const bool htma = CK > 0 && ei.htma;
         tc::mbar_arrive_expect_tx(fb, 3 * WMAX * D * 2 + (htma ? 3 * HIST * D * 2 : 0));
         const uint32_t rb = s_base + SM_RAW + (e & 1) * 3 * RAW_T;
 #pragma unroll
         for (int x3 = 0; x3 < 3; ++x3) {
-            tc::tma_load_4d(rb + x3 * RAW_T + HIST * D * 2, &tmX.rows8[x3], 0, h, tab.off[s], l, fb);
-            if (htma)
-                tc::tma_load_4d(rb + x3 * RAW_T, &tmX.rows3[x3], 0, h, tab.off[tab.perm[e - 1] + 1] - HIST, l, fb);
+            tc::tma_load_4d(rb + x3 * RAW_T + HIST * D * 2, &tmX.rows8[x3], 0, h, ei.off, l, fb);
+            if (htma) tc::tma_load_4d(rb + x3 * RAW_T, &tmX.rows3[x3], 0, h, ei.hrow, l, fb);
         }
     };
 
@@ -264,9 +270,10 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             okw = tc::bar_and(BAR_STATE, NS, wt);
             return reinterpret_cast<const float *>(sm + SM_BUF + (e & 1) * BUF_BYTES + BF_SMALL)[SMALL_GL];
         };
-        // thread 0 keeps the pair rows of entries e + 1 and e + 2 in registers,
-        // looked up one entry ahead of their use
-        int row1 = 0, row2 = 0;
+        // thread 0 keeps the pair rows of entries e + 1 and e + 2 in registers;
+        // the request table lives in the constant bank, whose misses cost
+        // thousands of cycles, so each lookup is issued an entry before its use
+        int row1 = 0, row2 = 0, row3 = 0;
         if (tid == 0 && n_ent > 0) {
             load_T(pair_row(0));
             load_SC(pair_row(0));
@@ -302,7 +309,10 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
         }
         for (int e = 0; e < n_ent && ok; ++e) {
             const uint8_t *buf = sm + SM_BUF + (e & 1) * BUF_BYTES;
-            if (tid == 0 && e + 2 < n_ent) prefetch_pair(row2);
+            if (tid == 0) {
+                if (e + 2 < n_ent) prefetch_pair(row2);
+                if (e + 3 < n_ent) row3 = pair_row(e + 3);
+            }
             bool wt = true;
             if (w > 0) {
                 // ---- seam outputs and the update operand W
@@ -315,8 +325,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                 float uz[2 * WMAX];
                 {
                     float p0[32], p1[32];
-                    tc::tmem_ld32(my + TM_D2, p0);
-                    tc::tmem_ld32(my + TM_D2 + 32, p1);
+                    tc::tmem_ld32x2(my + TM_D2, p0, p1);
 #pragma unroll
                     for (int cc = 0; cc < 2 * WMAX; ++cc) uz[cc] = (p0[cc] + p0[16 + cc]) + (p1[cc] + p1[16 + cc]);
                 }
@@ -427,7 +436,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                 sc_armed = e + 2;
                 if (w > 0) issue_seam(e + 1);
                 row1 = row2;
-                if (e + 3 < n_ent) row2 = pair_row(e + 3);
+                row2 = row3;
             }
         }
         if (!ok && tid == 0) {
@@ -458,29 +467,35 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
         float *scr = red + RED_SCR;
         // gates of entry e's seam tokens: threads 0-7 alpha_t (1 past the
         // segment), 8-15 beta_t (0 past the segment)
-        auto gate = [&](int e) {
+        auto gate = [&](const EntryInfo &ei) {
             float v = (c < WMAX) ? 1.f : 0.f;
-            if (c < 2 * WMAX && e < n_ent && (c & (WMAX - 1)) < seam_len(tab, e, w)) {
-                const size_t gi = gate_index(dm, a.tok.N, l, tab.off[tab.perm[e]] + (c & (WMAX - 1)), h);
+            if (c < 2 * WMAX && (c & (WMAX - 1)) < ei.sw) {
+                const size_t gi = gate_index(dm, a.tok.N, l, ei.off + (c & (WMAX - 1)), h);
                 const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(c < WMAX ? a.tok.alpha : a.tok.beta);
                 v = __bfloat162float(src[gi]);
             }
             return v;
         };
+        // entries e (cur), e + 1 (nx1) and e + 2 (nx2) of the request table
+        EntryInfo cur{0, 0, 0, 0}, nx1{0, 0, 0, 0}, nx2{0, 0, 0, 0};
+        if (w > 0 && n_ent > 0) cur = entry_info(tab, 0, w, CK);
+        if (w > 0 && n_ent > 1) nx1 = entry_info(tab, 1, w, CK);
         int raw_armed = 0;
         if (w > 0 && c == 0) {
-            for (int e = 0; e < 2 && e < n_ent; ++e) load_raw(e);
+            if (n_ent > 0) load_raw(0, cur);
+            if (n_ent > 1) load_raw(1, nx1);
             raw_armed = min(2, n_ent);
         }
-        float gab_next = (w > 0) ? gate(0) : 0.f;
+        float gab_next = (w > 0 && n_ent > 0) ? gate(cur) : 0.f;
         bool ok = true;
         for (int e = 0; w > 0 && e < n_ent && ok; ++e) {
             const int b = e & 1;
             uint8_t *buf = sm + SM_BUF + b * BUF_BYTES;
             const uint8_t *raw = sm + SM_RAW + b * 3 * RAW_T;
-            const int sw = seam_len(tab, e, w);
+            const int sw = cur.sw;
+            if (e + 2 < n_ent) nx2 = entry_info(tab, e + 2, w, CK);  // used after the conv
             const float gab = gab_next;
-            gab_next = gate(e + 1);  // in flight while this entry is staged
+            gab_next = (e + 1 < n_ent) ? gate(nx1) : 0.f;  // in flight while this entry is staged
             bool wt = true;
             if (c == 0) {
                 if (e >= 2) wt = wait_bar(bar(B_BUFFREE0 + b), ((e - 2) >> 1) & 1, abort_flag);
@@ -488,7 +503,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             }
             if (!tc::bar_and(BAR_STAGE, NG, wt)) { ok = false; break; }
             // ---- conv (along the request stream) and L2 normalisation of q, k
-            const bool htma = CK > 0 && hist_by_tma(tab, e);
+            const bool htma = CK > 0 && cur.htma;
             auto raw_at = [&](int tensor, int row) {
                 const uint16_t u = *reinterpret_cast<const uint16_t *>(raw + tensor * RAW_T + (row * D + c) * 2);
                 return __uint_as_float(static_cast<uint32_t>(u) << 16);
@@ -565,7 +580,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             // raw buffer b consumed: the rows of entry e + 2 may load into it
             tc::bar_sync(BAR_STAGE, NG);
             if (c == 0 && e + 2 < n_ent) {
-                load_raw(e + 2);
+                load_raw(e + 2, nx2);
                 raw_armed = e + 3;
             }
             // ---- operand tiles: [k ; q] in tf32 and in fp32, K^T split hi / lo, V
@@ -655,6 +670,8 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             }
             tc::bar_sync(BAR_STAGE, NG);
             if (c == 0) tc::mbar_arrive(bar(B_STAGED0 + b));
+            cur = nx1;
+            nx1 = nx2;
         }
         if (!ok && c == 0 && raw_armed > 0) {
             const long long t0 = clock64();
