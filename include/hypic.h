@@ -1,8 +1,8 @@
 /*
  * hypic.h -- C ABI of the linear-attention hot path of position-independent
  * caching (PIC) for hybrid-attention models, as described in the HYPIC pages
- * (codernav.top summary, sections "线性层", "全注意力层" and "段并行";
- * xix.ai article, paragraphs on linear layers, seam windows and segment-level
+ * (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, sections "线性层", "全注意力层" and "段并行";
+ * article “Xiaohongshu, Peking University, Shanghai Jiao Tong University Unveil HYPIC to Slash First Token Latency by 3.25x in Hybrid Attention Models”, paragraphs on linear layers, seam windows and segment-level
  * parallelism).
  *
  * The method.  A linear-attention layer keeps a state S (d_k x d_v, fp32 here)
@@ -206,7 +206,7 @@ int hypic_segment_build_noalloc(const hypic_desc *desc, const hypic_tokens *tok,
  * seams re-run under the full prefix, advancing the running state and passing
  * each seam token's output up.)  With conv_k > 0 a seam token's convolution
  * history is the previous entry's last raw tokens (zero before the request
- * start): the pages' "convolution state warm-up".
+ * start): the articles' "convolution state warm-up".
  *
  * T, S: the cache, as written by hypic_segment_build with the same desc and
  * n_seg.  tok: the request's tokens (may be NULL when seam_w == 0).

@@ -4,15 +4,15 @@
 // the fp32-input workloads (1e-5 tolerance) use.  One CTA per work item
 // (segment body, layer, head); items are launched longest body first, which
 // the block scheduler dispatches in order -- the greedy longest-processing-
-// time-first assignment of the HYPIC pages (codernav.top summary, section
-// "段并行"; xix.ai article, segment-parallelism paragraph).
+// time-first assignment of the HYPIC pages (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, section
+// "段并行"; article “Xiaohongshu, Peking University, Shanghai Jiao Tong University Unveil HYPIC to Slash First Token Latency by 3.25x in Hybrid Attention Models”, segment-parallelism paragraph).
 //
 // Gated delta keeps X = [T | S] (d_k x (d_k + d_v)) with one thread per
 // column: for each token, u_c = sum_r k_r X_rc and
 //     X_rc <- alpha (X_rc - beta k_r u_c) + beta k_r vbar_c ,
 // where vbar is 0 on the T columns and v on the S columns -- the transition
 // A_t = alpha (I - beta k k^T) applied on the left, plus the write
-// beta k v^T on the S half (the pair (T_C, S(C|0)) of the pages' "线性层").
+// beta k v^T on the S half (the pair (T_C, S(C|0)) of that article's "线性层").
 // The two specialisations keep only S and form T as the product of gates.
 #include "common.cuh"
 #include "kernels.h"

@@ -2,8 +2,9 @@
 // cores, chunked in the WY form, for d_k = d_v = 128 and bf16 inputs.
 //
 // Math (derived from the recurrence S_t = alpha_t (I - beta_t k_t k_t^T)
-// S_{t-1} + beta_t k_t v_t^T and the pair of the HYPIC pages' "线性层"
-// section).  Within a chunk of C = 64 tokens let g_t = sum_{s<=t} log alpha_s,
+// S_{t-1} + beta_t k_t v_t^T and the pair (T_C, S(C|0)) of section "线性层"
+// of the article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token
+// 延迟降低 3.25 倍，实现位置无关缓存”).  Within a chunk of C = 64 tokens let g_t = sum_{s<=t} log alpha_s,
 // Gamma_t = exp(g_t).  Writing u_t = v_t - alpha_t S_{t-1}^T k_t, one finds
 //   S_C = Gamma_C S_0 + K^T D U,   U = (I + L)^{-1} (V - diag(Gamma) K S_0),
 //   L_tj = beta_j exp(g_t - g_j) k_t.k_j  (j < t),  D = diag(beta_j exp(g_C - g_j)).
@@ -15,7 +16,9 @@
 //   Xt = Gamma_C Xt + Rt U~           (tf32 MMA, A = Rt from tensor memory)
 //   U~^T = K^T D (I + L)^{-1}         (Gram K K^T and U~ on the tensor core,
 //                                      the 64 x 64 unit lower inverse by
-//                                      blocked substitution on CUDA cores)
+//                                      doubling from 8 x 8 blocks: forward
+//                                      substitution on CUDA cores, block
+//                                      products on warp-level MMAs)
 // Operands written by threads are rounded to tf32 (the tensor core
 // truncates).
 //
@@ -30,7 +33,7 @@
 //   warps 0-3   epilogue of chunk n: Rt and the Gamma_C rescale of Xt, both
 //               halves, and the emission of each finished pair.
 // Work items (segment body, layer, head) arrive longest body first; CTA b
-// takes items b, b + grid, ... -- the greedy LPT order of the pages' "段并行"
+// takes items b, b + grid, ... -- the greedy LPT order of that article's "段并行"
 // section as a single-GPU stand-in for its scatter workers.
 #include <cuda.h>
 #include <cudaTypedefs.h>

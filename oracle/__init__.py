@@ -9,15 +9,15 @@ The arithmetic primitives below are the plain definitions (see ``oracle.c``
 for the recurrence, the pair and composition, cited there):
 
 * :func:`recurrence` -- the per-token recurrence S_t = A_t S_{t-1} + W_t,
-  o_t = S_t^T q_t (HYPIC pages: codernav.top summary, section "线性层";
-  xix.ai article, linear-layer paragraph; the gated-delta convention with
+  o_t = S_t^T q_t (HYPIC pages: article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, section "线性层";
+  article “Xiaohongshu, Peking University, Shanghai Jiao Tong University Unveil HYPIC to Slash First Token Latency by 3.25x in Hybrid Attention Models”, linear-layer paragraph; the gated-delta convention with
   scalar-decay and diagonal-gate specialisations).
 * :func:`pair` -- (T_C, S(C|0)) of a segment: ordered product of the
   transitions and the zero-initial final state (same sections).
 * :func:`compose` -- S(C1 C2) = T(C2) S(C1) + S(C2) (same sections).
 * :func:`causal_conv` and :func:`l2_normalize` -- the causal depthwise
   convolution that the pages' "convolution state warm-up" patch refers to
-  (codernav.top summary, section "线性层", last paragraph), followed by the
+  (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, section "线性层", last paragraph), followed by the
   per-head L2 normalisation of q and k that gated-delta layers apply after
   it.  The pages give neither formula; the readings are: kernel size K, lag j
   multiplies x_{t-j}, zero history before the request start, no bias, no

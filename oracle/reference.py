@@ -15,7 +15,7 @@ widened):
 Segments are given by offsets seg_off[0..n_seg] into the token axis; a
 request is an order of segment indices.  Each segment's first min(w, len)
 tokens are its seam window; the cached pair covers the rest (the body).
-HYPIC pages (codernav.top summary, section "全注意力层"; xix.ai article,
+HYPIC pages (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, section "全注意力层"; article “Xiaohongshu, Peking University, Shanghai Jiao Tong University Unveil HYPIC to Slash First Token Latency by 3.25x in Hybrid Attention Models”,
 seam-window paragraph): seam tokens are not cached and are re-run under the
 full prefix, advancing the running state and emitting per-token outputs.
 """

@@ -79,7 +79,7 @@ def test_brute_force_dense_products(mode, n):
 
 @pytest.mark.parametrize("mode", [GATED_DELTA, SCALAR_DECAY, DIAG_GATE])
 def test_composition_law(mode):
-    """S(C1 C2) = T(C2) S(C1) + S(C2) (codernav.top summary, 线性层)."""
+    """S(C1 C2) = T(C2) S(C1) + S(C2) (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, 线性层)."""
     rng = np.random.default_rng(11 + mode)
     dk = dv = 8
     n1, n2 = 37, 29
@@ -154,7 +154,7 @@ def test_diagonal_gate_closed_form():
 @pytest.mark.parametrize("mode", [SCALAR_DECAY, DIAG_GATE])
 def test_naive_addition_exact_for_plain_linear_attention(mode):
     """With A_t = I (plain linear attention) summing zero-initial states is
-    exact (codernav.top summary, 线性层)."""
+    exact (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, 线性层)."""
     rng = np.random.default_rng(8)
     dk = dv = 5
     ns = [13, 21, 8]
@@ -174,7 +174,7 @@ def test_naive_addition_exact_for_plain_linear_attention(mode):
 @pytest.mark.parametrize("mode", [GATED_DELTA, SCALAR_DECAY, DIAG_GATE])
 def test_naive_addition_wrong_under_decay(mode):
     """Under decay, gating or delta erasure the straw man is structurally
-    wrong (codernav.top summary, 线性层)."""
+    wrong (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, 线性层)."""
     rng = np.random.default_rng(9 + mode)
     dk = dv = 8
     n1 = n2 = 64
