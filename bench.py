@@ -328,7 +328,10 @@ def run_gpu(args):
     comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
 
     # end to end through the C ABI from pinned host buffers (h2d inputs,
-    # d2h final state and seam outputs inside the timed region)
+    # d2h final state and seam outputs inside the timed region).  The layers
+    # are independent, so the step streams them in groups: the inputs of
+    # group g + 1 cross the host link while group g is built and composed
+    # (token tensors are layer-major, so a group is one contiguous slab).
     e2e = None
     if not args.no_e2e:
         host = {}
@@ -336,19 +339,45 @@ def run_gpu(args):
             if v is not None:
                 host[key] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                 host[key].copy_(v)
-        h_Sf = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
-        h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        h_Sf = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
+        h_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
         d2h = Sf.numel() * 4 + o.numel() * 4
         n_e2e = max(1, min(args.steps, 3))
+        n_groups = min(L, args.e2e_groups)
+        bounds = [round(g * L / n_groups) for g in range(n_groups + 1)]
+        groups = [(bounds[g], bounds[g + 1]) for g in range(n_groups) if bounds[g + 1] > bounds[g]]
+        cs_in = torch.cuda.Stream(dev)
+        cs_out = torch.cuda.Stream(dev)
 
         def e2e_step():
-            for key, hv in host.items():
-                if hv is not None:
-                    wl.tok[key].copy_(hv, non_blocking=True)
-            step()
-            h_Sf.copy_(Sf, non_blocking=True)
-            h_o.copy_(o, non_blocking=True)
+            start_ev = torch.cuda.Event()
+            start_ev.record(stream)
+            cs_in.wait_event(start_ev)
+            ev_in = []
+            for (l0, l1) in groups:
+                with torch.cuda.stream(cs_in):
+                    for key, hv in host.items():
+                        wl.tok[key][l0:l1].copy_(hv[l0:l1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs_in)
+                ev_in.append(ev)
+            for (l0, l1), ev in zip(groups, ev_in):
+                stream.wait_event(ev)
+                dg = dict(d, n_layers=l1 - l0)
+                tg = {k: (None if v is None else v[l0:l1]) for k, v in wl.tok.items()}
+                hypic.segment_build(dg, tg, wl.seg_off, T[l0:l1], S[l0:l1], wsp, stream=stream)
+                hypic.compose(dg, tg, wl.seg_off, wl.order, T[l0:l1], S[l0:l1], Sf[l0:l1],
+                              o_out=o[l0:l1], stream=stream)
+                done = torch.cuda.Event()
+                done.record(stream)
+                cs_out.wait_event(done)
+                with torch.cuda.stream(cs_out):
+                    h_Sf[l0:l1].copy_(Sf[l0:l1], non_blocking=True)
+                    h_o[l0:l1].copy_(o[l0:l1], non_blocking=True)
+            end_ev = torch.cuda.Event()
+            end_ev.record(cs_out)
+            stream.wait_event(end_ev)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -363,7 +392,9 @@ def run_gpu(args):
         ms_e2e = _reduce_max(e0.elapsed_time(e1), ws) / n_e2e
         e2e = {"value": tokens * L * ws / (ms_e2e * 1e-3) / 1e6, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": n_e2e, "ms_per_step": ms_e2e}
+               "steps": n_e2e, "ms_per_step": ms_e2e,
+               "h2d_gbs": h2d / (ms_e2e * 1e-3) / 1e9,
+               "schedule": "%d layer groups; group g+1's inputs copy while group g computes" % len(groups)}
         del host
 
     cpu = None
@@ -409,6 +440,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=6,
+                    help="layer groups of the end-to-end step (copies overlap compute)")
     ap.add_argument("--layers", type=int, default=None,
                     help="first N layers of the workload only (small cases for profiling; "
                          "not a bench line)")
