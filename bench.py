@@ -146,11 +146,14 @@ def _dist():
 
 
 def _reduce_max(x, ws):
+    """Max of x over the ranks (each rank times its own replica; the job's
+    time is the slowest rank's)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -296,6 +299,19 @@ def run_gpu(args):
     build_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     comp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
+    # compose alone (the scan over the pairs without seams), same pairs
+    d0 = dict(d, seam_w=0, conv_k=0)  # no seams: the conv warm-up has nothing to do
+    for _ in range(2):
+        hypic.compose(d0, wl.tok, wl.seg_off, wl.order, T, S, Sf, stream=stream)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(args.steps):
+        hypic.compose(d0, wl.tok, wl.seg_off, wl.order, T, S, Sf, stream=stream)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    scan_ms = c0.elapsed_time(c1) / args.steps
+
     tokens = wl.n_tokens
     body_tokens = int(sum(max(0, int(x) - min(w, int(x))) for x in wl.lengths))
     ms_step = ms_total / args.steps
@@ -314,11 +330,23 @@ def run_gpu(args):
     achieved = flops / (build_ms * 1e-3) / 1e12
     tf32_peak = peaks["bf16_sustained"] * 1.1 / 2.25
     traffic = _build_traffic(L)
+    # full roofline time of the build: the recurrence's flops at tf32, the
+    # chunk overhead C (2 d_k + d_v) + C^2 / 3 per token-head at bf16, or the
+    # algorithmic bytes at HBM speed, whichever is longer
+    C = 64
+    f_bf16 = body_tokens * L * H * (C * (2.0 * D + D) + C * C / 3.0)
+    b_build = (body_tokens * L * H * (2 * D * 2 * (C + 3) / C + 4) + L * n_seg * H * 2 * D * D * 4)
+    t_roof = max(flops / (tf32_peak * 1e12) + f_bf16 / (peaks["bf16_sustained"] * 1e12),
+                 b_build / (peaks["hbm_gbs"] * 1e9))
     roof = {"kernel": "build_tc_kernel", "bound": "tensor", "achieved": achieved,
             "peak": tf32_peak, "unit": "TFLOP/s", "frac": achieved / tf32_peak, "traffic": traffic,
             "peak_source": "%s sustained bf16 %.1f TFLOP/s x 1.1/2.25 (tf32)"
                            % (peaks["source"], peaks["bf16_sustained"]),
-            "algorithmic": "131072 flop per body token-head x %d token-heads" % (body_tokens * L * H)}
+            "algorithmic": "131072 flop per body token-head x %d token-heads" % (body_tokens * L * H),
+            "t_roof_ms": t_roof * 1e3, "frac_of_t_roof": t_roof * 1e3 / build_ms,
+            "frac_vs_bf16_peak": achieved / peaks["bf16_sustained"],
+            "t_roof_note": "max(tf32 flops / tf32 peak + chunk-overhead flops (26k per token-head) / bf16 "
+                           "peak, algorithmic bytes / HBM)"}
     # compose + seams: HBM-bound; algorithmic bytes = pairs read + seam inputs + outputs
     pair_bytes = L * n_ord * H * (2 * D * D) * 4
     seam_tok = int(sum(min(w, int(wl.lengths[s])) for s in wl.order))
@@ -415,6 +443,10 @@ def run_gpu(args):
                                          if args.layers else {})),
             "components": {
                 "build": {"mtok_s_per_layer": build_mtok, "ms": build_ms, "launches_per_step": 1},
+                "compose_alone": {"segs_s_per_layer": n_ord * L / (scan_ms * 1e-3), "ms": scan_ms,
+                                  "gbs": pair_bytes / (scan_ms * 1e-3) / 1e9,
+                                  "hbm_frac": pair_bytes / (scan_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                  "launches_per_step": 1},
                 "compose_with_seams": {"segs_s_per_layer": comp_segs, "ms": comp_ms,
                                        "gbs": comp_gbs, "hbm_frac": comp_gbs / peaks["hbm_gbs"],
                                        "launches_per_step": 1}},
