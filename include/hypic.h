@@ -12,7 +12,11 @@
  *     A_t = alpha_t (I - beta_t k_t k_t^T),   W_t = beta_t k_t v_t^T,
  * or one of the two named specialisations
  *     scalar decay (RetNet):        A_t = gamma_h I,      W_t = k_t v_t^T,
- *     diagonal gate (Mamba2/GLA):   A_t = diag(alpha_t),  W_t = k_t v_t^T.
+ *     diagonal gate (Mamba2/GLA):   A_t = diag(alpha_t),  W_t = k_t v_t^T,
+ * or the delta rule with a per-channel decay (the pages name the KDA family
+ * without its formula; read here as decay first, then erase and write):
+ *     KDA:   A_t = (I - beta_t k_t k_t^T) diag(alpha_t),  W_t = beta_t k_t v_t^T.
+ * Plain DeltaNet is gated delta with alpha = 1.
  * For a segment C the pair (T_C, S(C|0)) -- the ordered product of the
  * segment's transitions and its final state from zero -- depends only on the
  * segment's own tokens, so it is cached once ("线性层": cache the pair at the
@@ -48,12 +52,12 @@
  * - Layouts are row-major and packed, layer-major, token-major:
  *     q, k, v   [L][N][H][d]   (in_dtype; raw pre-convolution tokens when
  *                               conv_k > 0)
- *     alpha     gated delta [L][N][H]; diagonal gate [L][N][H][d_k];
+ *     alpha     gated delta [L][N][H]; diagonal gate and KDA [L][N][H][d_k];
  *               scalar decay [L][H] (one gamma per head), all in in_dtype
- *     beta      [L][N][H] in in_dtype (gated delta only; NULL otherwise)
+ *     beta      [L][N][H] in in_dtype (gated delta and KDA; NULL otherwise)
  *     conv_w    fp32 [L][3][H][d][conv_k]: channels of q, k, v; tap j
  *               multiplies the token j positions earlier
- *     T         gated delta fp32 [L][n_seg][H][d_k][d_k];
+ *     T         gated delta and KDA fp32 [L][n_seg][H][d_k][d_k];
  *               diagonal gate fp32 [L][n_seg][H][d_k] (the diagonal);
  *               scalar decay fp32 [L][n_seg][H] (the scalar)
  *     S, states fp32 [..][d_k][d_v], row = key channel
@@ -94,7 +98,8 @@ typedef enum hypic_status {
 typedef enum hypic_mode {
     HYPIC_GATED_DELTA = 0,   /* A_t = alpha_t (I - beta_t k k^T), W = beta k v^T */
     HYPIC_SCALAR_DECAY = 1,  /* A_t = gamma_h I,                  W = k v^T      */
-    HYPIC_DIAG_GATE = 2      /* A_t = diag(alpha_t),              W = k v^T      */
+    HYPIC_DIAG_GATE = 2,     /* A_t = diag(alpha_t),              W = k v^T      */
+    HYPIC_KDA = 3            /* A_t = (I - beta_t k k^T) diag(alpha_t), W = beta k v^T */
 } hypic_mode;
 
 typedef enum hypic_dtype {

@@ -30,7 +30,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int check_desc(const hypic_desc *d)
 {
     if (!d) return fail(HYPIC_ERR_INVALID_ARG, "desc is NULL");
-    if (d->mode < HYPIC_GATED_DELTA || d->mode > HYPIC_DIAG_GATE)
+    if (d->mode < HYPIC_GATED_DELTA || d->mode > HYPIC_KDA)
         return fail(HYPIC_ERR_INVALID_ARG, "unknown mode %d", d->mode);
     if (d->in_dtype != HYPIC_F32 && d->in_dtype != HYPIC_BF16)
         return fail(HYPIC_ERR_DTYPE, "unknown in_dtype %d", d->in_dtype);
@@ -61,7 +61,7 @@ int check_tokens(const hypic_desc *d, const hypic_tokens *t, bool need_q)
         {t->k, "k", true},
         {t->v, "v", true},
         {t->alpha, "alpha", true},
-        {t->beta, "beta", d->mode == HYPIC_GATED_DELTA},
+        {t->beta, "beta", d->mode == HYPIC_GATED_DELTA || d->mode == HYPIC_KDA},
         {t->conv_w, "conv_w", d->conv_k > 0},
     };
     for (auto &x : ps) {

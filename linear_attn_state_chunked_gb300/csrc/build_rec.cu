@@ -24,7 +24,7 @@ constexpr int kChunk = 16;
 // Columns of the kept state and threads per CTA (at least one full warp;
 // threads past the last column only help staging).
 template <int D, int MODE> struct RecGeom {
-    static constexpr int NCOL = (MODE == HYPIC_GATED_DELTA ? 2 : 1) * D;
+    static constexpr int NCOL = (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA ? 2 : 1) * D;
     static constexpr int NT = NCOL < 32 ? 32 : NCOL;
 };
 
@@ -34,7 +34,8 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
 {
     constexpr int NT = RecGeom<D, MODE>::NT;
     constexpr int NCOL = RecGeom<D, MODE>::NCOL;
-    constexpr int AW = (MODE == HYPIC_DIAG_GATE) ? D : 1;
+    constexpr int AW = (MODE == HYPIC_DIAG_GATE || MODE == HYPIC_KDA) ? D : 1;
+    constexpr bool DENSE_T = (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA);
     __shared__ __align__(16) float ks[kChunk][D];
     __shared__ __align__(16) float vs[kChunk][D];
     __shared__ float as_[kChunk][AW];
@@ -59,7 +60,7 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
 
     float x[D];
 #pragma unroll
-    for (int r = 0; r < D; ++r) x[r] = (MODE == HYPIC_GATED_DELTA && r == c) ? 1.f : 0.f;
+    for (int r = 0; r < D; ++r) x[r] = (DENSE_T && r == c) ? 1.f : 0.f;
 
     float gamma = 1.f;
     if (MODE == HYPIC_SCALAR_DECAY) gamma = ld_f(ap, (size_t)l * dm.H + h);
@@ -94,12 +95,12 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
                 ks[i][ch] = kv;
                 vs[i][ch] = vv;
             }
-            if (MODE == HYPIC_DIAG_GATE) as_[i][ch] = ld_f(ap, tok_index(dm, N, l, tok, h, ch));
+            if (MODE == HYPIC_DIAG_GATE || MODE == HYPIC_KDA) as_[i][ch] = ld_f(ap, tok_index(dm, N, l, tok, h, ch));
         }
-        if (MODE == HYPIC_GATED_DELTA) {
+        if (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA) {
             for (int i = c; i < nc; i += NT) {
                 const size_t gi = gate_index(dm, N, l, b0 + t0 + i, h);
-                as_[i][0] = ld_f(ap, gi);
+                if (MODE == HYPIC_GATED_DELTA) as_[i][0] = ld_f(ap, gi);
                 bs[i] = ld_f(bp, gi);
             }
         }
@@ -140,6 +141,35 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
                     x[r + 2] = fmaf(k4.z, coef, al * x[r + 2]);
                     x[r + 3] = fmaf(k4.w, coef, al * x[r + 3]);
                 }
+            } else if (MODE == HYPIC_KDA) {
+                // decay the key channels, then erase along k and write:
+                // y = diag(alpha) x,  x = y + k beta (v - k.y)
+                const float be = bs[i];
+                float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+                for (int r = 0; r < D; r += 4) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(&ks[i][r]);
+                    const float4 a4 = *reinterpret_cast<const float4 *>(&as_[i][r]);
+                    x[r + 0] *= a4.x;
+                    x[r + 1] *= a4.y;
+                    x[r + 2] *= a4.z;
+                    x[r + 3] *= a4.w;
+                    u0 = fmaf(k4.x, x[r + 0], u0);
+                    u1 = fmaf(k4.y, x[r + 1], u1);
+                    u2 = fmaf(k4.z, x[r + 2], u2);
+                    u3 = fmaf(k4.w, x[r + 3], u3);
+                }
+                const float u = (u0 + u1) + (u2 + u3);
+                const float vt = (c >= D) ? vs[i][c - D] : 0.f;
+                const float coef = be * (vt - u);
+#pragma unroll
+                for (int r = 0; r < D; r += 4) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(&ks[i][r]);
+                    x[r + 0] = fmaf(k4.x, coef, x[r + 0]);
+                    x[r + 1] = fmaf(k4.y, coef, x[r + 1]);
+                    x[r + 2] = fmaf(k4.z, coef, x[r + 2]);
+                    x[r + 3] = fmaf(k4.w, coef, x[r + 3]);
+                }
             } else {
                 const float vc = vs[i][c];
 #pragma unroll
@@ -164,7 +194,7 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
 
     const size_t pair = ((size_t)l * tab.n_seg + s) * dm.H + h;
     if (c >= NCOL) return;
-    if (MODE == HYPIC_GATED_DELTA) {
+    if (DENSE_T) {
         float *dst = (c < D) ? a.T_out + pair * D * D + c : a.S_out + pair * D * D + (c - D);
 #pragma unroll
         for (int r = 0; r < D; ++r) dst[(size_t)r * D] = x[r];
@@ -218,6 +248,9 @@ cudaError_t launch_build_rec(const BuildArgs &a, const SegTable &tab, cudaStream
     case HYPIC_SCALAR_DECAY:
         return bf ? launch_m<HYPIC_SCALAR_DECAY, __nv_bfloat16>(a, tab, n_items, st)
                   : launch_m<HYPIC_SCALAR_DECAY, float>(a, tab, n_items, st);
+    case HYPIC_KDA:
+        return bf ? launch_m<HYPIC_KDA, __nv_bfloat16>(a, tab, n_items, st)
+                  : launch_m<HYPIC_KDA, float>(a, tab, n_items, st);
     default:
         return bf ? launch_m<HYPIC_DIAG_GATE, __nv_bfloat16>(a, tab, n_items, st)
                   : launch_m<HYPIC_DIAG_GATE, float>(a, tab, n_items, st);

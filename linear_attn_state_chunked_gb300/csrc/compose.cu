@@ -75,12 +75,12 @@ __device__ __forceinline__ void stage_token(const Dims &dm, const TokPtrs &tk, c
             st.k[ch] = kv;
             st.v[ch] = vv;
         }
-        if (MODE == HYPIC_DIAG_GATE) st.a[ch] = ld_f(ap, tok_index(dm, N, l, tok, h, ch));
+        if (MODE == HYPIC_DIAG_GATE || MODE == HYPIC_KDA) st.a[ch] = ld_f(ap, tok_index(dm, N, l, tok, h, ch));
     }
     if (tid == 0) {
-        if (MODE == HYPIC_GATED_DELTA) {
+        if (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA) {
             const size_t gi = gate_index(dm, N, l, tok, h);
-            st.a[0] = ld_f(ap, gi);
+            if (MODE == HYPIC_GATED_DELTA) st.a[0] = ld_f(ap, gi);
             st.beta = ld_f(static_cast<const Tin *>(tk.beta), gi);
         } else if (MODE == HYPIC_SCALAR_DECAY) {
             st.a[0] = ld_f(ap, (size_t)l * dm.H + h);
@@ -147,6 +147,20 @@ __device__ void run_seam(float (&xs)[CompGeom<D>::RPS], const Dims &dm, const To
                 const float coef = be * (vc - al * u);
 #pragma unroll
                 for (int i = 0; i < G::RPS; ++i) xs[i] = fmaf(st.k[part + G::TPC * i], coef, al * xs[i]);
+            } else if (MODE == HYPIC_KDA) {
+                // decay the key channels, then erase along k and write
+                const float be = st.beta;
+                float u = 0.f;
+#pragma unroll
+                for (int i = 0; i < G::RPS; ++i) {
+                    const int r = part + G::TPC * i;
+                    xs[i] *= st.a[r];
+                    u = fmaf(st.k[r], xs[i], u);
+                }
+                u = group_sum<G::TPC>(u);
+                const float coef = be * (vc - u);
+#pragma unroll
+                for (int i = 0; i < G::RPS; ++i) xs[i] = fmaf(st.k[part + G::TPC * i], coef, xs[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < G::RPS; ++i) {
@@ -168,7 +182,7 @@ template <int D, int MODE>
 constexpr size_t compose_smem_bytes()
 {
     using G = CompGeom<D>;
-    return sizeof(float) * ((size_t)D * G::CB + (MODE == HYPIC_GATED_DELTA ? (size_t)D * (D + 1) : 0)) +
+    return sizeof(float) * ((size_t)D * G::CB + (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA ? (size_t)D * (D + 1) : 0)) +
            sizeof(TokStage<D>);
 }
 
@@ -179,9 +193,9 @@ compose_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__ Se
     using G = CompGeom<D>;
     extern __shared__ __align__(16) float smem[];
     float *Sb = smem;                    // [D][CB] running-state block
-    float *Ts = Sb + D * G::CB;          // [D][D+1] T_C (gated delta)
+    float *Ts = Sb + D * G::CB;          // [D][D+1] T_C (gated delta, KDA)
     TokStage<D> &st = *reinterpret_cast<TokStage<D> *>(
-        Ts + (MODE == HYPIC_GATED_DELTA ? D * (D + 1) : 0));
+        Ts + (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA ? D * (D + 1) : 0));
 
     const Dims dm = a.dm;
     const int tid = threadIdx.x;
@@ -218,7 +232,7 @@ compose_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__ Se
         }
         const size_t pair = ((size_t)l * tab.n_seg + s) * dm.H + h;
         const float *Sc = a.S + pair * D * D + c0;
-        if (MODE == HYPIC_GATED_DELTA) {
+        if (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA) {
             const float *Tg = a.T + pair * D * D;
             for (int e = tid; e < D * D; e += G::NT) Ts[(e / D) * (D + 1) + e % D] = Tg[e];
             __syncthreads();
@@ -343,6 +357,7 @@ static cudaError_t launch_seam_t(const SeamArgs &a, const SegTable &tab, cudaStr
         switch (a.dm.mode) {                                                                  \
         case HYPIC_GATED_DELTA: return FN##_d<HYPIC_GATED_DELTA, Tin>(a, tab, st);             \
         case HYPIC_SCALAR_DECAY: return FN##_d<HYPIC_SCALAR_DECAY, Tin>(a, tab, st);           \
+        case HYPIC_KDA: return FN##_d<HYPIC_KDA, Tin>(a, tab, st);                             \
         default: return FN##_d<HYPIC_DIAG_GATE, Tin>(a, tab, st);                              \
         }                                                                                     \
     }

@@ -13,7 +13,7 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libhypic.so")
 
-GATED_DELTA, SCALAR_DECAY, DIAG_GATE = 0, 1, 2
+GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA = 0, 1, 2, 3
 F32, BF16 = 0, 1
 MAX_SEGMENTS = 2048
 
@@ -144,7 +144,7 @@ def workspace_status(workspace, stream=None):
 def pair_shapes(desc, n_seg):
     """Shapes of the T and S cache tensors for n_seg segments."""
     L, H, D = desc["n_layers"], desc["n_heads"], desc["d_k"]
-    if desc["mode"] == GATED_DELTA:
+    if desc["mode"] in (GATED_DELTA, KDA):
         tshape = (L, n_seg, H, D, D)
     elif desc["mode"] == DIAG_GATE:
         tshape = (L, n_seg, H, D)

@@ -12,9 +12,11 @@ input dtype; bf16 rounding happens here, so both sides see the same values):
   convolves and normalises them);
 * v ~ N(0, 1);
 * gated delta: alpha = exp(-softplus(z)), beta = sigmoid(z'), z, z' ~ N(0, 1);
-  the slow-gate stress variant uses alpha = exp(-softplus(z) / 64);
+  the slow-gate stress variant uses alpha = exp(-softplus(z) / 64), plain
+  DeltaNet alpha = 1;
 * scalar decay (RetNet): gamma_h = 1 - 2^(-5-h);
 * diagonal gate: alpha_t[c] = exp(-softplus(z)) per channel;
+* KDA: alpha_t[c] = exp(-softplus(z) / 16) per channel, beta = sigmoid(z');
 * conv weights ~ N(0, 1) / 2.
 
 Segment lengths, orders and seeds:
@@ -35,13 +37,18 @@ Segment lengths, orders and seeds:
                 request order = segment order (a cold prompt)
 * stress_tiny / stress_gdn  the tiny_gdn / gdn_bf16 shapes with the slow gate
                 (seeds 5 and 6), so that T_C stays far from zero.
+* deltanet      plain DeltaNet (gated delta with alpha = 1): 1 layer, 2 heads,
+                d=32, fp32, 6 x 50 tokens, seed 9, w=8
+* kda_tiny      KDA, 1 layer, 2 heads, d=16, fp32, 4 x 64 tokens, seed 7, w=0
+* kda_bf16      KDA, 1 layer, 4 heads, d=64, bf16, 12 segments with lengths
+                uniform on [40, 300], conv taps 4, seed 8, w=8
 """
 from dataclasses import dataclass, field
 
 import numpy as np
 import torch
 
-GATED_DELTA, SCALAR_DECAY, DIAG_GATE = 0, 1, 2
+GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA = 0, 1, 2, 3
 F32, BF16 = 0, 1
 
 _TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
@@ -89,6 +96,12 @@ def segment_lengths(name):
     if name == "warm_30l":
         raw = np.random.default_rng(3).integers(512, 1051, size=128)
         return _rescale(raw, 100_000, 512, 1050)
+    if name == "deltanet":
+        return np.full(6, 50, np.int64)
+    if name == "kda_tiny":
+        return np.full(4, 64, np.int64)
+    if name == "kda_bf16":
+        return np.random.default_rng(8).integers(40, 301, size=12).astype(np.int64)
     if name == "cold_30l":
         raw = np.random.default_rng(4).lognormal(np.log(512.0), 0.8, size=200)
         raw = np.clip(np.rint(raw), 64, 4096)
@@ -97,22 +110,25 @@ def segment_lengths(name):
 
 
 _SPECS = {
-    #  name            mode          L   H   d   dtype  seed w  conv slow
-    "tiny_gdn":     (GATED_DELTA,  1,  1, 16, F32,  0,   0, 0, False),
-    "decay_retnet": (SCALAR_DECAY, 1,  8, 64, F32,  1,   0, 0, False),
-    "decay_diag":   (DIAG_GATE,    1,  8, 64, F32,  1,   0, 0, False),
-    "gdn_bf16":     (GATED_DELTA,  1, 32, 128, BF16, 2,  8, 0, False),
-    "warm_30l":     (GATED_DELTA, 30, 32, 128, BF16, 3,  8, 0, False),
-    "cold_30l":     (GATED_DELTA, 30, 32, 128, BF16, 4,  8, 4, False),
-    "stress_tiny":  (GATED_DELTA,  1,  1, 16, F32,  5,   0, 0, True),
-    "stress_gdn":   (GATED_DELTA,  1, 32, 128, BF16, 6,  8, 0, True),
+    #  name            mode          L   H   d   dtype  seed w  conv gate divisor (0: alpha = 1)
+    "tiny_gdn":     (GATED_DELTA,  1,  1, 16, F32,  0,   0, 0, 1.0),
+    "decay_retnet": (SCALAR_DECAY, 1,  8, 64, F32,  1,   0, 0, 1.0),
+    "decay_diag":   (DIAG_GATE,    1,  8, 64, F32,  1,   0, 0, 1.0),
+    "gdn_bf16":     (GATED_DELTA,  1, 32, 128, BF16, 2,  8, 0, 1.0),
+    "warm_30l":     (GATED_DELTA, 30, 32, 128, BF16, 3,  8, 0, 1.0),
+    "cold_30l":     (GATED_DELTA, 30, 32, 128, BF16, 4,  8, 4, 1.0),
+    "stress_tiny":  (GATED_DELTA,  1,  1, 16, F32,  5,   0, 0, 64.0),
+    "stress_gdn":   (GATED_DELTA,  1, 32, 128, BF16, 6,  8, 0, 64.0),
+    "deltanet":     (GATED_DELTA,  1,  2, 32, F32,  9,   8, 0, 0.0),
+    "kda_tiny":     (KDA,          1,  2, 16, F32,  7,   0, 0, 16.0),
+    "kda_bf16":     (KDA,          1,  4, 64, BF16, 8,   8, 4, 16.0),
 }
 
 NAMES = tuple(_SPECS)
 
 
 def describe(name, **over):
-    mode, L, H, d, dt, seed, w, ck, slow = _SPECS[name]
+    mode, L, H, d, dt, seed, w, ck, gdiv = _SPECS[name]
     desc = dict(n_layers=L, n_heads=H, d_k=d, d_v=d, seam_w=w, conv_k=ck,
                 mode=mode, in_dtype=dt)
     desc.update(over)
@@ -141,7 +157,7 @@ def make(name, device="cpu", layers=None, lengths=None, order=None,
     lengths / order: override the segment lengths / request order (edge-case
     tests); desc_over overrides descriptor fields (e.g. n_heads).
     """
-    mode, L, H, d, dt, seed, w, ck, slow = _SPECS[name]
+    mode, L, H, d, dt, seed, w, ck, gdiv = _SPECS[name]
     L_spec = L
     desc = describe(name, **desc_over)
     if layers is not None:
@@ -164,6 +180,9 @@ def make(name, device="cpu", layers=None, lengths=None, order=None,
     elif mode == DIAG_GATE:
         alpha = torch.empty((L, N, H, d), dtype=tdt, device=dev)
         beta = None
+    elif mode == KDA:
+        alpha = torch.empty((L, N, H, d), dtype=tdt, device=dev)
+        beta = torch.empty((L, N, H), dtype=tdt, device=dev)
     else:
         alpha = torch.empty((L, H), dtype=tdt, device=dev)
         beta = None
@@ -180,7 +199,12 @@ def make(name, device="cpu", layers=None, lengths=None, order=None,
         if mode == GATED_DELTA:
             z = torch.randn((N, H), generator=g, device=dev, dtype=torch.float32)
             sp = torch.nn.functional.softplus(z)
-            alpha[l].copy_(torch.exp(-sp / 64.0) if slow else torch.exp(-sp))
+            alpha[l].copy_(torch.exp(-sp / gdiv) if gdiv > 0 else torch.ones_like(sp))
+            z = torch.randn((N, H), generator=g, device=dev, dtype=torch.float32)
+            beta[l].copy_(torch.sigmoid(z))
+        elif mode == KDA:
+            z = torch.randn((N, H, d), generator=g, device=dev, dtype=torch.float32)
+            alpha[l].copy_(torch.exp(-torch.nn.functional.softplus(z) / gdiv))
             z = torch.randn((N, H), generator=g, device=dev, dtype=torch.float32)
             beta[l].copy_(torch.sigmoid(z))
         elif mode == DIAG_GATE:

@@ -30,7 +30,7 @@ import numpy as np
 
 from . import build as _build
 
-GATED_DELTA, SCALAR_DECAY, DIAG_GATE = 0, 1, 2
+GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA = 0, 1, 2, 3
 L2_EPS = 1e-6
 
 _lib = None
@@ -72,13 +72,13 @@ def _check_shapes(mode, k, v, a, b):
     C, n, dk = k.shape
     if v.shape[:2] != (C, n):
         raise ValueError("v must be [n_chain, n, dv]")
-    if mode == DIAG_GATE:
+    if mode in (DIAG_GATE, KDA):
         if a.shape != (C, n, dk):
-            raise ValueError("diagonal gate alpha must be [n_chain, n, dk]")
+            raise ValueError("per-channel alpha must be [n_chain, n, dk]")
     elif a.shape != (C, n):
         raise ValueError("alpha must be [n_chain, n]")
-    if mode == GATED_DELTA and (b is None or b.shape != (C, n)):
-        raise ValueError("gated delta needs beta [n_chain, n]")
+    if mode in (GATED_DELTA, KDA) and (b is None or b.shape != (C, n)):
+        raise ValueError("the delta modes need beta [n_chain, n]")
     return C, n, dk, v.shape[2]
 
 
@@ -86,8 +86,8 @@ def recurrence(mode, q, k, v, a, b=None, S0=None, record_at=(), want_o=True):
     """Sequential fp64 recurrence over n tokens for each of C chains.
 
     q, k: [C, n, dk]; v: [C, n, dv]; a: [C, n] (gated delta: alpha, scalar
-    decay: gamma per token) or [C, n, dk] (diagonal gate); b: [C, n] (gated
-    delta only); S0: [C, dk, dv] or None for zero.
+    decay: gamma per token) or [C, n, dk] (diagonal gate, KDA); b: [C, n]
+    (gated delta and KDA); S0: [C, dk, dv] or None for zero.
     Returns (S_final [C, dk, dv], o [C, n, dv] or None, S_rec [C, R, dk, dv])
     where S_rec[:, r] is the state just before token record_at[r].
     """

@@ -21,7 +21,11 @@
  *        A_t = alpha_t (I - beta_t k_t k_t^T),   W_t = beta_t k_t v_t^T,
  *    with the two named specialisations
  *        scalar decay (RetNet):    A_t = gamma I,          W_t = k_t v_t^T
- *        diagonal gate (Mamba2/GLA): A_t = diag(alpha_t),  W_t = k_t v_t^T.
+ *        diagonal gate (Mamba2/GLA): A_t = diag(alpha_t),  W_t = k_t v_t^T,
+ *    and the delta rule with a per-channel decay (the KDA family, named by
+ *    the first article's "线性层" section without a formula; read as decay
+ *    first, then erase and write):
+ *        KDA:  A_t = (I - beta_t k_t k_t^T) diag(alpha_t),  W_t = beta_t k_t v_t^T.
  *  - The cached pair of a segment C (same sections): T_C is the ordered
  *    product A_L ... A_1 of the segment's transitions, applied one token at a
  *    time to T = I; S(C|0) is the recurrence's final state from S = 0.
@@ -31,8 +35,8 @@
  * Layouts (all row-major, contiguous, one "chain" = one independent
  * (layer, head) problem, chains stacked on the outermost axis):
  *    q, k : [n_chain][n][dk]      v : [n_chain][n][dv]
- *    a    : mode 0/1: [n_chain][n]   mode 2: [n_chain][n][dk]
- *    b    : [n_chain][n]  (mode 0 only; may be NULL otherwise)
+ *    a    : mode 0/1: [n_chain][n]   mode 2/3: [n_chain][n][dk]
+ *    b    : [n_chain][n]  (modes 0 and 3; may be NULL otherwise)
  *    S    : [n_chain][dk][dv]      T : [n_chain][dk][dk]
  * Independent chains run in parallel under OpenMP; each chain is a plain
  * sequential loop.
@@ -42,7 +46,7 @@
 #include <string.h>
 #include <math.h>
 
-enum { ORC_GATED_DELTA = 0, ORC_SCALAR_DECAY = 1, ORC_DIAG_GATE = 2 };
+enum { ORC_GATED_DELTA = 0, ORC_SCALAR_DECAY = 1, ORC_DIAG_GATE = 2, ORC_KDA = 3 };
 
 /* S <- A_t S + W_t for one token.  X is [dk][ncol]; v may be NULL (then the
  * write term is absent, which is how T is propagated).  u is scratch [ncol]. */
@@ -72,6 +76,19 @@ static void apply_token(int mode, int dk, int ncol, double *X,
                 if (v) x += k[i] * v[j];
                 X[(size_t)i * ncol + j] = x;
             }
+    } else if (mode == ORC_KDA) {
+        /* X = diag(alpha) X, then X = X - b k (X^T k)^T + b k v^T */
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < ncol; ++j) X[(size_t)i * ncol + j] *= a[i];
+        for (int j = 0; j < ncol; ++j) u[j] = 0.0;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < ncol; ++j) u[j] += k[i] * X[(size_t)i * ncol + j];
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < ncol; ++j) {
+                double x = X[(size_t)i * ncol + j] - b * k[i] * u[j];
+                if (v) x += b * k[i] * v[j];
+                X[(size_t)i * ncol + j] = x;
+            }
     } else { /* ORC_DIAG_GATE */
         for (int i = 0; i < dk; ++i)
             for (int j = 0; j < ncol; ++j) {
@@ -85,7 +102,7 @@ static void apply_token(int mode, int dk, int ncol, double *X,
 static const double *alpha_at(int mode, int dk, int64_t n, const double *a,
                               int c, int64_t t)
 {
-    if (mode == ORC_DIAG_GATE) return a + ((size_t)c * n + t) * dk;
+    if (mode == ORC_DIAG_GATE || mode == ORC_KDA) return a + ((size_t)c * n + t) * dk;
     return a + (size_t)c * n + t;
 }
 
@@ -117,7 +134,7 @@ int orc_recurrence(int mode, int dk, int dv, int64_t n, int n_chain,
             if (t == n) break;
             const double *kt = k + ((size_t)c * n + t) * dk;
             const double *vt = v + ((size_t)c * n + t) * dv;
-            double bt = (mode == ORC_GATED_DELTA) ? b[(size_t)c * n + t] : 0.0;
+            double bt = (mode == ORC_GATED_DELTA || mode == ORC_KDA) ? b[(size_t)c * n + t] : 0.0;
             apply_token(mode, dk, dv, X, kt, vt, alpha_at(mode, dk, n, a, c, t), bt, u);
             if (o) {
                 const double *qt = q + ((size_t)c * n + t) * dk;
@@ -158,7 +175,7 @@ int orc_pair(int mode, int dk, int dv, int64_t n, int n_chain,
             const double *kt = k + ((size_t)c * n + t) * dk;
             const double *vt = v + ((size_t)c * n + t) * dv;
             const double *at = alpha_at(mode, dk, n, a, c, t);
-            double bt = (mode == ORC_GATED_DELTA) ? b[(size_t)c * n + t] : 0.0;
+            double bt = (mode == ORC_GATED_DELTA || mode == ORC_KDA) ? b[(size_t)c * n + t] : 0.0;
             apply_token(mode, dk, dk, Tc, kt, NULL, at, bt, u);
             apply_token(mode, dk, dv, Sc, kt, vt, at, bt, u);
         }

@@ -21,7 +21,7 @@ full prefix, advancing the running state and emitting per-token outputs.
 """
 import numpy as np
 
-from . import (GATED_DELTA, SCALAR_DECAY, DIAG_GATE, recurrence, pair,
+from . import (GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA, recurrence, pair,
                causal_conv, l2_normalize)
 
 
@@ -51,7 +51,7 @@ def chain_stream(tok, mode, l, h, idx, conv_k=0):
         a = np.full(len(idx), float(_np(tok["alpha"][l, h])))
     else:
         a = _np(tok["alpha"][l, idx, h])
-    b = _np(tok["beta"][l, idx, h]) if mode == GATED_DELTA else None
+    b = _np(tok["beta"][l, idx, h]) if mode in (GATED_DELTA, KDA) else None
     return q, k, v, a, b
 
 
@@ -101,7 +101,7 @@ def request_reference(desc, tok, seg_off, order, chains, S_init=None, want_naive
         return {key: np.zeros(0) for key in out}
     streams = [chain_stream(tok, mode, l, h, idx, ck) for (l, h) in chains]
     q, k, v, a = (np.stack([st[i] for st in streams]) for i in range(4))
-    b = None if mode != GATED_DELTA else np.stack([st[4] for st in streams])
+    b = None if mode not in (GATED_DELTA, KDA) else np.stack([st[4] for st in streams])
     dk, dv = k.shape[2], v.shape[2]
     S0 = None if S_init is None else np.stack([_np(x) for x in S_init])
     # all chains in one call: independent chains run in parallel

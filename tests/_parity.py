@@ -49,7 +49,7 @@ def dense_T(desc, T):
     """GPU T block (dense / diagonal / scalar) as a dense numpy matrix."""
     T = np.asarray(T, dtype=np.float64)
     D = desc["d_k"]
-    if desc["mode"] == hypic.GATED_DELTA:
+    if desc["mode"] in (hypic.GATED_DELTA, hypic.KDA):
         return T
     if desc["mode"] == hypic.DIAG_GATE:
         return np.diag(T)

@@ -86,7 +86,7 @@ def _seam(desc, order=(0, 1), seg_off=(0, 10, 20), tok=None, S_in=FAKE, o=FAKE, 
 
 
 BAD_BUILD = [
-    ("mode", dict(desc=_desc(mode=3)), 1),
+    ("mode", dict(desc=_desc(mode=4)), 1),
     ("dtype", dict(desc=_desc(in_dtype=7)), 3),
     ("d_k != d_v", dict(desc=_desc(d_v=32)), 4),
     ("d unsupported", dict(desc=_desc(d_k=48, d_v=48)), 4),

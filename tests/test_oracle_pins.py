@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import GATED_DELTA, SCALAR_DECAY, DIAG_GATE
+from oracle import GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 TIGHT = 1e-12
@@ -26,11 +26,11 @@ def _rand_tokens(rng, n, dk, dv, mode, slow=False, unit_k=True):
         q /= np.linalg.norm(q, axis=1, keepdims=True)
         k /= np.linalg.norm(k, axis=1, keepdims=True)
     v = rng.standard_normal((n, dv))
-    sp = np.log1p(np.exp(rng.standard_normal(n if mode != DIAG_GATE else (n, dk))))
+    sp = np.log1p(np.exp(rng.standard_normal(n if mode not in (DIAG_GATE, KDA) else (n, dk))))
     a = np.exp(-sp / (64.0 if slow else 1.0))
     if mode == SCALAR_DECAY:
         a = np.full(n, 1.0 - 2.0 ** -6)
-    b = 1.0 / (1.0 + np.exp(-rng.standard_normal(n))) if mode == GATED_DELTA else None
+    b = 1.0 / (1.0 + np.exp(-rng.standard_normal(n))) if mode in (GATED_DELTA, KDA) else None
     return q, k, v, a, b
 
 
@@ -40,18 +40,20 @@ def _dense_A(mode, k, a, b):
         return a * (np.eye(dk) - b * np.outer(k, k))
     if mode == SCALAR_DECAY:
         return a * np.eye(dk)
+    if mode == KDA:
+        return (np.eye(dk) - b * np.outer(k, k)) @ np.diag(a)
     return np.diag(a)
 
 
 def _dense_W(mode, k, v, b):
-    return (b if mode == GATED_DELTA else 1.0) * np.outer(k, v)
+    return (b if mode in (GATED_DELTA, KDA) else 1.0) * np.outer(k, v)
 
 
 def _bf(x):
     return None if x is None else x[None]
 
 
-@pytest.mark.parametrize("mode", [GATED_DELTA, SCALAR_DECAY, DIAG_GATE])
+@pytest.mark.parametrize("mode", [GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA])
 @pytest.mark.parametrize("n", [1, 3, 8])
 def test_brute_force_dense_products(mode, n):
     """Tiny d: T is the ordered product of dense A_t, S and o follow from
@@ -326,3 +328,33 @@ def test_l2_normalize():
     np.testing.assert_allclose(np.linalg.norm(y, axis=1), nx / np.sqrt(nx ** 2 + oracle.L2_EPS), rtol=1e-12)
     np.testing.assert_allclose(oracle.l2_normalize(3.0 * x, eps=0.0), oracle.l2_normalize(x, eps=0.0), rtol=1e-12)
     assert np.all(oracle.l2_normalize(np.zeros((1, 4))) == 0)
+
+
+def test_kda_reduces_to_gated_delta_and_diagonal_gate():
+    """KDA with the same decay on every channel is gated delta (diag(alpha)
+    commutes with the projector); KDA with beta = 0 is the diagonal gate
+    without a write, so T = diag(prod alpha) and S(C|0) = 0."""
+    rng = np.random.default_rng(77)
+    n, dk, dv = 37, 6, 5
+    q, k, v, a, b = _rand_tokens(rng, n, dk, dv, KDA, slow=True)
+    a_uni = np.repeat(a[:, :1], dk, axis=1)
+    T1, S1 = oracle.pair(KDA, k[None], v[None], a_uni[None], b[None])
+    T2, S2 = oracle.pair(GATED_DELTA, k[None], v[None], a_uni[None, :, 0], b[None])
+    np.testing.assert_allclose(T1, T2, rtol=0, atol=TIGHT)
+    np.testing.assert_allclose(S1, S2, rtol=0, atol=TIGHT)
+    T0, S0 = oracle.pair(KDA, k[None], v[None], a[None], np.zeros((1, n)))
+    np.testing.assert_allclose(T0[0], np.diag(np.prod(a, axis=0)), rtol=1e-13, atol=0)
+    assert np.abs(S0).max() == 0.0
+
+
+def test_kda_composition_law():
+    """S(C1 C2) = T(C2) S(C1) + S(C2) for KDA pairs, against the recurrence
+    over the concatenated stream."""
+    rng = np.random.default_rng(78)
+    n1, n2, dk, dv = 23, 31, 8, 8
+    q, k, v, a, b = _rand_tokens(rng, n1 + n2, dk, dv, KDA, slow=True)
+    T1, S1 = oracle.pair(KDA, k[None, :n1], v[None, :n1], a[None, :n1], b[None, :n1])
+    T2, S2 = oracle.pair(KDA, k[None, n1:], v[None, n1:], a[None, n1:], b[None, n1:])
+    Sf, _, _ = oracle.recurrence(KDA, None, k[None], v[None], a[None], b[None], want_o=False)
+    np.testing.assert_allclose(T2[0] @ S1[0] + S2[0], Sf[0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oracle.compose(T2, S2, S1)[0], Sf[0], rtol=0, atol=1e-12)

@@ -23,11 +23,14 @@ def _all_chains(wl):
     return [(l, h) for l in range(d["n_layers"]) for h in range(d["n_heads"])]
 
 
-@pytest.mark.parametrize("name", ["tiny_gdn", "stress_tiny", "decay_retnet", "decay_diag"])
+@pytest.mark.parametrize("name", ["tiny_gdn", "stress_tiny", "decay_retnet", "decay_diag", "deltanet",
+                                  "kda_tiny", "kda_bf16"])
 def test_small_workloads(name):
     """tiny_gdn: build per segment, compose in order, against the sequential
     recurrence over all 256 tokens; decay_*: scalar-decay and diagonal-gate
-    specialisations; stress_tiny: slow gate so that T_C matters."""
+    specialisations; stress_tiny: slow gate so that T_C matters; deltanet:
+    plain DeltaNet (alpha = 1); kda_*: the delta rule with a per-channel
+    decay (fp32, and bf16 with conv warm-up and seams)."""
     wl = W.make(name, device="cuda")
     out = run_pipeline(wl)
     tol = tol_of(wl.desc)
@@ -41,7 +44,7 @@ def test_small_workloads(name):
         assert np.abs(T).max() > 1e-3
 
 
-@pytest.mark.parametrize("name", ["decay_retnet", "decay_diag", "stress_tiny"])
+@pytest.mark.parametrize("name", ["decay_retnet", "decay_diag", "stress_tiny", "kda_tiny"])
 def test_naive_addition_is_wrong(name):
     """Negative control: summing the GPU's zero-initial states (dropping T)
     misses the recurrence by far more than the tolerance."""
@@ -63,12 +66,12 @@ EDGE_ORDER = [5, 0, 9, 2, 2, 7, 1, 6, 3, 4, 8, 5]
 
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("dtype", [hypic.F32, hypic.BF16])
-@pytest.mark.parametrize("mode", [hypic.GATED_DELTA, hypic.SCALAR_DECAY, hypic.DIAG_GATE])
+@pytest.mark.parametrize("mode", [hypic.GATED_DELTA, hypic.SCALAR_DECAY, hypic.DIAG_GATE, hypic.KDA])
 def test_edge_cases_ragged_seams_order(d, dtype, mode):
     """Empty, one-token, shorter-than-seam and ragged segments, a shuffled
     request order with a repeated segment, seams of w = 8, two layers."""
     name = {hypic.GATED_DELTA: "stress_tiny", hypic.SCALAR_DECAY: "decay_retnet",
-            hypic.DIAG_GATE: "decay_diag"}[mode]
+            hypic.DIAG_GATE: "decay_diag", hypic.KDA: "kda_tiny"}[mode]
     wl = W.make(name, device="cuda", layers=2, lengths=EDGE_LENGTHS, order=EDGE_ORDER,
                 n_heads=2, d_k=d, d_v=d, seam_w=8, in_dtype=dtype)
     out = run_pipeline(wl)
@@ -113,11 +116,14 @@ def test_nonzero_initial_state_and_empty_request():
     assert torch.count_nonzero(Z).item() == 0
 
 
-@pytest.mark.parametrize("conv", [False, True])
+@pytest.mark.parametrize("conv", [False, True, "kda"])
 def test_seam_advance_matches_compose(conv):
     """All seams in parallel from the prefix states equal the fused pass and
     the oracle; S_out may alias S_in."""
-    if conv:
+    if conv == "kda":
+        wl = W.make("kda_bf16", device="cuda", layers=2, lengths=[9, 40, 3, 1, 25, 12, 17],
+                    order=[4, 2, 3, 0, 5, 1, 6], n_heads=2, d_k=32, d_v=32)
+    elif conv:
         wl = W.make("cold_30l", device="cuda", layers=2, lengths=[9, 40, 3, 1, 25, 12, 17],
                     order=[4, 2, 3, 0, 5, 1, 6], n_heads=2, d_k=32, d_v=32)
     else:
