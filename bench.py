@@ -312,6 +312,22 @@ def run_gpu(args):
     torch.cuda.synchronize()
     scan_ms = c0.elapsed_time(c1) / args.steps
 
+    # seam advance alone (all seams of the request in parallel from given
+    # prefix states): prefix states from one compose, then timed
+    Sp = torch.empty((L, n_ord, H, D, D), device=dev)
+    hypic.compose(d, wl.tok, wl.seg_off, wl.order, T, S, Sf, o_out=o, S_prefix_out=Sp, stream=stream)
+    for _ in range(2):
+        hypic.seam_advance(d, wl.tok, wl.seg_off, wl.order, Sp, o, stream=stream)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        hypic.seam_advance(d, wl.tok, wl.seg_off, wl.order, Sp, o, stream=stream)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    seam_ms = a0.elapsed_time(a1) / args.steps
+    del Sp
+
     tokens = wl.n_tokens
     body_tokens = int(sum(max(0, int(x) - min(w, int(x))) for x in wl.lengths))
     ms_step = ms_total / args.steps
@@ -447,6 +463,12 @@ def run_gpu(args):
                                   "gbs": pair_bytes / (scan_ms * 1e-3) / 1e9,
                                   "hbm_frac": pair_bytes / (scan_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                   "launches_per_step": 1},
+                "seam_advance": {"seams_s_per_layer": n_ord * L / (seam_ms * 1e-3), "ms": seam_ms,
+                                 "gbs": (L * n_ord * H * D * D * 4 + seam_bytes) / (seam_ms * 1e-3) / 1e9,
+                                 "hbm_frac": (L * n_ord * H * D * D * 4 + seam_bytes) / (seam_ms * 1e-3) / 1e9
+                                             / peaks["hbm_gbs"],
+                                 "launches_per_step": 1,
+                                 "note": "prefix states in, seam outputs out; state not written back"},
                 "compose_with_seams": {"segs_s_per_layer": comp_segs, "ms": comp_ms,
                                        "gbs": comp_gbs, "hbm_frac": comp_gbs / peaks["hbm_gbs"],
                                        "launches_per_step": 1}},

@@ -239,6 +239,12 @@ int hypic_compose(const hypic_desc *desc, const hypic_tokens *tok,
  * token's output.)  Same conv history rule as hypic_compose.
  * S_in: fp32 [L][n_order][H][d_k][d_v]; o_out: fp32 [L][n_order][w][H][d_v];
  * S_out: same layout as S_in or NULL; S_out may alias S_in.
+ * Gated delta seams (alpha = 1: DeltaNet) are computed in closed form, all
+ * tokens of a seam in one pass over S in fp32 (equal to the token-by-token
+ * recurrence up to rounding); the other modes step token by token.  At
+ * d = 128 with seam_w <= 8 the kernel is persistent and pipelined; its
+ * device-side waits are bounded, and if one gives up the outputs are left
+ * incomplete instead of the kernel hanging.
  */
 int hypic_seam_advance(const hypic_desc *desc, const hypic_tokens *tok,
                        const int64_t *seg_off, int32_t n_seg,

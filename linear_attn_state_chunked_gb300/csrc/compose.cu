@@ -378,6 +378,9 @@ cudaError_t launch_compose(const ComposeArgs &a, const SegTable &tab, cudaStream
 
 cudaError_t launch_seam(const SeamArgs &a, const SegTable &tab, cudaStream_t st)
 {
+    // Gated delta seams (DeltaNet included) run all their tokens in one pass
+    // over the prefix state; the other modes re-run them token by token.
+    if (a.dm.mode == HYPIC_GATED_DELTA) return launch_seam_chunk(a, tab, st);
     return a.dm.dtype == HYPIC_BF16 ? launch_seam_m<__nv_bfloat16>(a, tab, st)
                                     : launch_seam_m<float>(a, tab, st);
 }

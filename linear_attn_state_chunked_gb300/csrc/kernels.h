@@ -41,5 +41,6 @@ cudaError_t launch_compose(const ComposeArgs &a, const SegTable &tab, cudaStream
 bool compose_tc_supported(const Dims &dm);
 cudaError_t launch_compose_tc(const ComposeArgs &a, const SegTable &tab, cudaStream_t st);
 cudaError_t launch_seam(const SeamArgs &a, const SegTable &tab, cudaStream_t st);
+cudaError_t launch_seam_chunk(const SeamArgs &a, const SegTable &tab, cudaStream_t st);
 
 }  // namespace hypic

@@ -237,6 +237,22 @@ __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int c0, int c1
                  :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1) : "memory");
 }
 
+// Untiled bulk copy global -> shared, completing on an mbarrier.  Both
+// addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar) : "memory");
+}
+
+// Bulk prefetch of global memory into L2 (16-byte aligned, `bytes` a
+// multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 :: "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
+
 // Named barrier over `count` threads that also returns whether every
 // participating thread passed a true predicate.
 __device__ __forceinline__ bool bar_and(int id, int count, bool pred)

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 from linear_attn_state_chunked_gb300 import hypic, workloads as W
+from oracle import reference as ref
 from _parity import run_pipeline, check_pairs, check_request, tol_of
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -44,6 +45,33 @@ def test_full_size(name):
     if name == "stress_gdn":
         # the slow gate keeps T_C well away from zero, so composition matters
         assert out["T"].abs().amax().item() > 1e-5
+    # every seam again from the prefix states, in the call the benchmark
+    # times: against the fused pass on every block (norms on the device) and
+    # against the oracle's re-run of sampled seams from the same states
+    d = wl.desc
+    o2 = torch.full_like(out["o"], float("nan"))
+    S2 = torch.empty_like(out["S_prefix"])
+    hypic.seam_advance(d, wl.tok, wl.seg_off, wl.order, out["S_prefix"], o2, S_out=S2)
+    torch.cuda.synchronize()
+    num = (o2.double() - out["o"].double()).pow(2).sum(dim=(2, 4)).sqrt()
+    den = out["o"].double().pow(2).sum(dim=(2, 4)).sqrt()
+    rel = torch.where(den > 0, num / den.clamp_min(1e-300), num)
+    assert rel.max().item() <= tol, rel.max().item()
+    rng = np.random.default_rng(7)
+    L, H, n_ord = d["n_layers"], d["n_heads"], len(wl.order)
+    seams = {(L - 1, n_ord - 1, H - 1), (0, 1 % n_ord, 0)}
+    while len(seams) < 6:
+        seams.add((int(rng.integers(L)), int(rng.integers(n_ord)), int(rng.integers(H))))
+    worst = 0.0
+    for (l, e, h) in sorted(seams):
+        o_ref, s_ref = ref.seam_reference(d, wl.tok, wl.seg_off, wl.order, [(l, h)],
+                                          [[out["S_prefix"][l, e, h].cpu().numpy()]], [e])
+        eo = ref.rel_fro(o2[l, e, :, h].cpu().numpy(), o_ref[0, 0])
+        es_ = ref.rel_fro(S2[l, e, h].cpu().numpy(), s_ref[0, 0])
+        worst = max(worst, eo, es_)
+        assert eo <= tol and es_ <= tol, (l, e, h, eo, es_)
+    print("seam advance %s: vs fused %.2e, vs oracle %.2e" % (name, rel.max().item(), worst))
+    del o2, S2
     # the build has no atomics or races: a second run is bitwise identical
     out2 = run_pipeline(wl, prefix=False)
     assert torch.equal(out["T"], out2["T"]) and torch.equal(out["S"], out2["S"])
