@@ -182,7 +182,7 @@ def oracle_sample(wl, n_heads, n_segments):
     cpu_tok = {k: (None if v is None else v.detach().cpu()) for k, v in wl.tok.items()}
     w = d["seam_w"]
     t0 = time.perf_counter()
-    streams = [ref.chain_stream(cpu_tok, d["mode"], 0, h, idx, d["conv_k"]) for h in range(n_heads)]
+    streams = [ref.chain_stream(cpu_tok, d["mode"], 0, h, idx, d["conv_k"], d.get("conv_act", 0)) for h in range(n_heads)]
     q, k, v, a = (np.stack([s[i] for s in streams]) for i in range(4))
     b = np.stack([s[4] for s in streams])
     C, D = n_heads, d["d_k"]

@@ -20,8 +20,11 @@ for the recurrence, the pair and composition, cited there):
   (article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”, section "线性层", last paragraph), followed by the
   per-head L2 normalisation of q and k that gated-delta layers apply after
   it.  The pages give neither formula; the readings are: kernel size K, lag j
-  multiplies x_{t-j}, zero history before the request start, no bias, no
-  activation, and x / sqrt(sum x^2 + eps) with eps = 1e-6.
+  multiplies x_{t-j}, zero history before the request start, no bias, and
+  x / sqrt(sum x^2 + eps) with eps = 1e-6.
+* :func:`silu` -- the optional activation between the conv and the
+  normalisation (x sigma(x), as public gated-delta layers apply it; not on
+  the pages, off unless a descriptor asks for it).
 
 Parity status: every primitive is pinned by ``tests/test_oracle_pins.py``.
 """
@@ -148,6 +151,15 @@ def causal_conv(x, w):
         if j < n:
             y[j:] += w[:, j] * x[:n - j]
     return y
+
+
+def silu(x):
+    """x * sigma(x), sigma the logistic function 1 / (1 + e^-x), evaluated
+    without overflow for either sign of x."""
+    x = _f64(x)
+    e = np.exp(-np.abs(x))
+    sig = np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+    return x * sig
 
 
 def l2_normalize(x, eps=L2_EPS):

@@ -22,7 +22,7 @@ full prefix, advancing the running state and emitting per-token outputs.
 import numpy as np
 
 from . import (GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA, recurrence, pair,
-               causal_conv, l2_normalize)
+               causal_conv, l2_normalize, silu)
 
 
 def _np(x):
@@ -31,12 +31,13 @@ def _np(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def chain_stream(tok, mode, l, h, idx, conv_k=0):
+def chain_stream(tok, mode, l, h, idx, conv_k=0, conv_act=0):
     """q, k, v, a, b of chain (l, h) over token indices idx (a stream that
     starts a request: conv history before idx[0] is zero).
 
     With conv_k > 0 the tokens are raw: q, k, v are convolved along the
-    stream, then q and k are L2-normalised per token.
+    stream (then passed through SiLU when conv_act == 1), then q and k are
+    L2-normalised per token.
     """
     idx = np.asarray(idx, dtype=np.int64)
     q = _np(tok["q"][l, idx, h, :]) if tok.get("q") is not None else None
@@ -44,9 +45,10 @@ def chain_stream(tok, mode, l, h, idx, conv_k=0):
     v = _np(tok["v"][l, idx, h, :])
     if conv_k:
         w = _np(tok["conv_w"][l, :, h, :, :])  # [3, d, K]
-        q = l2_normalize(causal_conv(q, w[0]))
-        k = l2_normalize(causal_conv(k, w[1]))
-        v = causal_conv(v, w[2])
+        act = silu if conv_act == 1 else (lambda x: x)
+        q = l2_normalize(act(causal_conv(q, w[0]))) if q is not None else None
+        k = l2_normalize(act(causal_conv(k, w[1])))
+        v = act(causal_conv(v, w[2]))
     if mode == SCALAR_DECAY:
         a = np.full(len(idx), float(_np(tok["alpha"][l, h])))
     else:
@@ -70,7 +72,7 @@ def pair_reference(desc, tok, seg_off, items):
     Ts, Ss = [], []
     for (l, s, h) in items:
         lo, hi = int(seg_off[s]), int(seg_off[s + 1])
-        q, k, v, a, b = chain_stream(tok, mode, l, h, np.arange(lo, hi), ck)
+        q, k, v, a, b = chain_stream(tok, mode, l, h, np.arange(lo, hi), ck, desc.get("conv_act", 0))
         sw = seam_len(seg_off, s, w)
         T, S = pair(mode, k[None, sw:], v[None, sw:], a[None, sw:],
                     None if b is None else b[None, sw:])
@@ -99,7 +101,7 @@ def request_reference(desc, tok, seg_off, order, chains, S_init=None, want_naive
     out = {"S_prefix": [], "o_seam": [], "S_final": [], "S_naive": []}
     if not chains:
         return {key: np.zeros(0) for key in out}
-    streams = [chain_stream(tok, mode, l, h, idx, ck) for (l, h) in chains]
+    streams = [chain_stream(tok, mode, l, h, idx, ck, desc.get("conv_act", 0)) for (l, h) in chains]
     q, k, v, a = (np.stack([st[i] for st in streams]) for i in range(4))
     b = None if mode not in (GATED_DELTA, KDA) else np.stack([st[4] for st in streams])
     dk, dv = k.shape[2], v.shape[2]
@@ -138,7 +140,7 @@ def seam_reference(desc, tok, seg_off, order, chains, S_in, entries):
     starts = np.cumsum([0] + [int(seg_off[s + 1] - seg_off[s]) for s in order])
     os_, ss_ = [], []
     for ci, (l, h) in enumerate(chains):
-        q, k, v, a, b = chain_stream(tok, mode, l, h, idx, ck)
+        q, k, v, a, b = chain_stream(tok, mode, l, h, idx, ck, desc.get("conv_act", 0))
         dv = v.shape[1]
         o_c, s_c = [], []
         for j, e in enumerate(entries):

@@ -320,6 +320,25 @@ def test_causal_conv():
     np.testing.assert_allclose(y2[K - 1:], y[p:], atol=1e-12)
 
 
+def test_silu():
+    """SiLU = x sigma(x) pinned by identities that do not restate it: the odd
+    part silu(x) - silu(-x) = x (sigma(x) + sigma(-x) = 1), the logistic as
+    (1 + tanh(x / 2)) / 2, silu(0) = 0 with slope 1/2 there, the asymptotes
+    x and 0, and finiteness far out on both sides."""
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal(200) * 6
+    np.testing.assert_allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle.silu(x), x * 0.5 * (1.0 + np.tanh(0.5 * x)), rtol=1e-13, atol=1e-15)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    hstep = 1e-6
+    slope = (oracle.silu(np.array([hstep]))[0] - oracle.silu(np.array([-hstep]))[0]) / (2 * hstep)
+    assert abs(slope - 0.5) < 1e-9
+    big = np.array([40.0, 800.0])
+    np.testing.assert_allclose(oracle.silu(big), big, rtol=1e-15)
+    far = oracle.silu(np.array([-40.0, -800.0]))
+    assert np.all(np.isfinite(far)) and abs(far[0]) < 1e-15 and far[1] == 0.0
+
+
 def test_l2_normalize():
     rng = np.random.default_rng(19)
     x = rng.standard_normal((10, 16)) * 5
