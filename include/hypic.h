@@ -79,7 +79,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_ABI_VERSION 1
+#define HYPIC_ABI_VERSION 2
 #define HYPIC_MAX_SEGMENTS 2048
 
 typedef struct CUstream_st *hypic_stream; /* same type as cudaStream_t */
@@ -102,6 +102,12 @@ typedef enum hypic_mode {
     HYPIC_KDA = 3            /* A_t = (I - beta_t k k^T) diag(alpha_t), W = beta k v^T */
 } hypic_mode;
 
+/* Activation between the causal conv and the L2 normalisation (conv_k > 0). */
+typedef enum hypic_act {
+    HYPIC_ACT_NONE = 0,  /* conv output used as is */
+    HYPIC_ACT_SILU = 1   /* x * sigmoid(x) on q, k and v after the conv */
+} hypic_act;
+
 typedef enum hypic_dtype {
     HYPIC_F32 = 0,
     HYPIC_BF16 = 1
@@ -117,6 +123,7 @@ typedef struct hypic_desc {
     int32_t conv_k;    /* causal depthwise conv taps: 0 (none) or 2..4 */
     int32_t mode;      /* hypic_mode */
     int32_t in_dtype;  /* hypic_dtype of q, k, v, alpha, beta */
+    int32_t conv_act;  /* hypic_act after the conv; must be HYPIC_ACT_NONE when conv_k == 0 */
 } hypic_desc;
 
 /* The packed per-token inputs of a request's tokens (all device pointers). */

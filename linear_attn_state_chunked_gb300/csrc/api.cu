@@ -44,6 +44,10 @@ int check_desc(const hypic_desc *d)
         return fail(HYPIC_ERR_SHAPE, "seam_w=%d not in [0, 64]", d->seam_w);
     if (d->conv_k != 0 && (d->conv_k < 2 || d->conv_k > 4))
         return fail(HYPIC_ERR_UNSUPPORTED, "conv_k=%d not in {0, 2, 3, 4}", d->conv_k);
+    if (d->conv_act != HYPIC_ACT_NONE && d->conv_act != HYPIC_ACT_SILU)
+        return fail(HYPIC_ERR_INVALID_ARG, "unknown conv_act %d", d->conv_act);
+    if (d->conv_act != HYPIC_ACT_NONE && d->conv_k == 0)
+        return fail(HYPIC_ERR_INVALID_ARG, "conv_act %d without a conv (conv_k = 0)", d->conv_act);
     if (d->conv_k > 0 && d->seam_w < d->conv_k - 1)
         return fail(HYPIC_ERR_UNSUPPORTED,
                     "conv_k=%d needs seam_w >= %d so that cached bodies are prefix-independent",
@@ -108,7 +112,7 @@ int check_out(const void *p, const char *name)
 
 Dims make_dims(const hypic_desc *d)
 {
-    return Dims{d->n_layers, d->n_heads, d->d_k, d->seam_w, d->conv_k, d->mode, d->in_dtype};
+    return Dims{d->n_layers, d->n_heads, d->d_k, d->seam_w, d->conv_k, d->mode, d->in_dtype, d->conv_act};
 }
 
 TokPtrs make_tok(const hypic_tokens *t)

@@ -92,8 +92,8 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
                         vv = fmaf(wv[ch * CK + j], ld_f(vp, tok_index(dm, N, l, tj, h, ch)), vv);
                     }
                 }
-                ks[i][ch] = kv;
-                vs[i][ch] = vv;
+                ks[i][ch] = dm.act ? silu(kv) : kv;
+                vs[i][ch] = dm.act ? silu(vv) : vv;
             }
             if (MODE == HYPIC_DIAG_GATE || MODE == HYPIC_KDA) as_[i][ch] = ld_f(ap, tok_index(dm, N, l, tok, h, ch));
         }

@@ -719,6 +719,12 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                                 for (int i = 0; i < 8; ++i) kx[r][i] = fmaf(wj[i], rk[i], kx[r][i]);
                             }
                         }
+                        if (dm.act) {
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) kx[r][i] = silu(kx[r][i]);
+                        }
                     }
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
@@ -882,6 +888,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             } else {
 #pragma unroll
                                 for (int j = 0; j < (CK > 0 ? CK : 1); ++j) vv = fmaf(wvr[j], win[j], vv);
+                                if (dm.act) vv = silu(vv);
                             }
                             if (t >= nc) vv = 0.f;
                             p[i] = tc::round_tf32(fmaf(-G.eg[t], p[i], vv));

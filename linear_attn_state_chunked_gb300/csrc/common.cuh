@@ -19,8 +19,11 @@ constexpr int kMaxSeg = HYPIC_MAX_SEGMENTS;
 constexpr float kL2Eps = 1e-6f;
 
 struct Dims {
-    int L, H, D, w, conv_k, mode, dtype;
+    int L, H, D, w, conv_k, mode, dtype, act;  // act: hypic_act after the conv
 };
+
+// SiLU, x sigma(x), applied after the causal conv when Dims::act says so.
+__device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 
 struct TokPtrs {
     const void *q, *k, *v, *alpha, *beta;

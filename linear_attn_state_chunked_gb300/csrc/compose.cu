@@ -71,9 +71,9 @@ __device__ __forceinline__ void stage_token(const Dims &dm, const TokPtrs &tk, c
                     vv = fmaf(wv[lag], ld_f(vp, ix), vv);
                 }
             }
-            st.q[ch] = qv;
-            st.k[ch] = kv;
-            st.v[ch] = vv;
+            st.q[ch] = dm.act ? silu(qv) : qv;
+            st.k[ch] = dm.act ? silu(kv) : kv;
+            st.v[ch] = dm.act ? silu(vv) : vv;
         }
         if (MODE == HYPIC_DIAG_GATE || MODE == HYPIC_KDA) st.a[ch] = ld_f(ap, tok_index(dm, N, l, tok, h, ch));
     }

@@ -543,6 +543,14 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                     }
                 }
             }
+            if (CK > 0 && dm.act) {
+#pragma unroll
+                for (int t = 0; t < WMAX; ++t) {
+                    qv[t] = silu(qv[t]);
+                    kv[t] = silu(kv[t]);
+                    vv[t] = silu(vv[t]);
+                }
+            }
             if (CK > 0) {
                 float sq[WMAX], sk[WMAX];
 #pragma unroll

@@ -130,6 +130,11 @@ __device__ __forceinline__ void stage_pass(ChunkSmem<D> &sm, const Dims &dm, con
                 c = fmaf(wk[lag], rk[u + CK - 1 - lag], c);
                 e = fmaf(wv[lag], rv[u + CK - 1 - lag], e);
             }
+            if (dm.act) {
+                a = silu(a);
+                c = silu(c);
+                e = silu(e);
+            }
             const bool live = jb + u < sw;
             qq[u] = live ? a : 0.f;
             kk[u] = live ? c : 0.f;
@@ -681,6 +686,11 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
                         q_ = fmaf(wq[lag], rq_[j + CK - 1 - lag], q_);
                         k_ = fmaf(wk[lag], rk_[j + CK - 1 - lag], k_);
                         v_ = fmaf(wv[lag], rv_[j + CK - 1 - lag], v_);
+                    }
+                    if (dm.act) {
+                        q_ = silu(q_);
+                        k_ = silu(k_);
+                        v_ = silu(v_);
                     }
                     const bool live = j < sw;
                     qq[j] = live ? q_ : 0.f;

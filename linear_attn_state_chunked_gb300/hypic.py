@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_PKG, "libhypic.so")
 
 GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA = 0, 1, 2, 3
 F32, BF16 = 0, 1
+ACT_NONE, ACT_SILU = 0, 1
 MAX_SEGMENTS = 2048
 
 STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_INVALID_ARG", 2: "HYPIC_ERR_SHAPE", 3: "HYPIC_ERR_DTYPE",
@@ -35,7 +36,7 @@ class HypicError(RuntimeError):
 
 class Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("n_layers", "n_heads", "d_k", "d_v", "seam_w", "conv_k", "mode", "in_dtype")]
+                ("n_layers", "n_heads", "d_k", "d_v", "seam_w", "conv_k", "mode", "in_dtype", "conv_act")]
 
 
 class Tokens(ctypes.Structure):
@@ -89,8 +90,8 @@ def _p(t):
 
 
 def make_desc(d):
-    return Desc(*(int(d[n]) for n in ("n_layers", "n_heads", "d_k", "d_v", "seam_w", "conv_k",
-                                      "mode", "in_dtype")))
+    return Desc(*(int(d.get(n, 0)) for n in ("n_layers", "n_heads", "d_k", "d_v", "seam_w", "conv_k",
+                                             "mode", "in_dtype", "conv_act")))
 
 
 def make_tokens(tok, n_tokens):

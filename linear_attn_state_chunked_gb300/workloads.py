@@ -130,7 +130,7 @@ NAMES = tuple(_SPECS)
 def describe(name, **over):
     mode, L, H, d, dt, seed, w, ck, gdiv = _SPECS[name]
     desc = dict(n_layers=L, n_heads=H, d_k=d, d_v=d, seam_w=w, conv_k=ck,
-                mode=mode, in_dtype=dt)
+                mode=mode, in_dtype=dt, conv_act=0)
     desc.update(over)
     return desc
 

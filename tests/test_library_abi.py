@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(L):
     assert set(syms) == set(hypic.EXPORTS)
     for s in syms:
         assert hasattr(L, s), s
-    assert L.hypic_version() == 1
+    assert L.hypic_version() == 2
     assert b"" == L.hypic_last_error()
 
 
@@ -95,6 +95,8 @@ BAD_BUILD = [
     ("conv_k", dict(desc=_desc(conv_k=5)), 4),
     ("conv without seam", dict(desc=_desc(conv_k=4, seam_w=2)), 4),
     ("conv_w missing", dict(desc=_desc(conv_k=4)), 1),
+    ("conv_act unknown", dict(desc=_desc(conv_k=4, conv_act=2)), 1),
+    ("conv_act without conv", dict(desc=_desc(conv_act=1)), 1),
     ("k null", dict(desc=_desc(), tok=_tok(k=None)), 1),
     ("beta null", dict(desc=_desc(), tok=_tok(beta=None)), 1),
     ("v misaligned", dict(desc=_desc(), tok=_tok(v=FAKE + 4)), 1),

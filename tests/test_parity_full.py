@@ -30,9 +30,13 @@ def _sample(wl, n_items, n_chains, seed):
     return sorted(items), sorted(chains)
 
 
-@pytest.mark.parametrize("name", ["gdn_bf16", "stress_gdn", "warm_30l", "cold_30l"])
+@pytest.mark.parametrize("name", ["gdn_bf16", "stress_gdn", "warm_30l", "cold_30l", "cold_30l+silu"])
 def test_full_size(name):
-    wl = W.make(name, device="cuda")
+    if name == "cold_30l+silu":
+        # the cold prompt's full token count, three layers, SiLU after the conv
+        wl = W.make("cold_30l", device="cuda", layers=3, conv_act=hypic.ACT_SILU)
+    else:
+        wl = W.make(name, device="cuda")
     out = run_pipeline(wl, prefix=True)
     tol = tol_of(wl.desc)
     for key in ("T", "S", "S_final", "S_prefix", "o"):

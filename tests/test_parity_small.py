@@ -172,7 +172,17 @@ def test_seam_advance_from_given_states(d, dtype, ck, w, with_out):
     tokens in one pass over the state and longer ones in several passes;
     empty, one-token and shorter-than-seam segments; a repeated segment;
     the conv history crossing several short entries."""
-    over = dict(conv_k=ck) if ck else {}
+    _seam_from_states(d, dtype, ck, w, with_out)
+
+
+@pytest.mark.parametrize("d,dtype,ck,w", [(128, hypic.BF16, 4, 8), (64, hypic.F32, 3, 9)])
+def test_seam_advance_conv_silu(d, dtype, ck, w):
+    """The same with SiLU between the conv and the normalisation."""
+    _seam_from_states(d, dtype, ck, w, True, act=hypic.ACT_SILU)
+
+
+def _seam_from_states(d, dtype, ck, w, with_out, act=0):
+    over = dict(conv_k=ck, conv_act=act) if ck else {}
     wl = W.make("cold_30l" if ck else "stress_tiny", device="cuda", layers=2, lengths=EDGE_LENGTHS,
                 order=EDGE_ORDER, n_heads=2, d_k=d, d_v=d, seam_w=w, in_dtype=dtype, **over)
     desc = wl.desc
@@ -202,3 +212,23 @@ def test_seam_advance_from_given_states(d, dtype, ck, w, with_out):
             if with_out:
                 assert ref.rel_fro(Son[l, e, h], s_ref[0, e]) <= tol, ("S", l, e, h)
     print("\nseam advance d=%d w=%d: worst o %.2e (tol %.0e)" % (d, w, worst, tol))
+
+
+@pytest.mark.parametrize("d,dtype", [(128, hypic.BF16), (64, hypic.BF16), (32, hypic.F32)])
+def test_conv_silu(d, dtype):
+    """Causal conv followed by SiLU before the L2 normalisation (the
+    tensor-core path at d = 128 bf16, the CUDA-core path otherwise): every
+    pair, and composition with seams, against the oracle; negative control:
+    the oracle without the activation misses the GPU result by far more than
+    the tolerance."""
+    wl = W.make("cold_30l", device="cuda", layers=2, lengths=[9, 40, 3, 1, 25, 12, 0, 17, 300, 70],
+                order=[4, 2, 3, 0, 7, 5, 1, 6, 8, 9], n_heads=2, d_k=d, d_v=d, in_dtype=dtype,
+                conv_act=hypic.ACT_SILU)
+    out = run_pipeline(wl)
+    tol = tol_of(wl.desc)
+    et, es = check_pairs(wl, out, _all_items(wl), tol)
+    res = check_request(wl, out, _all_chains(wl), tol)
+    print("\nconv+SiLU d=%d: T %.2e  S %.2e  S_final %.2e  seam o %.2e  (tol %.0e)"
+          % (d, et, es, res["final"], res["o"], tol))
+    plain = ref.request_reference(dict(wl.desc, conv_act=0), wl.tok, wl.seg_off, wl.order, [(1, 1)])
+    assert ref.rel_fro(out["S_final"][1, 1].cpu().numpy(), plain["S_final"][0]) > 100 * tol
