@@ -161,6 +161,20 @@ size_t hypic_workspace_size(const hypic_desc *desc);
 int hypic_workspace_status(const void *workspace, hypic_stream stream);
 
 /*
+ * Self-test of the bounded device-side wait that every pipelined kernel
+ * uses (so that a missing arrival ends a CTA instead of hanging the GPU):
+ * clears the workspace status word and launches one CTA on `stream` in which
+ * one thread waits on an mbarrier that nothing completes, giving up after
+ * max_cycles SM cycles and raising the CTA's abort flag, while a thread of
+ * another warp, waiting on the same barrier with a 64x longer limit, must
+ * leave as soon as it sees the flag.  hypic_workspace_status then returns
+ * HYPIC_ERR_TIMEOUT with status 3 (1: the flag was raised; 2: the second
+ * waiter left without the phase completing).  The device stays usable.
+ * max_cycles in [1, 2^34]; workspace as for hypic_segment_build.
+ */
+int hypic_selftest_bounded_wait(void *workspace, int64_t max_cycles, hypic_stream stream);
+
+/*
  * Segment build: for every segment s, layer l and head h, the cached pair of
  * the segment's body -- the segment's tokens after its first min(w, len)
  * seam tokens -- computed from a zero state:

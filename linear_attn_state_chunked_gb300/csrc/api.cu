@@ -169,6 +169,11 @@ int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok, const i
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < hypic_workspace_size(desc))
         return fail(HYPIC_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes",
                     hypic_workspace_size(desc));
+    // every build starts from a clear status word, whichever kernel runs
+    {
+        cudaError_t e = cudaMemsetAsync(static_cast<char *>(workspace) + 128, 0, sizeof(int), (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "status word clear");
+    }
     if (n_seg == 0) return HYPIC_OK;
 
     static thread_local SegTable tab;

@@ -156,15 +156,7 @@ __device__ __forceinline__ float bf16_at(const uint8_t *tile, int row, int col)
 // Bounded wait by one thread; any failure (or another role's) aborts the CTA.
 __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
 {
-    const long long t0 = clock64();
-    while (!tc::mbar_try(mbar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            *abort_flag = 1;
-            return false;
-        }
-    }
-    return true;
+    return tc::wait_bounded(mbar, parity, abort_flag, kWaitCycles);
 }
 
 // Warp-level tf32 MMA, 16 x 8 x 8, accumulate into c.
@@ -404,7 +396,7 @@ __device__ __forceinline__ void issue_ps(uint32_t tb, uint32_t sK32)
         tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(128, 64), ks > 0);
 }
 
-template <int CK>
+template <int CK, bool ACT>
 __global__ void __launch_bounds__(NT, 1)
 build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ SegTable tab,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV)
@@ -719,7 +711,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                                 for (int i = 0; i < 8; ++i) kx[r][i] = fmaf(wj[i], rk[i], kx[r][i]);
                             }
                         }
-                        if (dm.act) {
+                        if (ACT) {
 #pragma unroll
                             for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -888,7 +880,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             } else {
 #pragma unroll
                                 for (int j = 0; j < (CK > 0 ? CK : 1); ++j) vv = fmaf(wvr[j], win[j], vv);
-                                if (dm.act) vv = silu(vv);
+                                if (ACT) vv = silu(vv);
                             }
                             if (t >= nc) vv = 0.f;
                             p[i] = tc::round_tf32(fmaf(-G.eg[t], p[i], vv));
@@ -975,15 +967,11 @@ cudaError_t launch_build_tc(const BuildArgs &a, const SegTable &tab, cudaStream_
     if ((e = make_token_map(&tmV, a.tok.v, a.dm, a.tok.N, rows)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.status, 0, sizeof(int), st)) != cudaSuccess) return e;
     const int grid = n_items < g_num_sms ? n_items : g_num_sms;
-    if (a.dm.conv_k == 0) {
-        if ((e = cudaFuncSetAttribute(build_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)))
-            return e;
-        build_tc_kernel<0><<<grid, NT, SMEM_DYN, st>>>(a, tab, tmK, tmV);
-    } else {
-        if ((e = cudaFuncSetAttribute(build_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN)))
-            return e;
-        build_tc_kernel<4><<<grid, NT, SMEM_DYN, st>>>(a, tab, tmK, tmV);
-    }
+    // the activation after the conv is a template flag: no cost when off
+    auto kern = a.dm.conv_k == 0 ? build_tc_kernel<0, false>
+                                 : (a.dm.act ? build_tc_kernel<4, true> : build_tc_kernel<4, false>);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN))) return e;
+    kern<<<grid, NT, SMEM_DYN, st>>>(a, tab, tmK, tmV);
     return cudaGetLastError();
 }
 

@@ -96,15 +96,7 @@ enum {
 
 __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
 {
-    const long long t0 = clock64();
-    while (!tc::mbar_try(mbar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            *abort_flag = 1;
-            return false;
-        }
-    }
-    return true;
+    return tc::wait_bounded(mbar, parity, abort_flag, kWaitCycles);
 }
 
 struct TokMaps {

@@ -237,6 +237,25 @@ __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int c0, int c1
                  :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1) : "memory");
 }
 
+// Bounded wait by one thread of a CTA whose roles share abort_flag: true once
+// the phase with the given parity has completed; false if another role has
+// already given up (the flag is set) or if max_cycles SM cycles pass first,
+// in which case this thread raises the flag.  Every pipelined kernel waits
+// this way, so that a missing arrival ends the CTA instead of hanging it.
+__device__ __forceinline__ bool wait_bounded(uint32_t mbar, uint32_t parity, volatile int *abort_flag,
+                                             long long max_cycles)
+{
+    const long long t0 = clock64();
+    while (!mbar_try(mbar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > max_cycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Untiled bulk copy global -> shared, completing on an mbarrier.  Both
 // addresses 16-byte aligned, `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar)

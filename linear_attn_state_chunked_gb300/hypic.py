@@ -25,7 +25,7 @@ STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_INVALID_ARG", 2: "HYPIC_ERR_SHAPE", 3: "H
 # Every symbol include/hypic.h declares.
 EXPORTS = ("hypic_version", "hypic_last_error", "hypic_workspace_size",
            "hypic_workspace_status", "hypic_segment_build", "hypic_segment_build_noalloc",
-           "hypic_compose", "hypic_seam_advance")
+           "hypic_compose", "hypic_seam_advance", "hypic_selftest_bounded_wait")
 
 
 class HypicError(RuntimeError):
@@ -65,6 +65,8 @@ def lib():
         L.hypic_workspace_size.argtypes = [ctypes.POINTER(Desc)]
         L.hypic_workspace_status.restype = ctypes.c_int
         L.hypic_workspace_status.argtypes = [vp, vp]
+        L.hypic_selftest_bounded_wait.restype = ctypes.c_int
+        L.hypic_selftest_bounded_wait.argtypes = [vp, ctypes.c_int64, vp]
         L.hypic_segment_build.restype = ctypes.c_int
         L.hypic_segment_build.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p, i32,
                                           fp, fp, vp, ctypes.c_size_t, vp]
@@ -140,6 +142,12 @@ def workspace_status(workspace, stream=None):
     """Raise HypicError(HYPIC_ERR_TIMEOUT) if a device-side wait of a build on
     this workspace gave up; waits for the stream."""
     _check(lib().hypic_workspace_status(_p(workspace), _stream(stream)))
+
+
+def selftest_bounded_wait(workspace, max_cycles, stream=None):
+    """Run the bounded-wait self-test into the workspace status word (read it
+    back with workspace_status, which then raises HYPIC_ERR_TIMEOUT)."""
+    _check(lib().hypic_selftest_bounded_wait(_p(workspace), int(max_cycles), _stream(stream)))
 
 
 def pair_shapes(desc, n_seg):

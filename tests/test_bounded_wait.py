@@ -1,0 +1,42 @@
+"""Failure detection without a fault: the bounded device-side wait that the
+pipelined kernels use gives up on a barrier that nothing completes, reports
+through the workspace status word, lets a second waiter leave on the CTA's
+abort flag, and leaves the device usable."""
+import time
+
+import pytest
+import torch
+
+from linear_attn_state_chunked_gb300 import hypic, workloads as W
+from _parity import run_pipeline, check_pairs, tol_of
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_gives_up_and_reports():
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    max_cycles = 20_000_000  # ~10 ms; the second waiter's own limit is 64x that (~0.6 s)
+    hypic.selftest_bounded_wait(ws, 1000)  # load the module before timing
+    with pytest.raises(hypic.HypicError):
+        hypic.workspace_status(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    hypic.selftest_bounded_wait(ws, max_cycles)
+    with pytest.raises(hypic.HypicError) as ei:
+        hypic.workspace_status(ws)
+    dt = time.perf_counter() - t0
+    assert ei.value.status == 7 and "status 3" in str(ei.value), str(ei.value)
+    assert dt < 0.3, dt  # the second waiter left on the flag, not on its own limit
+
+    # the device is still usable, and the next build on the workspace clears the word
+    wl = W.make("tiny_gdn", device="cuda")
+    d = wl.desc
+    tshape, sshape = hypic.pair_shapes(d, wl.n_seg)
+    T = torch.empty(tshape, device="cuda")
+    S = torch.empty(sshape, device="cuda")
+    hypic.segment_build(d, wl.tok, wl.seg_off, T, S, ws)
+    hypic.workspace_status(ws)
+    out = run_pipeline(wl)
+    items = [(l, s, h) for l in range(d["n_layers"]) for s in range(wl.n_seg) for h in range(d["n_heads"])]
+    check_pairs(wl, out, items, tol_of(d))
+    assert torch.equal(out["T"], T) and torch.equal(out["S"], S)

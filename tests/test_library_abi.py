@@ -165,3 +165,13 @@ def test_binding_raises_with_message(L):
     with pytest.raises(hypic.HypicError) as ei:
         hypic._check(_build(_desc(mode=9)))
     assert "HYPIC_ERR_INVALID_ARG" in str(ei.value) and "mode" in str(ei.value)
+
+
+def test_selftest_rejects_bad_arguments(L):
+    """Argument checks of the bounded-wait self-test happen on the host,
+    before anything is launched (no GPU needed)."""
+    assert L.hypic_selftest_bounded_wait(None, 1000, None) == 5
+    assert L.hypic_selftest_bounded_wait(FAKE + 16, 1000, None) == 5
+    assert L.hypic_selftest_bounded_wait(FAKE, 0, None) == 2
+    assert L.hypic_selftest_bounded_wait(FAKE, (1 << 34) + 1, None) == 2
+    assert b"max_cycles" in L.hypic_last_error()
