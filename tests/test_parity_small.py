@@ -175,6 +175,27 @@ def test_seam_advance_from_given_states(d, dtype, ck, w, with_out):
     _seam_from_states(d, dtype, ck, w, with_out)
 
 
+@pytest.mark.parametrize("d,dtype,ck,w", [(128, hypic.BF16, 4, 8), (128, hypic.F32, 0, 5), (32, hypic.BF16, 4, 12)])
+def test_seam_advance_in_place(d, dtype, ck, w):
+    """S_out aliasing S_in (the state advanced in place) gives the same
+    outputs and states as separate buffers."""
+    over = dict(conv_k=ck) if ck else {}
+    wl = W.make("cold_30l" if ck else "stress_tiny", device="cuda", layers=2, lengths=EDGE_LENGTHS,
+                order=EDGE_ORDER, n_heads=2, d_k=d, d_v=d, seam_w=w, in_dtype=dtype, **over)
+    desc = wl.desc
+    L, H, n_ord = desc["n_layers"], desc["n_heads"], len(wl.order)
+    g = torch.Generator(device="cuda").manual_seed(4242 + d)
+    S_in = 0.5 * torch.randn((L, n_ord, H, d, d), generator=g, device="cuda")
+    o1 = torch.empty((L, n_ord, w, H, d), device="cuda")
+    S1 = torch.empty_like(S_in)
+    hypic.seam_advance(desc, wl.tok, wl.seg_off, wl.order, S_in, o1, S_out=S1)
+    S2 = S_in.clone()
+    o2 = torch.empty_like(o1)
+    hypic.seam_advance(desc, wl.tok, wl.seg_off, wl.order, S2, o2, S_out=S2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+
+
 @pytest.mark.parametrize("d,dtype,ck,w", [(128, hypic.BF16, 4, 8), (64, hypic.F32, 3, 9)])
 def test_seam_advance_conv_silu(d, dtype, ck, w):
     """The same with SiLU between the conv and the normalisation."""
