@@ -81,6 +81,27 @@ def pair_reference(desc, tok, seg_off, items):
     return np.stack(Ts), np.stack(Ss)
 
 
+def body_output_reference(desc, tok, seg_off, items):
+    """Per-token outputs of the body of segment s from a zero state, for each
+    (l, s, h) in items: the segment's own first prefill (conv history from
+    the segment itself), o_t = S_t^T q_t over the body tokens.
+    Returns a list of [n_body, dv] arrays.
+    """
+    mode, w, ck = desc["mode"], desc["seam_w"], desc.get("conv_k", 0)
+    outs = []
+    for (l, s, h) in items:
+        lo, hi = int(seg_off[s]), int(seg_off[s + 1])
+        q, k, v, a, b = chain_stream(tok, mode, l, h, np.arange(lo, hi), ck, desc.get("conv_act", 0))
+        sw = seam_len(seg_off, s, w)
+        if hi - lo - sw == 0:
+            outs.append(np.zeros((0, v.shape[1])))
+            continue
+        _, o, _ = recurrence(mode, q[None, sw:], k[None, sw:], v[None, sw:], a[None, sw:],
+                             None if b is None else b[None, sw:], want_o=True)
+        outs.append(o[0])
+    return outs
+
+
 def request_reference(desc, tok, seg_off, order, chains, S_init=None, want_naive=False):
     """Run the recurrence over the whole request (segments in `order`) for
     each chain (l, h) in chains.

@@ -377,3 +377,24 @@ def test_kda_composition_law():
     Sf, _, _ = oracle.recurrence(KDA, None, k[None], v[None], a[None], b[None], want_o=False)
     np.testing.assert_allclose(T2[0] @ S1[0] + S2[0], Sf[0], rtol=0, atol=1e-12)
     np.testing.assert_allclose(oracle.compose(T2, S2, S1)[0], Sf[0], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["tiny_gdn", "decay_retnet", "decay_diag", "kda_tiny"])
+def test_body_outputs_end_on_the_pair(name):
+    """The body outputs of a segment's first prefill end on its pair: the
+    last body token's output is S(C|0)^T q of that token, with S(C|0) from
+    the pair routine (an independent code path: transitions applied to a
+    zero state, no outputs)."""
+    from linear_attn_state_chunked_gb300 import workloads as W
+    from oracle import reference as ref
+    wl = W.make(name, device="cpu")
+    d = wl.desc
+    items = [(0, s, 0) for s in range(wl.n_seg)]
+    outs = ref.body_output_reference(d, wl.tok, wl.seg_off, items)
+    _, Sref = ref.pair_reference(d, wl.tok, wl.seg_off, items)
+    for (l, s, h), o, S in zip(items, outs, Sref):
+        if len(o) == 0:
+            continue
+        lo, hi = int(wl.seg_off[s]), int(wl.seg_off[s + 1])
+        q, _, _, _, _ = ref.chain_stream(wl.tok, d["mode"], l, h, np.arange(lo, hi), d.get("conv_k", 0))
+        np.testing.assert_allclose(o[-1], S.T @ q[-1], rtol=1e-10, atol=1e-12)
