@@ -328,6 +328,28 @@ def run_gpu(args):
     seam_ms = a0.elapsed_time(a1) / args.steps
     del Sp
 
+    # segment forward (per-token body outputs from a zero state: the segment's
+    # first prefill) on the first layer, with and without the pair -- the
+    # pair's cost next to the linear layer's own prefill, on the exact-fp32
+    # token-serial CUDA-core build that serves the forward
+    d1 = dict(d, n_layers=1)
+    tok1 = {k: (None if v is None else v[:1]) for k, v in wl.tok.items()}
+    o1 = torch.empty((1, wl.n_tokens, H, D), device=dev)
+    T1 = torch.empty((1,) + tuple(tshape[1:]), device=dev)
+    S1 = torch.empty((1,) + tuple(sshape[1:]), device=dev)
+    fwd = {}
+    for key, kw in (("outputs_only", {}), ("with_pair", dict(T_out=T1, S_out=S1))):
+        hypic.segment_forward(d1, tok1, wl.seg_off, o1, stream=stream, **kw)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(2):
+            hypic.segment_forward(d1, tok1, wl.seg_off, o1, stream=stream, **kw)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        fwd[key] = f0.elapsed_time(f1) / 2
+    del o1, T1, S1
+
     tokens = wl.n_tokens
     body_tokens = int(sum(max(0, int(x) - min(w, int(x))) for x in wl.lengths))
     ms_step = ms_total / args.steps
@@ -469,6 +491,12 @@ def run_gpu(args):
                                              / peaks["hbm_gbs"],
                                  "launches_per_step": 1,
                                  "note": "prefix states in, seam outputs out; state not written back"},
+                "segment_forward_layer0": {"ms_outputs_only": fwd["outputs_only"],
+                                           "ms_with_pair": fwd["with_pair"],
+                                           "pair_overhead": fwd["with_pair"] / fwd["outputs_only"] - 1.0,
+                                           "note": "per-token body outputs of layer 0 from a zero state on the "
+                                                   "exact-fp32 token-serial CUDA-core build, alone and with "
+                                                   "(T_C, S(C|0)); the linear layer only, not a whole model"},
                 "compose_with_seams": {"segs_s_per_layer": comp_segs, "ms": comp_ms,
                                        "gbs": comp_gbs, "hbm_frac": comp_gbs / peaks["hbm_gbs"],
                                        "launches_per_step": 1}},

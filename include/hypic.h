@@ -34,7 +34,10 @@
  *   hypic_compose         -- the running state over a request's segment order,
  *                            with each entry's seam re-run in the same pass;
  *   hypic_seam_advance    -- the seams alone, all entries in parallel, from
- *                            given prefix states.
+ *                            given prefix states;
+ *   hypic_segment_forward -- the segment bodies' per-token outputs from a zero
+ *                            state (the segment's first prefill), with or
+ *                            without the pair.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -79,7 +82,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_ABI_VERSION 2
+#define HYPIC_ABI_VERSION 3
 #define HYPIC_MAX_SEGMENTS 2048
 
 typedef struct CUstream_st *hypic_stream; /* same type as cudaStream_t */
@@ -159,6 +162,27 @@ size_t hypic_workspace_size(const hypic_desc *desc);
  * clears the word.
  */
 int hypic_workspace_status(const void *workspace, hypic_stream stream);
+
+/*
+ * Segment forward: the per-token outputs of every segment body computed from
+ * a zero state -- the segment's own first prefill, the main forward that the
+ * pair is cached alongside (HYPIC pages: article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token 延迟降低 3.25 倍，实现位置无关缓存”,
+ * sections "线性层" and "段并行"; article “Xiaohongshu, Peking University, Shanghai Jiao Tong University Unveil HYPIC to Slash First Token Latency by 3.25x in Hybrid Attention Models”,
+ * linear-layer and segment-parallelism paragraphs) -- and, optionally, the
+ * pair itself:
+ *     o_out[l][t][h][:] = S_t^T q_t  for every body token t of every segment
+ *         (S_t the zero-initial state after t; the rows of seam tokens are
+ *         left untouched -- their outputs come from hypic_compose);
+ *     T_out, S_out exactly as hypic_segment_build, each optional (NULL skips
+ *         it: with both NULL this is the plain forward).
+ * q is required.  Runs on the exact-fp32 token-serial build for every mode,
+ * width and dtype (no tensor cores).  o_out: fp32 [L][N][H][d_v], 16-byte
+ * aligned; no workspace.
+ */
+int hypic_segment_forward(const hypic_desc *desc, const hypic_tokens *tok,
+                          const int64_t *seg_off, int32_t n_seg,
+                          float *o_out, float *T_out, float *S_out,
+                          hypic_stream stream);
 
 /*
  * Self-test of the bounded device-side wait that every pipelined kernel

@@ -132,6 +132,22 @@ void fill_offsets(SegTable &tab, const int64_t *seg_off, int32_t n_seg)
     for (int32_t i = 0; i <= n_seg; ++i) tab.off[i] = (int32_t)seg_off[i];
 }
 
+// Request table of a build: segment offsets, and the items' order longest
+// body first (ties: lower index first), the greedy LPT order.
+void fill_build_table(SegTable &tab, const int64_t *seg_off, int32_t n_seg, int w)
+{
+    fill_offsets(tab, seg_off, n_seg);
+    auto body = [&](int s) {
+        const int64_t len = seg_off[s + 1] - seg_off[s];
+        return len - std::min<int64_t>(w, len);
+    };
+    std::vector<int32_t> idx(n_seg);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return body(a) > body(b); });
+    for (int32_t i = 0; i < n_seg; ++i) tab.perm[i] = idx[i];
+    tab.n_perm = n_seg;
+}
+
 int cuda_fail(cudaError_t e, const char *what)
 {
     return fail(HYPIC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -177,18 +193,7 @@ int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok, const i
     if (n_seg == 0) return HYPIC_OK;
 
     static thread_local SegTable tab;
-    fill_offsets(tab, seg_off, n_seg);
-    // Longest body first (ties: lower index first): the greedy LPT order.
-    const int w = desc->seam_w;
-    auto body = [&](int s) {
-        const int64_t len = seg_off[s + 1] - seg_off[s];
-        return len - std::min<int64_t>(w, len);
-    };
-    std::vector<int32_t> idx(n_seg);
-    std::iota(idx.begin(), idx.end(), 0);
-    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return body(a) > body(b); });
-    for (int32_t i = 0; i < n_seg; ++i) tab.perm[i] = idx[i];
-    tab.n_perm = n_seg;
+    fill_build_table(tab, seg_off, n_seg, desc->seam_w);
 
     BuildArgs a{};
     a.dm = make_dims(desc);
@@ -203,6 +208,33 @@ int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok, const i
     cudaError_t e = build_tc_supported(a.dm) ? launch_build_tc(a, tab, (cudaStream_t)stream)
                                              : launch_build_rec(a, tab, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "segment build launch");
+    return HYPIC_OK;
+}
+
+int hypic_segment_forward(const hypic_desc *desc, const hypic_tokens *tok, const int64_t *seg_off,
+                          int32_t n_seg, float *o_out, float *T_out, float *S_out, hypic_stream stream)
+{
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_desc(desc))) return rc;
+    if ((rc = check_tokens(desc, tok, true))) return rc;
+    if ((rc = check_segments(seg_off, n_seg, tok->n_tokens))) return rc;
+    if ((rc = check_out(o_out, "o_out"))) return rc;
+    if (T_out && !aligned(T_out, 16)) return fail(HYPIC_ERR_INVALID_ARG, "T_out is not 16-byte aligned");
+    if (S_out && !aligned(S_out, 16)) return fail(HYPIC_ERR_INVALID_ARG, "S_out is not 16-byte aligned");
+    if (n_seg == 0) return HYPIC_OK;
+
+    static thread_local SegTable tab;
+    fill_build_table(tab, seg_off, n_seg, desc->seam_w);
+    BuildArgs a{};
+    a.dm = make_dims(desc);
+    a.tok = make_tok(tok);
+    a.T_out = T_out;
+    a.S_out = S_out;
+    a.o_out = o_out;
+    // the outputs come from the exact-fp32 token-serial build, for every mode
+    cudaError_t e = launch_build_rec(a, tab, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "segment forward launch");
     return HYPIC_OK;
 }
 

@@ -14,6 +14,11 @@
 // A_t = alpha (I - beta k k^T) applied on the left, plus the write
 // beta k v^T on the S half (the pair (T_C, S(C|0)) of that article's "线性层").
 // The two specialisations keep only S and form T as the product of gates.
+//
+// It also serves the segment forward: with an output buffer, each S-column
+// thread emits o_t = S_t^T q_t for every body token (its column of S_t dotted
+// with q_t, the segment's own zero-initial state); without a T buffer the T
+// columns stay idle (the forward without the transition product).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -38,6 +43,7 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
     constexpr bool DENSE_T = (MODE == HYPIC_GATED_DELTA || MODE == HYPIC_KDA);
     __shared__ __align__(16) float ks[kChunk][D];
     __shared__ __align__(16) float vs[kChunk][D];
+    __shared__ __align__(16) float qs[kChunk][D];  // forward outputs only
     __shared__ float as_[kChunk][AW];
     __shared__ float bs[kChunk];
 
@@ -53,6 +59,11 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
     const int32_t n = seg1 - b0;
     const int c = threadIdx.x;
 
+    const bool want_o = a.o_out != nullptr, want_t = a.T_out != nullptr, want_s = a.S_out != nullptr;
+    // S columns emit the outputs; T columns work only when T is wanted
+    const bool s_col = !DENSE_T || c >= D;
+    const bool active = c < NCOL && (s_col || want_t);
+    const Tin *qp = static_cast<const Tin *>(a.tok.q);
     const Tin *kp = static_cast<const Tin *>(a.tok.k);
     const Tin *vp = static_cast<const Tin *>(a.tok.v);
     const Tin *ap = static_cast<const Tin *>(a.tok.alpha);
@@ -67,8 +78,9 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
     float tprod = 1.f;
 
     // conv taps of this head for the k and v channels: w[(l*3 + m)*H + h][ch][j]
-    const float *wk = nullptr, *wv = nullptr;
+    const float *wq = nullptr, *wk = nullptr, *wv = nullptr;
     if (CK > 0) {
+        wq = a.tok.conv_w + (((size_t)l * 3 + 0) * dm.H + h) * D * CK;
         wk = a.tok.conv_w + (((size_t)l * 3 + 1) * dm.H + h) * D * CK;
         wv = a.tok.conv_w + (((size_t)l * 3 + 2) * dm.H + h) * D * CK;
     }
@@ -82,18 +94,21 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
             if (CK == 0) {
                 ks[i][ch] = ld_f(kp, tok_index(dm, N, l, tok, h, ch));
                 vs[i][ch] = ld_f(vp, tok_index(dm, N, l, tok, h, ch));
+                if (want_o) qs[i][ch] = ld_f(qp, tok_index(dm, N, l, tok, h, ch));
             } else {
-                float kv = 0.f, vv = 0.f;
+                float qv = 0.f, kv = 0.f, vv = 0.f;
 #pragma unroll
                 for (int j = 0; j < CK; ++j) {
                     const int32_t tj = tok - j;
                     if (tj >= seg0) {
                         kv = fmaf(wk[ch * CK + j], ld_f(kp, tok_index(dm, N, l, tj, h, ch)), kv);
                         vv = fmaf(wv[ch * CK + j], ld_f(vp, tok_index(dm, N, l, tj, h, ch)), vv);
+                        if (want_o) qv = fmaf(wq[ch * CK + j], ld_f(qp, tok_index(dm, N, l, tj, h, ch)), qv);
                     }
                 }
                 ks[i][ch] = dm.act ? silu(kv) : kv;
                 vs[i][ch] = dm.act ? silu(vv) : vv;
+                if (want_o) qs[i][ch] = dm.act ? silu(qv) : qv;
             }
             if (MODE == HYPIC_DIAG_GATE || MODE == HYPIC_KDA) as_[i][ch] = ld_f(ap, tok_index(dm, N, l, tok, h, ch));
         }
@@ -106,19 +121,20 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
         }
         __syncthreads();
         if (CK > 0) {
-            // L2-normalise each convolved k row over its D channels.
+            // L2-normalise each convolved k row (and q row) over its D channels.
             const int warp = c / 32, lane = c % 32;
-            for (int i = warp; i < nc; i += NT / 32) {
+            for (int row = warp; row < (want_o ? 2 : 1) * nc; row += NT / 32) {
+                float *xr = row < nc ? ks[row] : qs[row - nc];
                 float ss = 0.f;
-                for (int ch = lane; ch < D; ch += 32) ss = fmaf(ks[i][ch], ks[i][ch], ss);
+                for (int ch = lane; ch < D; ch += 32) ss = fmaf(xr[ch], xr[ch], ss);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 const float inv = 1.f / sqrtf(ss + kL2Eps);
-                for (int ch = lane; ch < D; ch += 32) ks[i][ch] *= inv;
+                for (int ch = lane; ch < D; ch += 32) xr[ch] *= inv;
             }
             __syncthreads();
         }
-        for (int i = 0; i < nc && c < NCOL; ++i) {
+        for (int i = 0; i < nc && active; ++i) {
             if (MODE == HYPIC_GATED_DELTA) {
                 const float al = as_[i][0], be = bs[i];
                 float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
@@ -189,21 +205,37 @@ build_rec_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Se
                 }
                 if (MODE == HYPIC_DIAG_GATE) tprod *= as_[i][c];
             }
+            if (want_o && s_col) {
+                // o_t[c_s] = sum_r q_t[r] S_t[r][c_s]
+                float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+                for (int r = 0; r < D; r += 4) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(&qs[i][r]);
+                    o0 = fmaf(q4.x, x[r + 0], o0);
+                    o1 = fmaf(q4.y, x[r + 1], o1);
+                    o2 = fmaf(q4.z, x[r + 2], o2);
+                    o3 = fmaf(q4.w, x[r + 3], o3);
+                }
+                a.o_out[tok_index(dm, N, l, b0 + t0 + i, h, DENSE_T ? c - D : c)] = (o0 + o1) + (o2 + o3);
+            }
         }
     }
 
     const size_t pair = ((size_t)l * tab.n_seg + s) * dm.H + h;
     if (c >= NCOL) return;
     if (DENSE_T) {
+        if (c < D ? !want_t : !want_s) return;
         float *dst = (c < D) ? a.T_out + pair * D * D + c : a.S_out + pair * D * D + (c - D);
 #pragma unroll
         for (int r = 0; r < D; ++r) dst[(size_t)r * D] = x[r];
     } else {
-        float *dst = a.S_out + pair * D * D + c;
+        if (want_s) {
+            float *dst = a.S_out + pair * D * D + c;
 #pragma unroll
-        for (int r = 0; r < D; ++r) dst[(size_t)r * D] = x[r];
-        if (MODE == HYPIC_DIAG_GATE) a.T_out[pair * D + c] = tprod;
-        if (MODE == HYPIC_SCALAR_DECAY && c == 0) {
+            for (int r = 0; r < D; ++r) dst[(size_t)r * D] = x[r];
+        }
+        if (MODE == HYPIC_DIAG_GATE && want_t) a.T_out[pair * D + c] = tprod;
+        if (MODE == HYPIC_SCALAR_DECAY && c == 0 && want_t) {
             for (int32_t t = 0; t < n; ++t) tprod *= gamma;
             a.T_out[pair] = tprod;
         }

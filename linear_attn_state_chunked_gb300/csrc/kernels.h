@@ -9,8 +9,9 @@ namespace hypic {
 struct BuildArgs {
     Dims dm;
     TokPtrs tok;
-    float *T_out;
-    float *S_out;
+    float *T_out;                // may be null (segment forward without the transition product)
+    float *S_out;                // may be null (segment forward)
+    float *o_out;                // per-token body outputs (segment forward), else null
     unsigned int *work_counter;  // device, zeroed by the caller's stream before launch
     int *status;                 // device status word (0 = ok)
 };

@@ -25,7 +25,8 @@ STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_INVALID_ARG", 2: "HYPIC_ERR_SHAPE", 3: "H
 # Every symbol include/hypic.h declares.
 EXPORTS = ("hypic_version", "hypic_last_error", "hypic_workspace_size",
            "hypic_workspace_status", "hypic_segment_build", "hypic_segment_build_noalloc",
-           "hypic_compose", "hypic_seam_advance", "hypic_selftest_bounded_wait")
+           "hypic_compose", "hypic_seam_advance", "hypic_selftest_bounded_wait",
+           "hypic_segment_forward")
 
 
 class HypicError(RuntimeError):
@@ -70,6 +71,9 @@ def lib():
         L.hypic_segment_build.restype = ctypes.c_int
         L.hypic_segment_build.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p, i32,
                                           fp, fp, vp, ctypes.c_size_t, vp]
+        L.hypic_segment_forward.restype = ctypes.c_int
+        L.hypic_segment_forward.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p, i32,
+                                            fp, fp, fp, vp]
         L.hypic_segment_build_noalloc.restype = ctypes.c_int
         L.hypic_segment_build_noalloc.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Tokens), i64p,
                                                   i32, fp, fp, vp]
@@ -170,6 +174,17 @@ def segment_build(desc, tok, seg_off, T_out, S_out, workspace, stream=None, n_to
     _check(lib().hypic_segment_build(ctypes.byref(d), ctypes.byref(t), offp, len(off) - 1,
                                      _p(T_out), _p(S_out), _p(workspace), ws_bytes,
                                      _stream(stream)))
+
+
+def segment_forward(desc, tok, seg_off, o_out, T_out=None, S_out=None, stream=None, n_tokens=None):
+    """Per-token outputs of every segment body from a zero state (fp32
+    [L][N][H][d_v]; seam-token rows untouched), plus the pair when T_out /
+    S_out are given."""
+    d = make_desc(desc)
+    t = make_tokens(tok, _tok_n(tok, n_tokens))
+    off, offp = _i64(seg_off)
+    _check(lib().hypic_segment_forward(ctypes.byref(d), ctypes.byref(t), offp, len(off) - 1, _p(o_out),
+                                       _p(T_out), _p(S_out), _stream(stream)))
 
 
 def segment_build_noalloc(desc, tok, seg_off, T_out, S_out, stream=None, n_tokens=None):

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(L):
     assert set(syms) == set(hypic.EXPORTS)
     for s in syms:
         assert hasattr(L, s), s
-    assert L.hypic_version() == 2
+    assert L.hypic_version() == 3
     assert b"" == L.hypic_last_error()
 
 

@@ -253,3 +253,45 @@ def test_conv_silu(d, dtype):
           % (d, et, es, res["final"], res["o"], tol))
     plain = ref.request_reference(dict(wl.desc, conv_act=0), wl.tok, wl.seg_off, wl.order, [(1, 1)])
     assert ref.rel_fro(out["S_final"][1, 1].cpu().numpy(), plain["S_final"][0]) > 100 * tol
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny_gdn", {}), ("decay_retnet", {}), ("decay_diag", {}), ("kda_tiny", {}), ("deltanet", {}),
+    ("stress_tiny", dict(d_k=128, d_v=128, in_dtype=hypic.BF16, seam_w=8, n_heads=2)),
+    ("cold_30l", dict(d_k=64, d_v=64, n_heads=2, conv_act=hypic.ACT_SILU))])
+def test_segment_forward(name, over):
+    """Per-token outputs of every segment body from a zero state against the
+    oracle's prefill of that body; seam rows untouched; the pair written
+    alongside equals the oracle's; without T and S the outputs are bitwise
+    the same (the forward alone)."""
+    kw = dict(over)
+    if name in ("stress_tiny", "cold_30l"):
+        kw.update(layers=2, lengths=EDGE_LENGTHS if name == "stress_tiny" else [9, 40, 3, 1, 25, 70, 0, 17],
+                  order=EDGE_ORDER if name == "stress_tiny" else None)
+    wl = W.make(name, device="cuda", **kw)
+    d = wl.desc
+    L, H, D, N = d["n_layers"], d["n_heads"], d["d_k"], wl.n_tokens
+    o = torch.full((L, N, H, D), float("nan"), device="cuda")
+    tshape, sshape = hypic.pair_shapes(d, wl.n_seg)
+    T = torch.empty(tshape, device="cuda")
+    S = torch.empty(sshape, device="cuda")
+    hypic.segment_forward(d, wl.tok, wl.seg_off, o, T_out=T, S_out=S)
+    o2 = torch.full_like(o, float("nan"))
+    hypic.segment_forward(d, wl.tok, wl.seg_off, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.nan_to_num(o, nan=7.0), torch.nan_to_num(o2, nan=7.0))
+    tol = tol_of(d)
+    items = _all_items(wl)
+    check_pairs(wl, {"T": T, "S": S}, items, tol)
+    refs = ref.body_output_reference(d, wl.tok, wl.seg_off, items)
+    on = o.cpu().numpy()
+    worst = 0.0
+    for (l, s, h), r in zip(items, refs):
+        lo, hi = int(wl.seg_off[s]), int(wl.seg_off[s + 1])
+        sw = min(d["seam_w"], hi - lo)
+        assert np.isnan(on[l, lo:lo + sw, h]).all()  # seam rows untouched
+        if len(r):
+            err = ref.rel_fro(on[l, lo + sw:hi, h], r)
+            worst = max(worst, err)
+            assert err <= tol, (l, s, h, err)
+    print("\nsegment forward %s: worst o %.2e (tol %.0e)" % (name, worst, tol))
