@@ -175,3 +175,36 @@ def test_selftest_rejects_bad_arguments(L):
     assert L.hypic_selftest_bounded_wait(FAKE, 0, None) == 2
     assert L.hypic_selftest_bounded_wait(FAKE, (1 << 34) + 1, None) == 2
     assert b"max_cycles" in L.hypic_last_error()
+
+
+def _forward(desc, tok=None, seg_off=(0, 10, 20), n_tokens=20, o=FAKE, T=None, S=None):
+    d = hypic.make_desc(desc)
+    t = hypic.make_tokens(tok if tok is not None else _tok(), n_tokens)
+    off = np.asarray(seg_off, dtype=np.int64)
+    return hypic.lib().hypic_segment_forward(
+        ctypes.byref(d), ctypes.byref(t), off.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        len(off) - 1, o, T, S, None)
+
+
+BAD_FORWARD = [
+    ("o_out null", dict(desc=_desc(), o=None), 1),
+    ("o_out misaligned", dict(desc=_desc(), o=FAKE + 4), 1),
+    ("q null", dict(desc=_desc(), tok=_tok(q=None)), 1),
+    ("T misaligned", dict(desc=_desc(), T=FAKE + 8), 1),
+    ("S misaligned", dict(desc=_desc(), S=FAKE + 8), 1),
+    ("mode", dict(desc=_desc(mode=4)), 1),
+    ("offsets past N", dict(desc=_desc(), seg_off=(0, 10, 21)), 2),
+]
+
+
+@pytest.mark.parametrize("what,kw,code", BAD_FORWARD, ids=[b[0] for b in BAD_FORWARD])
+def test_forward_rejects(L, what, kw, code):
+    """The segment forward validates on the host like the build (q and the
+    output are required, T and S optional but aligned) and launches nothing
+    on error."""
+    assert _forward(**kw) == code
+    assert L.hypic_last_error() != b""
+
+
+def test_forward_empty_request_is_ok(L):
+    assert _forward(desc=_desc(), seg_off=(0,), n_tokens=0) == 0
