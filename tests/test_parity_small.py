@@ -295,3 +295,32 @@ def test_segment_forward(name, over):
             worst = max(worst, err)
             assert err <= tol, (l, s, h, err)
     print("\nsegment forward %s: worst o %.2e (tol %.0e)" % (name, worst, tol))
+
+
+@pytest.mark.parametrize("d,dtype", [(128, hypic.BF16), (32, hypic.F32)])
+def test_maximum_segment_count(d, dtype):
+    """The request table at its limit: as many segments as the library takes
+    (0 to 40 tokens each: empty ones, ones shorter than the seam or the conv
+    history) and a request order of the same length with repeats; every pair
+    of two sampled heads' items, the two chains over the whole order (every
+    prefix state, seam output and the final state), and all seams in
+    parallel from the prefix states, against the oracle."""
+    rng = np.random.default_rng(99)
+    n = hypic.MAX_SEGMENTS
+    lengths = rng.integers(0, 41, size=n)
+    order = rng.integers(0, n, size=n).astype(np.int32)
+    wl = W.make("cold_30l", device="cuda", layers=1, lengths=lengths, order=order, n_heads=2,
+                d_k=d, d_v=d, in_dtype=dtype)
+    out = run_pipeline(wl)
+    tol = tol_of(wl.desc)
+    pick = sorted(set([int(np.argmax(lengths)), int(np.argmin(lengths)), 0, n - 1] +
+                      [int(x) for x in rng.integers(0, n, size=12)]))
+    check_pairs(wl, out, [(0, s, h) for s in pick for h in range(2)], tol)
+    res = check_request(wl, out, [(0, 0), (0, 1)], tol)
+    o2 = torch.full_like(out["o"], float("nan"))
+    hypic.seam_advance(wl.desc, wl.tok, wl.seg_off, wl.order, out["S_prefix"], o2)
+    torch.cuda.synchronize()
+    num = (o2.double() - out["o"].double()).pow(2).sum(dim=(2, 4)).sqrt()
+    den = out["o"].double().pow(2).sum(dim=(2, 4)).sqrt()
+    assert (torch.where(den > 0, num / den.clamp_min(1e-300), num) <= tol).all()
+    print("\nmax segments d=%d: S_final %.2e  S_prefix %.2e  seam o %.2e" % (d, res["final"], res["prefix"], res["o"]))
