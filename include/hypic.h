@@ -26,7 +26,7 @@
  * are re-run under the composed prefix state, advancing it and emitting their
  * per-token outputs.
  *
- * Three calls form the hot path:
+ * Three calls form the hot path; a fourth serves a segment's first prefill:
  *   hypic_segment_build   -- the cached pair of every segment body, all
  *                            segments x layers x heads in one launch (the
  *                            single-GPU stand-in for "段并行"'s scatter stage,
@@ -35,6 +35,7 @@
  *                            with each entry's seam re-run in the same pass;
  *   hypic_seam_advance    -- the seams alone, all entries in parallel, from
  *                            given prefix states;
+ * and
  *   hypic_segment_forward -- the segment bodies' per-token outputs from a zero
  *                            state (the segment's first prefill), with or
  *                            without the pair.
