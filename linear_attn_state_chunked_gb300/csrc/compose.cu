@@ -371,7 +371,9 @@ cudaError_t launch_compose(const ComposeArgs &a, const SegTable &tab, cudaStream
     // Gated delta at d = 128 with bf16 inputs composes on the tensor cores
     // (tf32 T_C S, 2e-3 class); fp32-input requests (1e-5 class) and the other
     // modes and widths use the CUDA-core kernel below.
-    if (compose_tc_supported(a.dm)) return launch_compose_tc(a, tab, st);
+    // (its TMA row coordinate, pair x 128, must fit 31 bits)
+    const long long pair_rows = (long long)a.dm.L * (tab.n_seg > 0 ? tab.n_seg : 1) * a.dm.H * a.dm.D;
+    if (compose_tc_supported(a.dm) && pair_rows < (1LL << 31)) return launch_compose_tc(a, tab, st);
     return a.dm.dtype == HYPIC_BF16 ? launch_compose_m<__nv_bfloat16>(a, tab, st)
                                     : launch_compose_m<float>(a, tab, st);
 }
