@@ -37,6 +37,9 @@ Segment lengths, orders and seeds:
                 request order = segment order (a cold prompt)
 * stress_tiny / stress_gdn  the tiny_gdn / gdn_bf16 shapes with the slow gate
                 (seeds 5 and 6), so that T_C stays far from zero.
+* stress_cold   the cold_30l shape (200 lognormal segments up to 4096 tokens,
+                conv taps 4, w=8) with the slow gate, 2 layers, seed 10: the
+                longest bodies under a gate that keeps T_C large.
 * deltanet      plain DeltaNet (gated delta with alpha = 1): 1 layer, 2 heads,
                 d=32, fp32, 6 x 50 tokens, seed 9, w=8
 * kda_tiny      KDA, 1 layer, 2 heads, d=16, fp32, 4 x 64 tokens, seed 7, w=0
@@ -102,7 +105,7 @@ def segment_lengths(name):
         return np.full(4, 64, np.int64)
     if name == "kda_bf16":
         return np.random.default_rng(8).integers(40, 301, size=12).astype(np.int64)
-    if name == "cold_30l":
+    if name in ("cold_30l", "stress_cold"):
         raw = np.random.default_rng(4).lognormal(np.log(512.0), 0.8, size=200)
         raw = np.clip(np.rint(raw), 64, 4096)
         return _rescale(raw, 100_000, 64, 4096)
@@ -119,6 +122,7 @@ _SPECS = {
     "cold_30l":     (GATED_DELTA, 30, 32, 128, BF16, 4,  8, 4, 1.0),
     "stress_tiny":  (GATED_DELTA,  1,  1, 16, F32,  5,   0, 0, 64.0),
     "stress_gdn":   (GATED_DELTA,  1, 32, 128, BF16, 6,  8, 0, 64.0),
+    "stress_cold":  (GATED_DELTA,  2, 32, 128, BF16, 10, 8, 4, 64.0),
     "deltanet":     (GATED_DELTA,  1,  2, 32, F32,  9,   8, 0, 0.0),
     "kda_tiny":     (KDA,          1,  2, 16, F32,  7,   0, 0, 16.0),
     "kda_bf16":     (KDA,          1,  4, 64, BF16, 8,   8, 4, 16.0),

@@ -81,6 +81,52 @@ def pair_reference(desc, tok, seg_off, items):
     return np.stack(Ts), np.stack(Ss)
 
 
+def layer_arrays(tok, l):
+    """One layer of the packed token tensors as float32 numpy arrays
+    (q, k, v [N, H, d]; alpha, beta as laid out; conv_w [3, H, d, K]).
+    Gathering only: the values are the bf16 / fp32 inputs, widened."""
+    out = {}
+    for key in ("q", "k", "v", "alpha", "beta", "conv_w"):
+        x = tok.get(key)
+        out[key] = None if x is None else x[l].detach().float().cpu().numpy()
+    return out
+
+
+def segment_pairs(desc, arrs, seg_off, s):
+    """Dense fp64 (T, S) of segment s's body for every head of one layer, in
+    one call of the primitive (the heads are independent chains).
+
+    arrs: one layer from :func:`layer_arrays`.  The body is the segment minus
+    its first min(w, len) seam tokens, taken as the segment's own first
+    prefill (conv history from the segment itself).
+    Returns T [H, dk, dk], S [H, dk, dv].
+    """
+    mode, w, ck = desc["mode"], desc["seam_w"], desc.get("conv_k", 0)
+    act = silu if desc.get("conv_act", 0) == 1 else (lambda x: x)
+    lo, hi = int(seg_off[s]), int(seg_off[s + 1])
+    H = arrs["k"].shape[1]
+    sw = seam_len(seg_off, s, w)
+    ks, vs, as_, bs = [], [], [], []
+    for h in range(H):
+        k = np.asarray(arrs["k"][lo:hi, h, :], dtype=np.float64)
+        v = np.asarray(arrs["v"][lo:hi, h, :], dtype=np.float64)
+        if ck:
+            wts = np.asarray(arrs["conv_w"][:, h, :, :], dtype=np.float64)
+            k = l2_normalize(act(causal_conv(k, wts[1])))
+            v = act(causal_conv(v, wts[2]))
+        if mode == SCALAR_DECAY:
+            a = np.full(hi - lo, float(arrs["alpha"][h]))
+        else:
+            a = np.asarray(arrs["alpha"][lo:hi, h], dtype=np.float64)
+        ks.append(k[sw:])
+        vs.append(v[sw:])
+        as_.append(a[sw:])
+        if mode in (GATED_DELTA, KDA):
+            bs.append(np.asarray(arrs["beta"][lo:hi, h], dtype=np.float64)[sw:])
+    return pair(mode, np.stack(ks), np.stack(vs), np.stack(as_),
+                np.stack(bs) if bs else None)
+
+
 def body_output_reference(desc, tok, seg_off, items):
     """Per-token outputs of the body of segment s from a zero state, for each
     (l, s, h) in items: the segment's own first prefill (conv history from
