@@ -4,37 +4,54 @@
 // Math (derived from the recurrence S_t = alpha_t (I - beta_t k_t k_t^T)
 // S_{t-1} + beta_t k_t v_t^T and the pair (T_C, S(C|0)) of section "线性层"
 // of the article “小红书联合北大、上交提出 HYPIC：混合注意力大模型首 Token
-// 延迟降低 3.25 倍，实现位置无关缓存”).  Within a chunk of C = 64 tokens let g_t = sum_{s<=t} log alpha_s,
-// Gamma_t = exp(g_t).  Writing u_t = v_t - alpha_t S_{t-1}^T k_t, one finds
-//   S_C = Gamma_C S_0 + K^T D U,   U = (I + L)^{-1} (V - diag(Gamma) K S_0),
+// 延迟降低 3.25 倍，实现位置无关缓存”).  Within a chunk of C = 64 tokens let
+// g_t = sum_{s<=t} log alpha_s, Gamma_t = exp(g_t), Gamma_C = Gamma_{C-1},
 //   L_tj = beta_j exp(g_t - g_j) k_t.k_j  (j < t),  D = diag(beta_j exp(g_C - g_j)).
-// The same map advances T (with V replaced by 0), so X = [T | S] (d_k x 2d)
-// is carried as one matrix.  Kept transposed in tensor memory (Xt = X^T,
-// two 128-lane halves x 128 columns), one chunk is
-//   Pt = Xt K^T                       (tf32 MMA, A = Xt from tensor memory)
-//   Rt = [0 | V]^T - Pt diag(Gamma)   (CUDA cores, written back over Pt)
-//   Xt = Gamma_C Xt + Rt U~           (tf32 MMA, A = Rt from tensor memory)
-//   U~^T = K^T D (I + L)^{-1}         (Gram K K^T and U~ on the tensor core,
-//                                      the 64 x 64 unit lower inverse by
-//                                      doubling from 8 x 8 blocks: forward
-//                                      substitution on CUDA cores, block
-//                                      products on warp-level MMAs)
-// Operands written by threads are rounded to tf32 (the tensor core
-// truncates).
+// Writing u_t = v_t - alpha_t S_{t-1}^T k_t one finds that X = [T | S]
+// (d_k x 2d, T from I and S from 0) advances per chunk as
+//   X <- Gamma_C X + U~^T R,   R = [0 | V] - diag(Gamma) K X,
+//   U~ = (I + L)^{-T} D K      (C x d_k).
+// U~ solves the unit upper triangular system (I + L)^T U~ = D K.  In blocks
+// of 16 tokens, with M_ii = (I + L_ii)^{-1} the inverse of a diagonal block,
+//   U~_i = (D_i M_ii)^T K_i - sum_{j > i} (L_ji M_ii)^T U~_j ,  i = 3, 2, 1, 0,
+// and the columns (channels) of U~ are independent, so each warp of the
+// solve group back-substitutes its own 32 channels with warp-level MMAs and no
+// synchronisation with the others.
 //
-// Warp roles (one CTA per SM, persistent over work items):
-//   warp 13     TMA producer: raw bf16 K/V rows (+ conv history) and gates of
-//               each chunk into a 3-stage ring;
-//   warp 12     one thread issues every tcgen05.mma: chunk n's Gram, Pt, U~
-//               and Xt updates, each as soon as its inputs are ready;
-//   warps 4-11  preparation of chunk n+1 while chunk n runs (two warps per
-//               tensor-memory lane quadrant): gates, conv + normalisation,
-//               tf32 K, L, the inverse, U~;
-//   warps 0-3   epilogue of chunk n: Rt and the Gamma_C rescale of Xt, both
-//               halves, and the emission of each finished pair.
-// Work items (segment body, layer, head) arrive longest body first; CTA b
-// takes items b, b + grid, ... -- the greedy LPT order of that article's "段并行"
-// section as a single-GPU stand-in for its scatter workers.
+// Kernel form: X is kept transposed in tensor memory (Xt = X^T, two 128-lane
+// halves: Xt_T = T^T and Xt_S = S^T).  Per chunk
+//   Pt   = Xt K^T                         tcgen05 tf32, A = Xt from tensor memory
+//   Rt_S = V^T - Pt_S diag(Gamma),   Xt_S <- Gamma_C Xt_S      (CUDA cores)
+//   Rt_T = -Pt_T diag(Gamma / Gamma_C)    (Xt_T was multiplied by Gamma_C when
+//                                          the previous chunk finished)
+//   Xt  += Rt U~                          tcgen05 tf32, A = Rt from tensor memory
+// The tensor core reads an fp32 A operand truncated to tf32.  For the T half
+// that truncation would bias the product chunk after chunk, so the part it
+// drops, Xt_T - trunc(Xt_T), is kept beside Xt_T in bf16 and multiplied by K
+// in bf16 into the same accumulator: Pt_T is then exact to ~2^-19.
+// Operands written by threads are rounded to nearest tf32.
+//
+// Warp roles (one CTA per SM, persistent over work items (segment body,
+// layer, head); every role walks the same items and chunks in order):
+//   warp 17      TMA producer: lane 0 streams raw bf16 K rows (+ conv history)
+//                into a 3-stage ring, lane 1 raw V rows into a 2-stage ring;
+//   warp 16      one thread issues every tcgen05.mma of chunk n: Pt_S, Pt_T
+//                (+ its bf16 correction), the Gram of chunk n+1, the Xt_T and
+//                Xt_S updates, each behind a bounded mbarrier wait;
+//   warps 8-11   conversion: causal conv + L2 normalisation of K into tf32
+//                (operand of the Gram, Pt and the solve) and into bf16 (in
+//                place in the raw ring stage, operand of the correction), and
+//                the chunk's gates;
+//   warps 12-15  solve: L from the Gram, the four 16 x 16 diagonal inverses,
+//                the (L_ji M_ii)^T blocks, and U~ by block back substitution
+//                into the 128-byte-swizzled B operand of the Xt update;
+//   warps 0-3    T epilogue: Rt_T, then (after the update) Xt_T scaled by the
+//                next chunk's Gamma_C and its bf16 low part; emits T;
+//   warps 4-7    S epilogue: Rt_S (conv of V in registers) and the Gamma_C
+//                rescale of Xt_S; emits S.
+// Work items arrive longest body first; CTA b takes items b, b + grid, ... --
+// the greedy LPT order of that article's "段并行" section as a single-GPU
+// stand-in for its scatter workers.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -48,48 +65,52 @@ namespace {
 
 constexpr int D = 128;   // head width
 constexpr int C = 64;    // chunk length
-constexpr int RS = 2;    // raw-input ring stages
+constexpr int NB = 16;   // block of the back substitution
+constexpr int RK = 3;    // raw-K ring stages
+constexpr int RV = 2;    // raw-V ring stages
+constexpr int RG = 4;    // gate ring stages
 constexpr int HMAX = 3;  // conv history rows kept per chunk (conv_k <= 4)
-constexpr int ROWS = C + HMAX;
-constexpr int NP = 256;  // preparation threads (warps 4-11, two per tensor-memory lane quadrant)
-constexpr int NT = 448;  // 14 warps
-constexpr int WARP_MMA = 12, WARP_TMA = 13;
-constexpr int BAR_EPI = 1, BAR_PREP = 2;
+constexpr int NT = 576;  // 18 warps
+constexpr int WARP_MMA = 16, WARP_TMA = 17;
+constexpr int BAR_TEPI = 1, BAR_SEPI = 2, BAR_CONV = 3, BAR_SOLVE = 4;
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds
+// Largest log-decay span g_0 - g_{C-1} of a chunk for which Xt_T is
+// pre-multiplied by Gamma_C (the factors Gamma_t / Gamma_C stay below e^80).
+constexpr float kSpan = 80.f;
 
 // tensor-memory columns
-constexpr uint32_t TM_XT = 0;    // Xt, T half: 128 lanes x 128
-constexpr uint32_t TM_XS = 128;  // Xt, S half
-constexpr uint32_t TM_PT = 256;  // Pt then Rt, T half: 128 x 64
-constexpr uint32_t TM_PS = 320;  // Pt then Rt, S half
-constexpr uint32_t TM_G = 384;   // Gram (M = 64 layout), then K^T (A of U~): 64 columns
-constexpr uint32_t TM_U = 448;   // U~^T: 128 x 64
+constexpr uint32_t TM_XT = 0;     // Xt_T: 128 lanes x 128
+constexpr uint32_t TM_XS = 128;   // Xt_S
+constexpr uint32_t TM_PT = 256;   // Pt_T, then Rt_T: 128 x 64
+constexpr uint32_t TM_PS = 320;   // Pt_S, then Rt_S
+constexpr uint32_t TM_G = 384;    // Gram (M = 64 layout): 64 columns
+constexpr uint32_t TM_XLO = 448;  // Xt_T - trunc(Xt_T) in bf16 pairs: 64 columns
 constexpr uint32_t TM_COLS = 512;
 
-// raw stage: K rows, V rows (bf16 [ROWS][128]), alpha[64], beta[64] (fp32)
-constexpr uint32_t ST_K = 0;
-constexpr uint32_t ST_V = ROWS * D * 2;
-constexpr uint32_t ST_G = 2 * ROWS * D * 2;  // the chunk's Gates, written by the producer warp
-constexpr uint32_t ST_BYTES = ST_G + 5 * C * 4;
-
 // shared memory (byte offsets from a 1024-aligned base)
-constexpr uint32_t SM_RAW = 0;
-constexpr uint32_t SM_K32 = (RS * ST_BYTES + 1023) / 1024 * 1024;  // K [64][128] tf32, sw128
-constexpr uint32_t SM_UT = SM_K32 + 32768;     // U~^T [128][64] tf32, sw128 (B of the Xt update)
-constexpr uint32_t SM_MT = SM_UT + 32768;      // (D M)^T [64][64] tf32, sw128 (B of U~)
-constexpr int LP = C + 4;                      // row pitch of L and M: 16-byte rows for ldmatrix
-constexpr uint32_t SM_L = SM_MT + 16384;       // L [64][68], tf32 values
-constexpr uint32_t SM_M = SM_L + C * LP * 4;   // M = (I + L)^-1 [64][68], tf32 values
-constexpr int QP = 36;                         // row pitch of the per-warp Q^T scratch
-constexpr uint32_t SM_Q = SM_M + C * LP * 4;   // per-warp Q^T [8][36] for the inverse
-constexpr uint32_t SM_WK = SM_Q + 8 * 8 * QP * 4;  // K conv weights of the current item [4 lags][128]
+constexpr uint32_t KR_STAGE = 17408;  // raw K rows [C + 3][128] bf16, then K in bf16, sw128
+constexpr uint32_t VR_STAGE = 17152;  // raw V rows [C + 3][128] bf16
+constexpr uint32_t G_STAGE = 2176;    // Gates
+constexpr int LP = C + 4;             // row pitch of L (16-byte rows for ldmatrix)
+constexpr int BP = 20;                // row pitch of the 16 x 16 blocks
+constexpr uint32_t BLK = NB * BP * 4; // bytes of one 16 x 16 block
+constexpr uint32_t SM_KR = 0;
+constexpr uint32_t SM_VR = SM_KR + RK * KR_STAGE;
+constexpr uint32_t SM_GATE = SM_VR + RV * VR_STAGE;
+constexpr uint32_t SM_K32 = (SM_GATE + RG * G_STAGE + 1023) / 1024 * 1024;  // 2 x K [64][128] tf32, sw128
+constexpr uint32_t SM_UT = SM_K32 + 2 * 32768;  // U~^T [128][64] tf32, sw128 (B of the Xt update)
+constexpr uint32_t SM_L = SM_UT + 32768;        // L [64][LP]; upper blocks hold -(L_ji M_ii)^T
+constexpr uint32_t SM_A1 = SM_L + C * LP * 4;   // 4 x (D_i M_ii)^T [16][BP]
+constexpr uint32_t SM_MT = SM_A1 + 4 * BLK;     // 4 x M_ii^T [16][BP]
+constexpr uint32_t SM_WK = SM_MT + 4 * BLK;     // K conv weights of the current item [4 lags][128]
 constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
-constexpr uint32_t SM_MISC = SM_BAR + 32 * 8;
+constexpr uint32_t SM_MISC = SM_BAR + 40 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
-static_assert(SM_K32 % 1024 == 0 && SM_UT % 1024 == 0 && SM_MT % 1024 == 0, "tile alignment");
-static_assert(SM_L % 16 == 0 && SM_M % 16 == 0 && SM_Q % 16 == 0, "ldmatrix row alignment");
-static_assert(ST_BYTES % 128 == 0 && ST_V % 128 == 0, "TMA destination alignment");
+static_assert(KR_STAGE % 1024 == 0 && SM_K32 % 1024 == 0 && SM_UT % 1024 == 0, "tile alignment");
+static_assert((C + HMAX) * D * 2 <= (int)KR_STAGE && (C + HMAX) * D * 2 <= (int)VR_STAGE, "ring stage size");
+static_assert(SM_VR % 128 == 0 && VR_STAGE % 128 == 0, "TMA destination alignment");
+static_assert(SM_L % 16 == 0 && SM_A1 % 16 == 0 && SM_MT % 16 == 0, "ldmatrix row alignment");
 static_assert(SMEM_DYN <= 232448, "shared memory budget");
 
 struct Gates {
@@ -98,25 +119,38 @@ struct Gates {
     float dc[C];  // beta_j exp(g_C - g_j)
     float b[C];   // beta
     float fb[C];  // beta_j exp(g_m - g_j), g_m = (g_0 + g_C) / 2
+    float nrc[C]; // -exp(g_t - g_C) (used when the chunk is pre-scaled)
+    float neg[C]; // -exp(g_t)
+    int safe;     // g_0 - g_C <= kSpan
 };
+static_assert(sizeof(Gates) <= G_STAGE, "gate stage size");
 
 // mbarriers
 enum {
-    B_FULL = 0,          // [RS] raw stage loaded (TMA bytes + producer arrive)
-    B_EMPTY = RS,        // [RS] raw stage released (prep + epilogue)
-    B_KREADY = 2 * RS,   // K32 written                      prep -> mma
-    B_GRAM,              // Gram done                        mma -> prep
-    B_KTREADY,           // K^T in TMEM and (D M)^T written   prep -> mma
-    B_UDONE,             // U~ done                          mma -> prep
-    B_UTREADY,           // U~^T copied to smem               prep -> mma
-    B_PTDONE,            // Pt (T half) done                 mma -> epilogue
-    B_PSDONE,            // Pt (S half) done                 mma -> epilogue, prep (K32 free)
-    B_RTREADY,           // Rt (T half) written, Xt_T scaled  epilogue -> mma
-    B_RSREADY,           // Rt (S half) written, Xt_S scaled  epilogue -> mma
-    B_DSDONE,            // both Xt updates done              mma -> epilogue, prep (U~^T free)
-    B_XREADY,            // Xt initialised for a new item     epilogue -> mma
+    B_KRF = 0,            // [RK] raw K stage loaded                    TMA -> conversion
+    B_KRE = B_KRF + RK,   // [RK] stage free (bf16 K consumed)          MMA -> TMA
+    B_VRF = B_KRE + RK,   // [RV] raw V stage loaded                    TMA -> S epilogue
+    B_VRE = B_VRF + RV,   // [RV] stage free                            S epilogue -> TMA
+    B_GF = B_VRE + RV,    // [RG] gates written                         conversion -> solve, epilogues
+    B_GE = B_GF + RG,     // [RG] gates consumed (3 arrivals)           solve, epilogues -> conversion
+    B_KRDY = B_GE + RG,   // [2] K tf32 + bf16 written                  conversion -> MMA
+    B_K32E = B_KRDY + 2,  // [2] K tf32 free (2 arrivals)               MMA, solve -> conversion
+    B_GRAMF = B_K32E + 2, // Gram done                                  MMA -> solve
+    B_GRAME,              // Gram read into L                           solve -> MMA
+    B_UTF,                // U~^T written                               solve -> MMA
+    B_UTE,                // U~^T consumed (Xt_S update done)           MMA -> solve
+    B_PTF,                // Pt_T done                                  MMA -> T epilogue
+    B_RTF,                // Rt_T written                               T epilogue -> MMA
+    B_PSF,                // Pt_S done                                  MMA -> S epilogue
+    B_RSF,                // Rt_S written, Xt_S rescaled                S epilogue -> MMA
+    B_XTD,                // Xt_T update done                           MMA -> T epilogue
+    B_XTR,                // Xt_T (+ low part) ready for Pt_T           T epilogue -> MMA
+    B_XSD,                // Xt_S update done                           MMA -> S epilogue
+    B_XSI,                // Xt_S zeroed for a new item                 S epilogue -> MMA
+    B_FIN,                // every MMA of the CTA completed             MMA -> MMA
     B_COUNT
 };
+static_assert(B_COUNT <= 40, "barrier space");
 
 struct Item {
     int s, l, h;
@@ -142,15 +176,16 @@ __device__ __forceinline__ Item decode_item(int item, const Dims &dm, const SegT
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ void unpack8(const uint4 &u, float *x)
-{
-    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
-    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
-}
 __device__ __forceinline__ float bf16_at(const uint8_t *tile, int row, int col)
 {
     const uint16_t u = *reinterpret_cast<const uint16_t *>(tile + (row * D + col) * 2);
     return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+// Two floats as bf16 (round to nearest even), the first in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&p);
 }
 
 // Bounded wait by one thread; any failure (or another role's) aborts the CTA.
@@ -181,165 +216,19 @@ __device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr)
                  : "=r"(r[0]), "=r"(r[1]) : "r"(addr) : "memory");
 }
 
-// Row-major fp32 matrix with pitch LP floats: A fragment of the 16 x 8 tile at (r0, k0).
-__device__ __forceinline__ void frag_a(uint32_t (&a)[4], uint32_t base, int r0, int k0, int lane)
+// A fragment of the 16 x 8 tile at (r0, k0) of a row-major fp32 matrix with
+// the given row pitch (floats).
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], uint32_t base, int pitch, int r0, int k0, int lane)
 {
     const int row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8, col = k0 + (lane >> 4) * 4;
-    ldsm_x4(a, base + (row * LP + col) * 4);
+    ldsm_x4(a, base + (row * pitch + col) * 4);
 }
 
-// B fragment (k0 .. k0+8) x (n0 .. n0+8) of a matrix stored transposed in the
-// 64 x 64 sw128 tile at base (row n holds column n of the matrix).
-__device__ __forceinline__ void frag_b_sw(uint32_t (&b)[2], uint32_t base, int k0, int n0, int lane)
+// B fragment (k0 .. k0+8) x (n0 .. n0+8) of a matrix stored transposed,
+// row-major with the given pitch (row n holds column n of the matrix).
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], uint32_t base, int pitch, int k0, int n0, int lane)
 {
-    ldsm_x2(b, base + tc::sw128_f32(n0 + (lane & 7), k0 + ((lane >> 3) & 1) * 4, C));
-}
-
-// B fragment of the per-warp Q^T scratch (pitch QP): rows k0 .. k0+8 of Q.
-__device__ __forceinline__ void frag_b_q(uint32_t (&b)[2], uint32_t qt, int k0, int lane)
-{
-    ldsm_x2(b, qt + ((lane & 7) * QP + k0 + ((lane >> 3) & 1) * 4) * 4);
-}
-
-// Store a 16 x 8 accumulator fragment (rows r0.., columns c0..) as tf32 values,
-// negated, into M (row-major) and M^T (sw128 tile).
-__device__ __forceinline__ void store_m(float *Ms, uint8_t *Mt, int r0, int c0, const float (&c)[4], int lane)
-{
-    const int g = lane >> 2, t4 = lane & 3;
-    const float v0 = tc::round_tf32(-c[0]), v1 = tc::round_tf32(-c[1]);
-    const float v2 = tc::round_tf32(-c[2]), v3 = tc::round_tf32(-c[3]);
-    *reinterpret_cast<float2 *>(Ms + (r0 + g) * LP + c0 + 2 * t4) = make_float2(v0, v1);
-    *reinterpret_cast<float2 *>(Ms + (r0 + g + 8) * LP + c0 + 2 * t4) = make_float2(v2, v3);
-    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4, r0 + g, C)) = v0;
-    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4 + 1, r0 + g, C)) = v1;
-    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4, r0 + g + 8, C)) = v2;
-    *reinterpret_cast<float *>(Mt + tc::sw128_f32(c0 + 2 * t4 + 1, r0 + g + 8, C)) = v3;
-}
-
-// Store a 16 x 8 accumulator fragment as tf32 values into rows r0.. of the Q^T scratch.
-__device__ __forceinline__ void store_q(float *Qt, int r0, const float (&c)[4], int lane)
-{
-    const int g = lane >> 2, t4 = lane & 3;
-    Qt[(2 * t4) * QP + r0 + g] = tc::round_tf32(c[0]);
-    Qt[(2 * t4 + 1) * QP + r0 + g] = tc::round_tf32(c[1]);
-    Qt[(2 * t4) * QP + r0 + g + 8] = tc::round_tf32(c[2]);
-    Qt[(2 * t4 + 1) * QP + r0 + g + 8] = tc::round_tf32(c[3]);
-}
-
-// M = (I + L)^{-1} for the unit lower triangular 64 x 64 matrix I + L, by
-// doubling: with I + L = [[A, 0], [B, E]] in equal halves,
-//   M = [[A^{-1}, 0], [-E^{-1} B A^{-1}, E^{-1}]],
-// applied from 8 x 8 diagonal blocks (forward substitution) up to 16, 32
-// and 64.  The 8 -> 16 step runs on CUDA cores inside each of four warps;
-// the 16 -> 32 and 32 -> 64 products on the warp-level tensor-core MMA
-// (tf32 operands, fp32 accumulation).  L holds tf32 values; M is written as
-// tf32 values twice, row-major (Ms, A operands) and transposed into the
-// sw128 tile Mt (B operands, and later (D M)^T in place).  Only the lower
-// blocks are written: the strictly upper 8 x 8 blocks stay zero from the
-// start of the kernel.  pt = 0 .. NP-1.
-__device__ __noinline__ void unit_lower_inverse(const float *Ls, float *Ms, uint8_t *Mt, float *Qs, int pt)
-{
-    const int wq = pt >> 5, ln = pt & 31;
-    float *Qt = Qs + wq * 8 * QP;  // this warp's Q^T
-    const uint32_t sL = tc::smem_u32(Ls), sM = tc::smem_u32(Ms), sMt = tc::smem_u32(Mt), sQ = tc::smem_u32(Qt);
-    if (wq < 4) {
-        // 16 x 16 diagonal block wq: its two 8 x 8 diagonal blocks (one column per lane) ...
-        const int B = 16 * wq;
-        if (ln < 16) {
-            const int base = B + 8 * (ln >> 3), cc = ln & 7;
-            float x[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                float acc = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-                for (int j = 0; j < r; ++j) acc = fmaf(-Ls[(base + r) * LP + base + j], x[j], acc);
-                x[r] = (r < cc) ? 0.f : tc::round_tf32(acc);
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) Ms[(base + r) * LP + base + cc] = x[r];
-            *reinterpret_cast<float4 *>(Mt + tc::sw128_f32(base + cc, base, C)) = make_float4(x[0], x[1], x[2], x[3]);
-            *reinterpret_cast<float4 *>(Mt + tc::sw128_f32(base + cc, base + 4, C)) = make_float4(x[4], x[5], x[6], x[7]);
-        }
-        __syncwarp();
-        // ... then its lower-left 8 x 8: -M_bb (L_ba M_aa), two entries per lane
-        float q[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int i = (ln >> 3) + 4 * h, j = ln & 7;
-            float acc = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc = fmaf(Ls[(B + 8 + i) * LP + B + k], Ms[(B + k) * LP + B + j], acc);
-            q[h] = acc;
-        }
-        Qt[ln] = q[0];
-        Qt[ln + 32] = q[1];
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int i = (ln >> 3) + 4 * h, j = ln & 7;
-            float acc = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc = fmaf(Ms[(B + 8 + i) * LP + B + 8 + k], Qt[k * 8 + j], acc);
-            const float v = tc::round_tf32(-acc);
-            Ms[(B + 8 + i) * LP + B + j] = v;
-            *reinterpret_cast<float *>(Mt + tc::sw128_f32(B + j, B + 8 + i, C)) = v;
-        }
-    }
-    tc::bar_sync(BAR_PREP, NP);
-    if (wq < 4) {
-        // 16 -> 32: M_10 and M_32 (16 x 16), one 8-column half per warp
-        const int bj = 2 * (wq >> 1), bi = bj + 1, c0 = 16 * bj + 8 * (wq & 1);
-        float q[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t a[4], b[2];
-        // M_jj[k][c0..] vanishes for the first k-step when c0 is the upper half
-        if ((wq & 1) == 0) {
-            frag_a(a, sL, 16 * bi, 16 * bj, ln);
-            frag_b_sw(b, sMt, 16 * bj, c0, ln);
-            mma16x8x8(q, a, b);
-        }
-        frag_a(a, sL, 16 * bi, 16 * bj + 8, ln);
-        frag_b_sw(b, sMt, 16 * bj + 8, c0, ln);
-        mma16x8x8(q, a, b);
-        store_q(Qt, 0, q, ln);
-        __syncwarp();
-        float r[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            frag_a(a, sM, 16 * bi, 16 * bi + 8 * ks, ln);
-            frag_b_q(b, sQ, 8 * ks, ln);
-            mma16x8x8(r, a, b);
-        }
-        store_m(Ms, Mt, 16 * bi, c0, r, ln);
-    }
-    tc::bar_sync(BAR_PREP, NP);
-    {
-        // 32 -> 64: rows 32..63 x columns 0..31; warp wq takes row block
-        // 32 + 16 rb and the 8-column strip cs.  Q = L[32.., 0..32) M[0..32, strip]
-        // (M[k][strip] = 0 for k < 8 cs), then -M[rows, 32..64) Q.
-        const int rb = wq >> 2, cs = wq & 3, c0 = 8 * cs;
-        float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t a[4], b[2];
-        for (int ks = cs; ks < 4; ++ks) {
-            frag_b_sw(b, sMt, 8 * ks, c0, ln);
-            frag_a(a, sL, 32, 8 * ks, ln);
-            mma16x8x8(q0, a, b);
-            if (rb) {
-                frag_a(a, sL, 48, 8 * ks, ln);
-                mma16x8x8(q1, a, b);
-            }
-        }
-        store_q(Qt, 0, q0, ln);
-        if (rb) store_q(Qt, 16, q1, ln);
-        __syncwarp();
-        float r[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int ks = 0; ks < 2 * (rb + 1); ++ks) {
-            frag_a(a, sM, 32 + 16 * rb, 32 + 8 * ks, ln);
-            frag_b_q(b, sQ, 8 * ks, ln);
-            mma16x8x8(r, a, b);
-        }
-        store_m(Ms, Mt, 32 + 16 * rb, c0, r, ln);
-    }
-    tc::bar_sync(BAR_PREP, NP);
+    ldsm_x2(b, base + ((n0 + (lane & 7)) * pitch + k0 + ((lane >> 3) & 1) * 4) * 4);
 }
 
 // Cursor over this CTA's chunks (non-empty items only), used by the MMA issuer.
@@ -349,7 +238,7 @@ struct Cursor {
     int nch;
     int n;     // CTA-wide chunk number
     int xi;    // index of the item among this CTA's non-empty items
-    Item it;   // the item, decoded once
+    Item it;
 };
 
 __device__ __forceinline__ void cursor_seek(Cursor &cu, int n_items, const Dims &dm, const SegTable &tab)
@@ -375,7 +264,6 @@ __device__ __forceinline__ void cursor_next(Cursor &cu, int n_items, const Dims 
     }
 }
 
-// The three K32-operand MMA groups of a chunk (issued by one thread).
 __device__ __forceinline__ void issue_gram(uint32_t tb, uint32_t sK32)
 {
 #pragma unroll
@@ -383,17 +271,48 @@ __device__ __forceinline__ void issue_gram(uint32_t tb, uint32_t sK32)
         tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(64, 64),
                    ks > 0);
 }
-__device__ __forceinline__ void issue_pt(uint32_t tb, uint32_t sK32)
+
+// Xt_T <- s Xt_T and its truncated-away low part in bf16 (this thread's lane).
+__device__ __forceinline__ void scale_split_xt(uint32_t my, float s)
 {
+    const float2 s2 = make_float2(s, s), m1 = make_float2(-1.f, -1.f);
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+        float x[32];
+        uint32_t lo[16];
+        tc::tmem_ld32(my + TM_XT + cc, x);
 #pragma unroll
-    for (int ks = 0; ks < D / 8; ++ks)
-        tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(128, 64), ks > 0);
+        for (int i = 0; i < 16; ++i) {
+            const float2 v = __fmul2_rn(s2, make_float2(x[2 * i], x[2 * i + 1]));
+            const float2 h = make_float2(__uint_as_float(__float_as_uint(v.x) & 0xffffe000u),
+                                         __uint_as_float(__float_as_uint(v.y) & 0xffffe000u));
+            const float2 l = __ffma2_rn(h, m1, v);  // v - h, exact
+            lo[i] = pack_bf16(l.x, l.y);
+            x[2 * i] = v.x;
+            x[2 * i + 1] = v.y;
+        }
+        tc::tmem_st32_async(my + TM_XT + cc, x);
+        tc::tmem_st16_async(my + TM_XLO + cc / 2, lo);
+        tc::tmem_wait_st();
+    }
 }
-__device__ __forceinline__ void issue_ps(uint32_t tb, uint32_t sK32)
+
+// 128 consecutive columns of this thread's lane scaled by s.
+__device__ __forceinline__ void scale_cols(uint32_t taddr, float s)
 {
+    const float2 s2 = make_float2(s, s);
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+        float x[32];
+        tc::tmem_ld32(taddr + cc, x);
 #pragma unroll
-    for (int ks = 0; ks < D / 8; ++ks)
-        tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(128, 64), ks > 0);
+        for (int i = 0; i < 16; ++i) {
+            const float2 v = __fmul2_rn(s2, make_float2(x[2 * i], x[2 * i + 1]));
+            x[2 * i] = v.x;
+            x[2 * i + 1] = v.y;
+        }
+        tc::tmem_st32(taddr + cc, x);
+    }
 }
 
 template <int CK, bool ACT>
@@ -403,16 +322,17 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
 {
     constexpr int HIST = CK > 0 ? CK - 1 : 0;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // the 1024-aligned base, derived from the shared array itself so that every
+    // access through it stays a shared-memory access
+    const uint32_t raw_u32 = tc::smem_u32(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
     const uint32_t s_base = tc::smem_u32(sm);
-    const uint32_t sK32 = s_base + SM_K32, sUT = s_base + SM_UT, sMT = s_base + SM_MT;
     auto bar = [&](int i) { return s_base + SM_BAR + 8u * i; };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM_MISC);
     uint32_t *tmem_base_sh = reinterpret_cast<uint32_t *>(sm + SM_MISC + 16);
-    float *Ls = reinterpret_cast<float *>(sm + SM_L);
-    float *Ms = reinterpret_cast<float *>(sm + SM_M);
-    float *Qs = reinterpret_cast<float *>(sm + SM_Q);
-    uint8_t *Mt = sm + SM_MT;  // M^T during the inverse, then (D M)^T in place
+    auto gates = [&](int n) -> const Gates & {
+        return *reinterpret_cast<const Gates *>(sm + SM_GATE + (n % RG) * G_STAGE);
+    };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Dims dm = a.dm;
@@ -423,54 +343,291 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t cnt = 1;
-            if (i >= B_EMPTY && i < B_EMPTY + RS) cnt = 2;
+            if (i >= B_GE && i < B_GE + RG) cnt = 3;
+            if (i >= B_K32E && i < B_K32E + 2) cnt = 2;
             tc::mbar_init(bar(i), cnt);
         }
         tc::fence_mbar_init();
     }
-    for (int i = tid; i < C * LP; i += NT) Ms[i] = 0.f;  // the upper blocks of M stay zero
-    for (int i = tid; i < C * C; i += NT) reinterpret_cast<float *>(Mt)[i] = 0.f;
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_base_sh), TM_COLS);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tb = *tmem_base_sh;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t my = tb + lane_off;  // this thread's lane (quadrant of its warp), column 0
+    const uint32_t my = tb + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // this warp's lane quadrant
 
     if (warp == WARP_TMA) {
         // ------------------------------------------------------------ producer
-        const __nv_bfloat16 *ap = static_cast<const __nv_bfloat16 *>(a.tok.alpha);
-        const __nv_bfloat16 *bp = static_cast<const __nv_bfloat16 *>(a.tok.beta);
+        // lane 0: raw K ring, lane 1: raw V ring (independent loops)
+        if (lane < 2) {
+            const bool kside = lane == 0;
+            const int R = kside ? RK : RV;
+            const int bfull = kside ? B_KRF : B_VRF, bempty = kside ? B_KRE : B_VRE;
+            const uint32_t dst0 = s_base + (kside ? SM_KR : SM_VR);
+            const uint32_t stage = kside ? KR_STAGE : VR_STAGE;
+            const CUtensorMap *map = kside ? &tmK : &tmV;
+            int n = 0;
+            bool ok = true;
+            for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
+                const Item it = decode_item(itx, dm, tab);
+                for (int c = 0; c < it.nch; ++c, ++n) {
+                    const int s = n % R, use = n / R;
+                    if (use > 0 && !wait_bar(bar(bempty + s), (use - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(bar(bfull + s), (C + HIST) * D * 2);
+                    tc::tma_load_4d(dst0 + s * stage, map, 0, it.h, it.b0 + c * C - HIST, it.l, bar(bfull + s));
+                }
+            }
+            if (!ok) {
+                // aborted: let the copies this lane started land before the CTA exits
+                for (int k = (n > R ? n - R : 0); k < n; ++k) {
+                    const long long t0 = clock64();
+                    while (!tc::mbar_test(bar(bfull + k % R), (k / R) & 1) && clock64() - t0 < kWaitCycles) {
+                    }
+                }
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------ MMA issuer
+        // Per chunk n: Pt_S(n), Pt_T(n) and its bf16 correction, Gram(n+1),
+        // Xt_T update(n), Xt_S update(n).  tcgen05.mma from one thread execute
+        // in issue order, so a later MMA never overwrites tensor memory that
+        // an earlier one still reads.
+        if (lane == 0) {
+            Cursor mc{static_cast<int>(blockIdx.x), 0, 0, 0, 0, {}};
+            cursor_seek(mc, n_items, dm, tab);
+            bool ok = true;
+            if (mc.item < n_items) {
+                ok = wait_bar(bar(B_KRDY), 0, abort_flag);
+                tc::fence_after();
+                if (ok) {
+                    issue_gram(tb, s_base + SM_K32);
+                    tc::commit(bar(B_GRAMF));
+                }
+            }
+            while (ok && mc.item < n_items) {
+                const int n = mc.n;
+                const uint32_t par = n & 1;
+                const uint32_t sK = s_base + SM_K32 + (n & 1) * 32768;
+                const uint32_t sK16 = s_base + SM_KR + (n % RK) * KR_STAGE;
+                if (mc.c == 0 && !wait_bar(bar(B_XSI), mc.xi & 1, abort_flag)) break;
+                tc::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ts(tb + TM_PS, tb + TM_XS + ks * 8, tc::sdesc_kstep(sK, C, ks), tc::idesc_tf32(128, 64),
+                               ks > 0);
+                tc::commit(bar(B_PSF));
+                if (!wait_bar(bar(B_XTR), par, abort_flag)) break;
+                tc::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_ts(tb + TM_PT, tb + TM_XT + ks * 8, tc::sdesc_kstep(sK, C, ks), tc::idesc_tf32(128, 64),
+                               ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    tc::mma_ts_bf16(tb + TM_PT, tb + TM_XLO + ks * 8, tc::sdesc_kstep(sK16, C, ks),
+                                    tc::idesc_bf16(128, 64), 1);
+                tc::commit(bar(B_PTF));
+                tc::commit(bar(B_K32E + (n & 1)));
+                tc::commit(bar(B_KRE + n % RK));
+                Cursor nx = mc;
+                cursor_next(nx, n_items, dm, tab);
+                if (nx.item < n_items) {
+                    const int n1 = n + 1;
+                    if (!wait_bar(bar(B_KRDY + (n1 & 1)), (n1 >> 1) & 1, abort_flag)) break;
+                    if (!wait_bar(bar(B_GRAME), par, abort_flag)) break;
+                    tc::fence_after();
+                    issue_gram(tb, s_base + SM_K32 + (n1 & 1) * 32768);
+                    tc::commit(bar(B_GRAMF));
+                }
+                if (!wait_bar(bar(B_UTF), par, abort_flag)) break;
+                if (!wait_bar(bar(B_RTF), par, abort_flag)) break;
+                tc::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks)
+                    tc::mma_ts(tb + TM_XT, tb + TM_PT + ks * 8, tc::sdesc_kstep(s_base + SM_UT, D, ks),
+                               tc::idesc_tf32(128, 128), 1);
+                tc::commit(bar(B_XTD));
+                if (!wait_bar(bar(B_RSF), par, abort_flag)) break;
+                tc::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks)
+                    tc::mma_ts(tb + TM_XS, tb + TM_PS + ks * 8, tc::sdesc_kstep(s_base + SM_UT, D, ks),
+                               tc::idesc_tf32(128, 128), 1);
+                tc::commit(bar(B_XSD));
+                tc::commit(bar(B_UTE));
+                mc = nx;
+            }
+            // every MMA issued must complete before tensor memory is released
+            tc::commit(bar(B_FIN));
+            const long long t0 = clock64();
+            while (!tc::mbar_test(bar(B_FIN), 0) && clock64() - t0 < kWaitCycles) {
+            }
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ------------------------------------------------------------ conversion
+        const int ct = tid - 256;       // 0 .. 127
+        const int c0 = lane * 4;        // the 4 channels this thread converts ...
+        const int r0 = 16 * (warp - 8); // ... in chunk rows r0 .. r0+15 (one warp per 16 rows)
+        const uint16_t *ap = static_cast<const uint16_t *>(a.tok.alpha);
+        const uint16_t *bp = static_cast<const uint16_t *>(a.tok.beta);
+        // bf16 bits of (alpha, beta) of tokens 2 lane, 2 lane + 1 of a chunk, packed
+        // alpha | beta << 16 (padding: alpha = 1, beta = 0); warp 8 loads them one
+        // chunk ahead so that the global-load latency hides behind a conversion
+        auto load_gates = [&](const Item &itg, int cg, uint32_t (&gv)[2]) {
+            const int ncg = min(C, (int)(itg.n - cg * C));
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int tt = 2 * lane + u;
+                gv[u] = 0x3F80u;
+                if (tt < ncg) {
+                    const size_t gi = gate_index(dm, N, itg.l, itg.b0 + cg * C + tt, itg.h);
+                    gv[u] = static_cast<uint32_t>(ap[gi]) | (static_cast<uint32_t>(bp[gi]) << 16);
+                }
+            }
+        };
+        uint32_t gcur[2] = {0x3F80u, 0x3F80u};
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
             const Item it = decode_item(itx, dm, tab);
-            for (int c = 0; c < it.nch; ++c) {
-                const int s = n % RS, use = n / RS;
-                if (use > 0) {
-                    bool w = true;
-                    if (lane == 0) w = wait_bar(bar(B_EMPTY + s), (use - 1) & 1, abort_flag);
-                    if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-                }
-                uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                const int32_t t0 = c * C;
-                const int nc = min(C, (int)(it.n - t0));
-                {
-                    // gates of tokens 2 lane, 2 lane + 1 (padding: alpha = 1, beta = 0)
-                    float al[2] = {1.f, 1.f}, be[2] = {0.f, 0.f};
+            if (it.nch == 0) continue;
+            if (warp == 8 && n == 0) load_gates(it, 0, gcur);
+            if (CK > 0) {
+                // K conv weights of this item (the previous chunk's readers
+                // passed the group barrier that ends it); read after the
+                // barrier below
+                const float *wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
+                const float4 w4 = *reinterpret_cast<const float4 *>(wk + ct * CK);
+                float *ws = reinterpret_cast<float *>(sm + SM_WK);
+                ws[ct] = w4.x;
+                ws[D + ct] = w4.y;
+                ws[2 * D + ct] = w4.z;
+                ws[3 * D + ct] = w4.w;
+            }
+            for (int c = 0; c < it.nch && ok; ++c, ++n) {
+                const int nc = min(C, (int)(it.n - c * C));
+                bool w = true;
+                if (ct == 0) w = wait_bar(bar(B_KRF + n % RK), (n / RK) & 1, abort_flag);
+                if (ct == 32 && n >= 2) w = wait_bar(bar(B_K32E + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
+                if (ct == 64 && n >= RG) w = wait_bar(bar(B_GE + n % RG), ((n / RG) - 1) & 1, abort_flag);
+                if (!tc::bar_and(BAR_CONV, 128, w)) { ok = false; break; }
+                uint8_t *stg = sm + SM_KR + (n % RK) * KR_STAGE;
+                uint8_t *k32 = sm + SM_K32 + (n & 1) * 32768;
+#pragma unroll 1
+                for (int hf = 0; hf < 4; ++hf) {
+                    const int rb = r0 + 4 * hf;
+                    // rows rb .. rb+3 from staged rows rb .. rb+3+HIST (staged row t + HIST - j is
+                    // lag j of row t); channel pairs (c0, c0 + 1), (c0 + 2, c0 + 3) packed
+                    float2 kx[4][2];
+                    if (CK == 0) {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int tt = 2 * lane + u;
-                        if (tt < nc) {
-                            const size_t gi = gate_index(dm, N, it.l, it.b0 + t0 + tt, it.h);
-                            al[u] = __bfloat162float(ap[gi]);
-                            be[u] = __bfloat162float(bp[gi]);
+                        for (int r = 0; r < 4; ++r) {
+                            const uint2 u = *reinterpret_cast<const uint2 *>(stg + ((rb + r) * D + c0) * 2);
+                            kx[r][0] = make_float2(bf16_lo(u.x), bf16_hi(u.x));
+                            kx[r][1] = make_float2(bf16_lo(u.y), bf16_hi(u.y));
+                        }
+                    } else {
+                        float2 w2[CK > 0 ? CK : 1][2];
+#pragma unroll
+                        for (int j = 0; j < (CK > 0 ? CK : 1); ++j) {
+                            const float4 wa = *reinterpret_cast<const float4 *>(sm + SM_WK + (j * D + c0) * 4);
+                            w2[j][0] = make_float2(wa.x, wa.y);
+                            w2[j][1] = make_float2(wa.z, wa.w);
+                        }
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) kx[r][0] = kx[r][1] = make_float2(0.f, 0.f);
+                        // each staged row is unpacked once and feeds every output row that uses it
+#pragma unroll
+                        for (int i = 0; i < 4 + HIST; ++i) {
+                            const uint2 u = *reinterpret_cast<const uint2 *>(stg + ((rb + i) * D + c0) * 2);
+                            const float2 x0 = make_float2(bf16_lo(u.x), bf16_hi(u.x));
+                            const float2 x1 = make_float2(bf16_lo(u.y), bf16_hi(u.y));
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                const int j = r + HIST - i;
+                                if (j >= 0 && j < CK) {
+                                    kx[r][0] = __ffma2_rn(w2[j][0], x0, kx[r][0]);
+                                    kx[r][1] = __ffma2_rn(w2[j][1], x1, kx[r][1]);
+                                }
+                            }
+                        }
+                        if (ACT) {
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                                for (int pp = 0; pp < 2; ++pp)
+                                    kx[r][pp] = make_float2(silu(kx[r][pp].x), silu(kx[r][pp].y));
                         }
                     }
-                    Gates &G = *reinterpret_cast<Gates *>(stg + ST_G);
-                    const float x0 = fmaxf(logf(al[0]), -88.f);  // alpha = 0 -> exp(-88)
-                    const float x1 = fmaxf(logf(al[1]), -88.f);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        if (rb + r >= nc) kx[r][0] = kx[r][1] = make_float2(0.f, 0.f);
+                    }
+                    if (CK > 0) {
+                        // L2 norm over the row's 128 channels: the warp's 32 lanes
+                        float ss[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float2 s2 = __ffma2_rn(kx[r][1], kx[r][1], __fmul2_rn(kx[r][0], kx[r][0]));
+                            ss[r] = s2.x + s2.y;
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float inv = rsqrtf(ss[r] + kL2Eps);  // hardware reciprocal square root
+                            const float2 i2 = make_float2(inv, inv);
+                            kx[r][0] = __fmul2_rn(kx[r][0], i2);
+                            kx[r][1] = __fmul2_rn(kx[r][1], i2);
+                        }
+                    }
+                    // K in tf32 (sw128): a row's 32 16-byte chunks, one per lane -- conflict-free
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        *reinterpret_cast<float4 *>(k32 + tc::sw128_f32(rb + r, c0, C)) =
+                            make_float4(tc::round_tf32(kx[r][0].x), tc::round_tf32(kx[r][0].y),
+                                        tc::round_tf32(kx[r][1].x), tc::round_tf32(kx[r][1].y));
+                }
+                uint32_t gnext[2] = {0x3F80u, 0x3F80u};
+                if (warp == 8) {
+                    // the next chunk of this CTA: the next one of this item, else the first
+                    // of the next non-empty item
+                    if (c + 1 < it.nch) {
+                        load_gates(it, c + 1, gnext);
+                    } else {
+                        for (int nx = itx + gridDim.x; nx < n_items; nx += gridDim.x) {
+                            const Item itn = decode_item(nx, dm, tab);
+                            if (itn.nch > 0) {
+                                load_gates(itn, 0, gnext);
+                                break;
+                            }
+                        }
+                    }
+                }
+                tc::bar_sync(BAR_CONV, 128);  // every raw row of the stage has been read
+                // K in bf16, in place over the raw rows: bf16 of the tf32 values just
+                // written (the correction product it feeds is ~2^-11 of Pt_T, so the
+                // second rounding is far below the tolerance)
+#pragma unroll 4
+                for (int r = 0; r < 16; ++r) {
+                    const int row = r0 + r;
+                    const float4 v = *reinterpret_cast<const float4 *>(k32 + tc::sw128_f32(row, c0, C));
+                    *reinterpret_cast<uint2 *>(stg + (c0 >> 6) * 8192 + row * 128 +
+                                               ((((c0 & 63) >> 3) ^ (row & 7)) << 4) + (c0 & 7) * 2) =
+                        make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+                }
+                tc::fence_async_smem();
+                if (warp == 8) {
+                    Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (n % RG) * G_STAGE);
+                    const float al0 = __uint_as_float(gcur[0] << 16), al1 = __uint_as_float(gcur[1] << 16);
+                    const float be[2] = {__uint_as_float(gcur[0] & 0xffff0000u), __uint_as_float(gcur[1] & 0xffff0000u)};
+                    const float x0 = fmaxf(logf(al0), -88.f);  // alpha = 0 -> exp(-88)
+                    const float x1 = fmaxf(logf(al1), -88.f);
                     float sum = x0 + x1;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
@@ -478,7 +635,9 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         if (lane >= o) sum += y;
                     }
                     const float total = __shfl_sync(0xffffffffu, sum, 31);
+                    const float first = __shfl_sync(0xffffffffu, x0, 0);
                     const float g1 = sum, g0 = sum - x1;
+                    const float gm = 0.5f * (first + total);
                     G.g[2 * lane] = g0;
                     G.g[2 * lane + 1] = g1;
                     G.eg[2 * lane] = expf(g0);
@@ -487,318 +646,333 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     G.b[2 * lane + 1] = be[1];
                     G.dc[2 * lane] = be[0] * expf(total - g0);
                     G.dc[2 * lane + 1] = be[1] * expf(total - g1);
-                    const float gm = 0.5f * (__shfl_sync(0xffffffffu, x0, 0) + total);
                     G.fb[2 * lane] = be[0] * __expf(fmaxf(gm - g0, -87.f));
                     G.fb[2 * lane + 1] = be[1] * __expf(fmaxf(gm - g1, -87.f));
+                    *reinterpret_cast<float2 *>(&G.nrc[2 * lane]) =
+                        make_float2(-expf(fminf(g0 - total, 88.f)), -expf(fminf(g1 - total, 88.f)));
+                    *reinterpret_cast<float2 *>(&G.neg[2 * lane]) = make_float2(-expf(g0), -expf(g1));
+                    if (lane == 0) G.safe = (first - total <= kSpan) ? 1 : 0;
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    const uint32_t fb = bar(B_FULL + s);
-                    tc::mbar_arrive_expect_tx(fb, 2u * (C + HIST) * D * 2);
-                    const int row0 = it.b0 + t0 - HIST;
-                    tc::tma_load_4d(s_base + SM_RAW + s * ST_BYTES + ST_K, &tmK, 0, it.h, row0, it.l, fb);
-                    tc::tma_load_4d(s_base + SM_RAW + s * ST_BYTES + ST_V, &tmV, 0, it.h, row0, it.l, fb);
+                tc::bar_sync(BAR_CONV, 128);
+                if (ct == 0) {
+                    tc::mbar_arrive(bar(B_KRDY + (n & 1)));
+                    tc::mbar_arrive(bar(B_GF + n % RG));
                 }
-                ++n;
+                gcur[0] = gnext[0];
+                gcur[1] = gnext[1];
             }
         }
-        if (!ok && lane == 0) {
-            // aborted: let the copies this warp started land before the CTA exits
-            for (int k = (n > RS ? n - RS : 0); k < n; ++k) {
-                const long long t0 = clock64();
-                while (!tc::mbar_test(bar(B_FULL + k % RS), (k / RS) & 1) && clock64() - t0 < kWaitCycles) {
-                }
-            }
-        }
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------ MMA issuer
-        // Issue order: Gram(0), Pt(0); then per chunk n: U~(n), Gram(n+1),
-        // Xt_T update (n), Xt_S update (n), Pt(n+1) -- each as soon as its
-        // inputs are ready (hardware-suspended bounded waits).  Gram(n+1)
-        // runs ahead of chunk n's Xt updates so that the preparation warps
-        // find it done; tcgen05.mma from one thread execute in issue order, so
-        // a later MMA never overwrites tensor memory that an earlier one reads.
-        if (lane == 0) {
-            Cursor mc{static_cast<int>(blockIdx.x), 0, 0, 0, 0, {}};
-            cursor_seek(mc, n_items, dm, tab);
-            bool go = mc.item < n_items;
-            if (go) {
-                go = wait_bar(bar(B_KREADY), 0, abort_flag) && wait_bar(bar(B_XREADY), 0, abort_flag);
-                tc::fence_after();
-                if (go) {
-                    issue_gram(tb, sK32);
-                    tc::commit(bar(B_GRAM));
-                    issue_pt(tb, sK32);
-                    tc::commit(bar(B_PTDONE));
-                    issue_ps(tb, sK32);
-                    tc::commit(bar(B_PSDONE));
-                }
-            }
-            while (go && mc.item < n_items) {
-                const uint32_t par = mc.n & 1;
-                if (!wait_bar(bar(B_KTREADY), par, abort_flag)) break;
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    tc::mma_ts(tb + TM_U, tb + TM_G + ks * 8, tc::sdesc_kstep(sMT, C, ks),
-                               tc::idesc_tf32(128, 64), ks > 0);
-                tc::commit(bar(B_UDONE));
-                Cursor nx = mc;
-                cursor_next(nx, n_items, dm, tab);
-                const bool more = nx.item < n_items;
-                if (more) {
-                    if (!wait_bar(bar(B_KREADY), par ^ 1u, abort_flag)) break;
-                    tc::fence_after();
-                    issue_gram(tb, sK32);
-                    tc::commit(bar(B_GRAM));
-                }
-                if (!wait_bar(bar(B_UTREADY), par, abort_flag)) break;
-                if (!wait_bar(bar(B_RTREADY), par, abort_flag)) break;
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    tc::mma_ts(tb + TM_XT, tb + TM_PT + ks * 8, tc::sdesc_kstep(sUT, D, ks),
-                               tc::idesc_tf32(128, 128), 1);
-                if (!wait_bar(bar(B_RSREADY), par, abort_flag)) break;
-                tc::fence_after();
-#pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    tc::mma_ts(tb + TM_XS, tb + TM_PS + ks * 8, tc::sdesc_kstep(sUT, D, ks),
-                               tc::idesc_tf32(128, 128), 1);
-                tc::commit(bar(B_DSDONE));
-                if (more) {
-                    if (nx.c == 0 && !wait_bar(bar(B_XREADY), nx.xi & 1, abort_flag)) break;
-                    tc::fence_after();
-                    issue_pt(tb, sK32);
-                    tc::commit(bar(B_PTDONE));
-                    issue_ps(tb, sK32);
-                    tc::commit(bar(B_PSDONE));
-                }
-                mc = nx;
-            }
-        }
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ preparation
-        // Step k: finish chunk k-1 up to its U~ operands (L, inverse, K^T,
-        // (D M)^T), convert chunk k (gates, conv + normalisation, tf32 K)
-        // while U~(k-1) runs, then copy U~(k-1)^T to shared memory.
-        const int pt = tid - 128;      // 0 .. NP-1
-        const int li = pt & 127;       // tensor-memory lane of this thread
-        const int hh = pt >> 7;        // which half of a 64-column operand this warp handles
-        const int c0 = (pt & 15) * 8;  // the 8 channels this thread converts ...
-        const int r0 = 4 * (pt >> 4);  // ... in chunk rows r0 .. r0+3
-        int wk_item = -1;  // item whose conv weights are in shared memory
-        Cursor cv{static_cast<int>(blockIdx.x), 0, 0, 0, 0, {}};
-        cursor_seek(cv, n_items, dm, tab);
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ solve
+        const int sp = tid - 384;  // 0 .. 127
+        const int q = warp & 3;    // lane quadrant; diagonal block; channels 32q .. 32q+31
+        const int g = lane >> 2, t4 = lane & 3;
+        float *Ls = reinterpret_cast<float *>(sm + SM_L);
+        const uint32_t sL = s_base + SM_L, sA1 = s_base + SM_A1, sMT = s_base + SM_MT, sUT = s_base + SM_UT;
+        uint8_t *ut = sm + SM_UT;
+        int n = 0;
         bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const bool conv_k = cv.item < n_items;  // chunk k exists
-            if (k > 0) {
-                // ---- chunk m = k-1: L from the Gram rows (M = 64 layout: row 16q + i in lane 32q + i)
-                const int m = k - 1;
-                const Gates &G = *reinterpret_cast<const Gates *>(sm + SM_RAW + (m % RS) * ST_BYTES + ST_G);
+        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
+            const Item it = decode_item(itx, dm, tab);
+            for (int c = 0; c < it.nch; ++c, ++n) {
                 bool w = true;
-                if (pt == 0) w = wait_bar(bar(B_GRAM), m & 1, abort_flag);
-                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
+                if (sp == 0) w = wait_bar(bar(B_GRAMF), n & 1, abort_flag);
+                if (sp == 32) w = wait_bar(bar(B_GF + n % RG), (n / RG) & 1, abort_flag);
+                if (!tc::bar_and(BAR_SOLVE, 128, w)) { ok = false; break; }
                 tc::fence_after();
+                const Gates &G = gates(n);
                 {
-                    // Gram row 16q + i sits in lane 32q + i (i < 16) of quadrant q; this
-                    // warp takes columns 32hh .. 32hh+31 of its 16 rows, lanes 16-31
-                    // the upper 16 of those (shuffled from their partner lane).
+                    // L from the Gram rows: row 16q + i sits in lane 32q + i (i < 16);
+                    // lanes 0-15 take its columns 0-31, lanes 16-31 columns 32-63
                     float gr[32];
-                    tc::tmem_ld32(my + TM_G + hh * 32, gr);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float o = __shfl_up_sync(0xffffffffu, gr[16 + j], 16);
-                        if (lane >= 16) gr[j] = o;
-                    }
-                    const int t = 16 * (warp & 3) + (lane & 15);
-                    const int j0 = hh * 32 + ((lane >= 16) ? 16 : 0);
+                    tc::tmem_ld16x2_32(my + TM_G, gr);
+                    const int t = 16 * q + (lane & 15);
+                    const int j0 = (lane >= 16) ? 32 : 0;
                     const float gt_t = G.g[t];
-                    if (G.g[0] - G.g[C - 1] < 80.f) {
+                    if (G.safe) {
                         // exp(g_t - g_j) = exp(g_t - g_m) exp(g_m - g_j), g_m the chunk midpoint:
                         // both factors stay within e^{+-40}, one exp per row
                         const float gm = 0.5f * (G.g[0] + G.g[C - 1]);
                         const float et = __expf(gt_t - gm);
+                        const float2 e2 = make_float2(et, et);
+                        const float2 *fb2 = reinterpret_cast<const float2 *>(G.fb + j0);
+                        // entries on and above the diagonal are never read (the inverses use
+                        // the strictly lower part; the upper blocks are overwritten below), so
+                        // they are written unmasked: finite, as both factors are bounded
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            gr[j] = (j0 + j < t) ? tc::round_tf32(G.fb[j0 + j] * et * gr[j]) : 0.f;
+                        for (int j = 0; j < 32; j += 2) {
+                            const float2 v = __fmul2_rn(__fmul2_rn(fb2[j / 2], e2), make_float2(gr[j], gr[j + 1]));
+                            gr[j] = tc::round_tf32(v.x);
+                            gr[j + 1] = tc::round_tf32(v.y);
+                        }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            gr[j] = (j0 + j < t) ? tc::round_tf32(G.b[j0 + j] * __expf(gt_t - G.g[j0 + j]) * gr[j]) : 0.f;
+                        for (int j = 0; j < 32; ++j)
+                            gr[j] = (j0 + j < t) ? tc::round_tf32(G.b[j0 + j] * __expf(gt_t - G.g[j0 + j]) * gr[j])
+                                                 : 0.f;
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4)
+                    for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4 *>(Ls + t * LP + j0 + j) = make_float4(gr[j], gr[j + 1], gr[j + 2], gr[j + 3]);
                 }
-                tc::bar_sync(BAR_PREP, NP);
-                unit_lower_inverse(Ls, Ms, Mt, Qs, pt);
-                // K^T into tensor memory (A of U~): lane i holds K[j][i], this warp j = 32hh .. +31
-                {
-                    float kt[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        kt[j] = *reinterpret_cast<const float *>(sm + SM_K32 + tc::sw128_f32(hh * 32 + j, li, C));
-                    tc::tmem_st32(my + TM_G + hh * 32, kt);
-                }
-                // B of U~: element (t, j) = dc_j M[j][t], scaled in place in the M^T tile
-#pragma unroll
-                for (int e = pt; e < C * C / 4; e += NP) {
-                    const int t = e & (C - 1), j = (e >> 6) * 4;
-                    float4 *p = reinterpret_cast<float4 *>(Mt + tc::sw128_f32(t, j, C));
-                    const float4 mv = *p;
-                    *p = make_float4(tc::round_tf32(G.dc[j] * mv.x), tc::round_tf32(G.dc[j + 1] * mv.y),
-                                     tc::round_tf32(G.dc[j + 2] * mv.z), tc::round_tf32(G.dc[j + 3] * mv.w));
-                }
-                tc::fence_async_smem();
                 tc::fence_before();
-                tc::bar_sync(BAR_PREP, NP);
-                if (pt == 0) {
-                    tc::mbar_arrive(bar(B_KTREADY));
-                    tc::mbar_arrive(bar(B_EMPTY + m % RS));  // K rows and gates consumed
-                }
-            }
-            if (conv_k) {
-                // ---- chunk k: gates and K -> tf32 (conv + L2 normalisation first when present)
-                const Item &it = cv.it;
-                if (CK > 0 && cv.item != wk_item) {
-                    // visible to all preparation threads after the barrier below
-                    const float *wk = a.tok.conv_w + (((size_t)it.l * 3 + 1) * dm.H + it.h) * D * CK;
-                    if (pt < D) {
-                        const float4 w4 = *reinterpret_cast<const float4 *>(wk + pt * CK);
-                        float *ws = reinterpret_cast<float *>(sm + SM_WK);
-                        ws[pt] = w4.x;
-                        ws[D + pt] = w4.y;
-                        ws[2 * D + pt] = w4.z;
-                        ws[3 * D + pt] = w4.w;
+                tc::bar_sync(BAR_SOLVE, 128);
+                if (sp == 0) tc::mbar_arrive(bar(B_GRAME));
+                if (lane < NB) {
+                    // column `lane` of M_qq = (I + L_qq)^{-1} by forward substitution
+                    const float *Lb = Ls + (NB * q) * LP + NB * q;
+                    float x[NB];
+#pragma unroll
+                    for (int r = 0; r < NB; ++r) x[r] = (r == lane) ? 1.f : 0.f;
+                    // column r of L_qq is loaded one step ahead of its use
+                    float col[NB - 1];
+#pragma unroll
+                    for (int k = 0; k < NB - 1; ++k) col[k] = Lb[(k + 1) * LP];
+#pragma unroll
+                    for (int r = 0; r < NB - 1; ++r) {
+                        float nxt[NB - 1];
+#pragma unroll
+                        for (int k = 0; k < NB - 2 - r; ++k) nxt[k] = Lb[(r + 2 + k) * LP + r + 1];
+                        asm volatile("" ::: "memory");  // issue them before this step's products
+#pragma unroll
+                        for (int k = 0; k < NB - 1 - r; ++k) x[r + 1 + k] = fmaf(-col[k], x[r], x[r + 1 + k]);
+#pragma unroll
+                        for (int k = 0; k < NB - 2 - r; ++k) col[k] = nxt[k];
                     }
-                    wk_item = cv.item;
+                    // M^T row `lane` = column `lane` of M; (D M)^T row `lane` = d_k M[k][lane]
+                    float *mt = reinterpret_cast<float *>(sm + SM_MT + q * BLK) + lane * BP;
+                    float *a1 = reinterpret_cast<float *>(sm + SM_A1 + q * BLK) + lane * BP;
+#pragma unroll
+                    for (int k = 0; k < NB; k += 4) {
+                        *reinterpret_cast<float4 *>(mt + k) =
+                            make_float4(tc::round_tf32(x[k]), tc::round_tf32(x[k + 1]), tc::round_tf32(x[k + 2]),
+                                        tc::round_tf32(x[k + 3]));
+                        *reinterpret_cast<float4 *>(a1 + k) = make_float4(
+                            tc::round_tf32(G.dc[NB * q + k] * x[k]), tc::round_tf32(G.dc[NB * q + k + 1] * x[k + 1]),
+                            tc::round_tf32(G.dc[NB * q + k + 2] * x[k + 2]),
+                            tc::round_tf32(G.dc[NB * q + k + 3] * x[k + 3]));
+                    }
                 }
-                const int s = k % RS;
-                const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                const int nc = min(C, (int)(it.n - cv.c * C));
-                bool w = true;
-                if (pt == 0) w = wait_bar(bar(B_FULL + s), (k / RS) & 1, abort_flag);
-                if (pt == 32 && k > 0) w = wait_bar(bar(B_PSDONE), (k - 1) & 1, abort_flag);  // K32 free
-                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
+                tc::bar_sync(BAR_SOLVE, 128);
                 {
-                    // rows r0 .. r0+3 use staged rows r0 .. r0+3+HIST (row t + HIST - j is lag j)
-                    uint4 raw[4 + HIST];
+                    // -(L_ji M_ii)^T for j > i into the upper block (i, j) of L
+                    // (pairs (1,0) (2,0) (3,0) (2,1) (3,1) (3,2); warp q takes q and q + 4)
+#pragma unroll 1
+                    for (int pi = q; pi < 6; pi += 4) {
+                        const int jj = pi < 3 ? pi + 1 : (pi < 5 ? pi - 1 : 3);
+                        const int ii = pi < 3 ? 0 : (pi < 5 ? 1 : 2);
 #pragma unroll
-                    for (int i = 0; i < 4 + HIST; ++i)
-                        raw[i] = *reinterpret_cast<const uint4 *>(stg + ST_K + ((r0 + i) * D + c0) * 2);
-                    float kx[4][8];
-                    if (CK == 0) {
+                        for (int nt = 0; nt < 2; ++nt) {
+                            float cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) unpack8(raw[r], kx[r]);
-                    } else {
+                            for (int ks = 0; ks < 2; ++ks) {
+                                uint32_t af[4], bf[2];
+                                frag_a(af, sL, LP, NB * jj, NB * ii + 8 * ks, lane);
+                                frag_b(bf, sMT + ii * BLK, BP, 8 * ks, 8 * nt, lane);
+                                mma16x8x8(cc, af, bf);
+                            }
+                            const int nn = NB * ii + 8 * nt + 2 * t4, rr = NB * jj + g;
+                            Ls[nn * LP + rr] = tc::round_tf32(-cc[0]);
+                            Ls[(nn + 1) * LP + rr] = tc::round_tf32(-cc[1]);
+                            Ls[nn * LP + rr + 8] = tc::round_tf32(-cc[2]);
+                            Ls[(nn + 1) * LP + rr + 8] = tc::round_tf32(-cc[3]);
+                        }
+                    }
+                }
+                w = true;
+                if (sp == 0 && n > 0) w = wait_bar(bar(B_UTE), (n - 1) & 1, abort_flag);  // U~^T free
+                if (!tc::bar_and(BAR_SOLVE, 128, w)) { ok = false; break; }
+                {
+                    // U~ for channels 32q .. 32q+31, token blocks 3, 2, 1, 0.  The swizzled
+                    // offsets below are those of tc::sw128_f32 with the block-dependent
+                    // terms split off (token blocks are multiples of 8 rows / 16 columns).
+                    const uint32_t k32 = s_base + SM_K32 + (n & 1) * 32768;
+                    const int h = (lane >> 3) & 1, l7 = lane & 7;
+                    // B of the K_i product: K[16 i + 8 ks + t4 (+4)][32 q + 8 nt + g]
+                    uint32_t kofs[4][2];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r)
+                    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) kx[r][i] = 0.f;
+                        for (int bb = 0; bb < 2; ++bb)
+                            kofs[nt][bb] = q * 8192 + (t4 + 4 * bb) * 128 +
+                                           ((((2 * nt + (g >> 2)) ^ (t4 + 4 * bb)) << 4) + (g & 3) * 4);
+                    // B of the U~_j products (ldmatrix rows = channels): swizzle of column
+                    // group 4 (j & 1) + 2 ks + h
+                    uint32_t sx[4];
 #pragma unroll
-                        for (int j = 0; j < (CK > 0 ? CK : 1); ++j) {
-                            // lag-j weights of channels c0 .. c0+7
-                            const float4 wa = *reinterpret_cast<const float4 *>(sm + SM_WK + (j * D + c0) * 4);
-                            const float4 wb = *reinterpret_cast<const float4 *>(sm + SM_WK + (j * D + c0 + 4) * 4);
-                            const float wj[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                    for (int v = 0; v < 4; ++v) sx[v] = (((2 * v + h) ^ l7) << 4);
+                    const uint32_t ubase = sUT + (32 * q + l7) * 128;
+                    // C stores: element e = (channel + (e & 1), token + 8 (e >> 1))
+                    uint32_t so[2][4];
 #pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                float rk[8];
-                                unpack8(raw[r + HIST - j], rk);
+                    for (int i1 = 0; i1 < 2; ++i1)
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) kx[r][i] = fmaf(wj[i], rk[i], kx[r][i]);
+                        for (int e = 0; e < 4; ++e)
+                            so[i1][e] = (e & 1) * 128 +
+                                        ((((4 * i1 + (g >> 2) + 2 * (e >> 1)) ^ (2 * t4 + (e & 1))) << 4) + (g & 3) * 4);
+                    const uint32_t sbase = SM_UT + (32 * q + 2 * t4) * 128;
+                    const uint32_t a1row = (((lane & 7) + h * 8) * BP + (lane >> 4) * 4) * 4;
+                    const uint32_t lrow = (((lane & 7) + h * 8) * LP + (lane >> 4) * 4) * 4;
+#pragma unroll 1
+                    for (int i = 3; i >= 0; --i) {
+                        float acc[4][4];
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            uint32_t af[4];
+                            ldsm_x4(af, sA1 + i * BLK + a1row + ks * 32);
+                            const uint32_t kb = k32 + (NB * i + 8 * ks) * 128;
+#pragma unroll
+                            for (int nt = 0; nt < 4; ++nt) {
+                                uint32_t bf[2];
+                                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[0]) : "r"(kb + kofs[nt][0]));
+                                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[1]) : "r"(kb + kofs[nt][1]));
+                                mma16x8x8(acc[nt], af, bf);
                             }
                         }
-                        if (ACT) {
+#pragma unroll 1
+                        for (int j = i + 1; j < 4; ++j)
 #pragma unroll
-                            for (int r = 0; r < 4; ++r)
+                            for (int ks = 0; ks < 2; ++ks) {
+                                uint32_t af[4];
+                                ldsm_x4(af, sL + (NB * i * LP + NB * j + 8 * ks) * 4 + lrow);
+                                const uint32_t ub = ubase + (j >> 1) * 16384 + ((j & 1) ? sx[2 + ks] : sx[ks]);
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) kx[r][i] = silu(kx[r][i]);
-                        }
-                    }
+                                for (int nt = 0; nt < 4; ++nt) {
+                                    uint32_t bf[2];
+                                    ldsm_x2(bf, ub + nt * 1024);
+                                    mma16x8x8(acc[nt], af, bf);
+                                }
+                            }
+                        uint8_t *ub = sm + sbase + (i >> 1) * 16384;
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        if (r0 + r >= nc) {
+                        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) kx[r][i] = 0.f;
-                        }
-                    }
-                    if (CK > 0) {
-                        float ss[4];
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            ss[r] = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) ss[r] = fmaf(kx[r][i], kx[r][i], ss[r]);
-                        }
-#pragma unroll
-                        for (int o = 8; o > 0; o >>= 1)
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const float inv = rsqrtf(ss[r] + kL2Eps);  // hardware reciprocal square root
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) kx[r][i] *= inv;
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(r0 + r, c0, C)) =
-                            make_float4(tc::round_tf32(kx[r][0]), tc::round_tf32(kx[r][1]),
-                                        tc::round_tf32(kx[r][2]), tc::round_tf32(kx[r][3]));
-                        *reinterpret_cast<float4 *>(sm + SM_K32 + tc::sw128_f32(r0 + r, c0 + 4, C)) =
-                            make_float4(tc::round_tf32(kx[r][4]), tc::round_tf32(kx[r][5]),
-                                        tc::round_tf32(kx[r][6]), tc::round_tf32(kx[r][7]));
+                            for (int e = 0; e < 4; ++e)
+                                *reinterpret_cast<float *>(ub + nt * 1024 + ((i & 1) ? so[1][e] : so[0][e])) =
+                                    tc::round_tf32(acc[nt][e]);
+                        __syncwarp();
                     }
                 }
                 tc::fence_async_smem();
-                tc::bar_sync(BAR_PREP, NP);
-                if (pt == 0) tc::mbar_arrive(bar(B_KREADY));
-                cursor_next(cv, n_items, dm, tab);
-            }
-            if (k > 0) {
-                // ---- chunk m = k-1: U~^T rows into shared memory once the previous Xt update is done
-                const int m = k - 1;
-                bool w = true;
-                if (pt == 0) w = wait_bar(bar(B_UDONE), m & 1, abort_flag);
-                if (pt == 32 && m > 0) w = wait_bar(bar(B_DSDONE), (m - 1) & 1, abort_flag);
-                if (!tc::bar_and(BAR_PREP, NP, w)) { ok = false; break; }
-                tc::fence_after();
-                {
-                    float u[32];
-                    tc::tmem_ld32(my + TM_U + hh * 32, u);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4 *>(sm + SM_UT + tc::sw128_f32(li, hh * 32 + i, D)) =
-                            make_float4(tc::round_tf32(u[i]), tc::round_tf32(u[i + 1]), tc::round_tf32(u[i + 2]),
-                                        tc::round_tf32(u[i + 3]));
+                tc::bar_sync(BAR_SOLVE, 128);
+                if (sp == 0) {
+                    tc::mbar_arrive(bar(B_UTF));
+                    tc::mbar_arrive(bar(B_K32E + (n & 1)));
+                    tc::mbar_arrive(bar(B_GE + n % RG));
                 }
-                tc::fence_async_smem();
-                tc::fence_before();
-                tc::bar_sync(BAR_PREP, NP);
-                if (pt == 0) tc::mbar_arrive(bar(B_UTREADY));
             }
-            if (!conv_k) break;
         }
-    } else {
-        // ------------------------------------------------------------ epilogue (warps 0-3)
-        const int m = tid;  // row of Xt / Pt in each half = tensor-memory lane
-        float wvr[CK > 0 ? CK : 1];
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ T epilogue (warps 0-3)
+        const int m = tid;  // row of Xt_T / Pt_T = tensor-memory lane = column m of T
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
             const Item it = decode_item(itx, dm, tab);
             const size_t pair = ((size_t)it.l * tab.n_seg + it.s) * dm.H + it.h;
             float *To = a.T_out + pair * D * D + m;
+            if (it.nch == 0) {
+                for (int i = 0; i < D; ++i) To[(size_t)i * D] = (i == m) ? 1.f : 0.f;
+                continue;
+            }
+            // Xt_T = s I with s = Gamma_C of the first chunk (pre-scaled) or 1
+            bool w = true;
+            if (m == 0) w = wait_bar(bar(B_GF + n % RG), (n / RG) & 1, abort_flag);
+            if (!tc::bar_and(BAR_TEPI, 128, w)) { ok = false; break; }
+            {
+                const Gates &G0 = gates(n);
+                const float s = G0.safe ? G0.eg[C - 1] : 1.f;
+                const float slo = s - __uint_as_float(__float_as_uint(s) & 0xffffe000u);
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 32) {
+                    float v[32];
+                    uint32_t lo[16];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = (cc + i == m) ? s : 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        lo[i] = pack_bf16((cc + 2 * i == m) ? slo : 0.f, (cc + 2 * i + 1 == m) ? slo : 0.f);
+                    tc::tmem_st32_async(my + TM_XT + cc, v);
+                    tc::tmem_st16_async(my + TM_XLO + cc / 2, lo);
+                    tc::tmem_wait_st();
+                }
+            }
+            tc::fence_before();
+            tc::bar_sync(BAR_TEPI, 128);
+            if (m == 0) tc::mbar_arrive(bar(B_XTR));
+            for (int c = 0; c < it.nch; ++c, ++n) {
+                w = true;
+                if (m == 0) w = wait_bar(bar(B_PTF), n & 1, abort_flag);
+                if (!tc::bar_and(BAR_TEPI, 128, w)) { ok = false; break; }
+                tc::fence_after();
+                const Gates &G = gates(n);
+                const bool safe = G.safe != 0;
+                {
+                    float p[32];
+#pragma unroll 1
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        // pre-scaled: Rt_T = -Pt_T Gamma_t / Gamma_C; else -Pt_T Gamma_t
+                        const float2 *f = reinterpret_cast<const float2 *>((safe ? G.nrc : G.neg) + h2 * 32);
+                        tc::tmem_ld32(my + TM_PT + h2 * 32, p);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 r = __fmul2_rn(f[i], make_float2(p[2 * i], p[2 * i + 1]));
+                            p[2 * i] = tc::round_tf32(r.x);
+                            p[2 * i + 1] = tc::round_tf32(r.y);
+                        }
+                        tc::tmem_st32(my + TM_PT + h2 * 32, p);
+                    }
+                    // not pre-scaled: Xt_T <- Gamma_C Xt_T here, after Pt_T has read it
+                    if (!safe) scale_cols(my + TM_XT, G.eg[C - 1]);
+                }
+                tc::fence_before();
+                tc::bar_sync(BAR_TEPI, 128);
+                if (m == 0) {
+                    tc::mbar_arrive(bar(B_RTF));
+                    tc::mbar_arrive(bar(B_GE + n % RG));
+                }
+                const bool last = c + 1 == it.nch;
+                w = true;
+                if (m == 0) {
+                    w = wait_bar(bar(B_XTD), n & 1, abort_flag);
+                    if (w && !last) w = wait_bar(bar(B_GF + (n + 1) % RG), ((n + 1) / RG) & 1, abort_flag);
+                }
+                if (!tc::bar_and(BAR_TEPI, 128, w)) { ok = false; break; }
+                tc::fence_after();
+                if (last) {
+                    // emit T[i][m] = Xt_T[m][i]
+                    float x[32];
+#pragma unroll 1
+                    for (int cc = 0; cc < D; cc += 32) {
+                        tc::tmem_ld32(my + TM_XT + cc, x);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) To[(size_t)(cc + i) * D] = x[i];
+                    }
+                } else {
+                    const Gates &G1 = gates(n + 1);
+                    scale_split_xt(my, G1.safe ? G1.eg[C - 1] : 1.f);
+                    tc::fence_before();
+                    tc::bar_sync(BAR_TEPI, 128);
+                    if (m == 0) tc::mbar_arrive(bar(B_XTR));
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ S epilogue (warps 4-7)
+        const int m = tid - 128;  // row of Xt_S / Pt_S = column m of S (and value channel m)
+        float wvr[CK > 0 ? CK : 1];
+        int n = 0;
+        bool ok = true;
+        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
+            const Item it = decode_item(itx, dm, tab);
+            const size_t pair = ((size_t)it.l * tab.n_seg + it.s) * dm.H + it.h;
             float *So = a.S_out + pair * D * D + m;
             if (it.nch == 0) {
-                for (int i = 0; i < D; ++i) {
-                    To[(size_t)i * D] = (i == m) ? 1.f : 0.f;
-                    So[(size_t)i * D] = 0.f;
-                }
+                for (int i = 0; i < D; ++i) So[(size_t)i * D] = 0.f;
                 continue;
             }
             if (CK > 0) {
@@ -806,120 +980,86 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
 #pragma unroll
                 for (int j = 0; j < (CK > 0 ? CK : 1); ++j) wvr[j] = __ldg(wv + m * CK + j);
             }
-            // Xt = [I | 0]^T
             {
                 float v[32];
 #pragma unroll
-                for (int c = 0; c < D; c += 32) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = (c + i == m) ? 1.f : 0.f;
-                    tc::tmem_st32(my + TM_XT + c, v);
-                }
-#pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
 #pragma unroll
-                for (int c = 0; c < D; c += 32) tc::tmem_st32(my + TM_XS + c, v);
+                for (int cc = 0; cc < D; cc += 32) tc::tmem_st32_async(my + TM_XS + cc, v);
+                tc::tmem_wait_st();
             }
             tc::fence_before();
-            tc::bar_sync(BAR_EPI, 128);
-            if (m == 0) tc::mbar_arrive(bar(B_XREADY));
+            tc::bar_sync(BAR_SEPI, 128);
+            if (m == 0) tc::mbar_arrive(bar(B_XSI));
             for (int c = 0; c < it.nch; ++c, ++n) {
-                const int s = n % RS;
-                const uint8_t *stg = sm + SM_RAW + s * ST_BYTES;
-                const Gates &G = *reinterpret_cast<const Gates *>(stg + ST_G);
                 const int nc = min(C, (int)(it.n - c * C));
-                // ---- T half
+                const uint8_t *stg = sm + SM_VR + (n % RV) * VR_STAGE;
                 bool w = true;
-                if (m == 0) w = wait_bar(bar(B_PTDONE), n & 1, abort_flag);
-                if (!tc::bar_and(BAR_EPI, 128, w)) { ok = false; break; }
+                if (m == 0) w = wait_bar(bar(B_PSF), n & 1, abort_flag);
+                if (m == 32) w = wait_bar(bar(B_VRF + n % RV), (n / RV) & 1, abort_flag);
+                if (m == 64) w = wait_bar(bar(B_GF + n % RG), (n / RG) & 1, abort_flag);
+                if (!tc::bar_and(BAR_SEPI, 128, w)) { ok = false; break; }
                 tc::fence_after();
-                const float gC = G.eg[C - 1];
+                const Gates &G = gates(n);
                 {
                     float p[32];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        tc::tmem_ld32(my + TM_PT + h2 * 32, p);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) p[i] = tc::round_tf32(-G.eg[h2 * 32 + i] * p[i]);
-                        tc::tmem_st32(my + TM_PT + h2 * 32, p);
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
-                        tc::tmem_ld32(my + TM_XT + cc, p);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) p[i] *= gC;
-                        tc::tmem_st32(my + TM_XT + cc, p);
-                    }
-                }
-                tc::fence_before();
-                tc::bar_sync(BAR_EPI, 128);
-                if (m == 0) tc::mbar_arrive(bar(B_RTREADY));
-                // ---- S half
-                if (m == 0) {
-                    w = wait_bar(bar(B_PSDONE), n & 1, abort_flag);
-                    if (w) w = wait_bar(bar(B_FULL + s), (n / RS) & 1, abort_flag);
-                }
-                if (!tc::bar_and(BAR_EPI, 128, w)) { ok = false; break; }
-                tc::fence_after();
-                {
-                    float p[32];
-                    // raw V history window for the conv: win[j] = row t + HIST - j
-                    float win[HMAX + 1];
-#pragma unroll
-                    for (int j = 1; j <= HMAX; ++j) win[j] = (j <= HIST) ? bf16_at(stg + ST_V, HIST - j, m) : 0.f;
-#pragma unroll
+#pragma unroll 1
                     for (int h2 = 0; h2 < 2; ++h2) {
                         tc::tmem_ld32(my + TM_PS + h2 * 32, p);
+                        const float2 *ng = reinterpret_cast<const float2 *>(G.neg + h2 * 32);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int t = h2 * 32 + i;
-                            win[0] = bf16_at(stg + ST_V, t + HIST, m);
-                            float vv = 0.f;
-                            if (CK == 0) {
-                                vv = win[0];
-                            } else {
+                        for (int qq = 0; qq < 2; ++qq) {
+                            // raw V of channel m, tokens t0 - HIST .. t0 + 15 (staged rows t0 ..)
+                            const int t0 = h2 * 32 + qq * 16;
+                            float v[16 + HIST];
 #pragma unroll
-                                for (int j = 0; j < (CK > 0 ? CK : 1); ++j) vv = fmaf(wvr[j], win[j], vv);
-                                if (ACT) vv = silu(vv);
+                            for (int i = 0; i < 16 + HIST; ++i) v[i] = bf16_at(stg, t0 + i, m);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int t = t0 + 2 * i, e = qq * 16 + 2 * i;
+                                float2 vv;
+                                if (CK == 0) {
+                                    vv = make_float2(v[2 * i], v[2 * i + 1]);
+                                } else {
+                                    // token t + u uses staged row t + u + HIST - j (lag j)
+                                    vv = make_float2(0.f, 0.f);
+#pragma unroll
+                                    for (int j = 0; j < (CK > 0 ? CK : 1); ++j)
+                                        vv = __ffma2_rn(make_float2(wvr[j], wvr[j]),
+                                                        make_float2(v[2 * i + HIST - j], v[2 * i + 1 + HIST - j]), vv);
+                                    if (ACT) vv = make_float2(silu(vv.x), silu(vv.y));
+                                }
+                                if (t >= nc) vv.x = 0.f;
+                                if (t + 1 >= nc) vv.y = 0.f;
+                                const float2 r = __ffma2_rn(ng[qq * 8 + i], make_float2(p[e], p[e + 1]), vv);
+                                p[e] = tc::round_tf32(r.x);
+                                p[e + 1] = tc::round_tf32(r.y);
                             }
-                            if (t >= nc) vv = 0.f;
-                            p[i] = tc::round_tf32(fmaf(-G.eg[t], p[i], vv));
-#pragma unroll
-                            for (int j = HMAX; j > 0; --j) win[j] = win[j - 1];
                         }
                         tc::tmem_st32(my + TM_PS + h2 * 32, p);
                     }
-#pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
-                        tc::tmem_ld32(my + TM_XS + cc, p);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) p[i] *= gC;
-                        tc::tmem_st32(my + TM_XS + cc, p);
-                    }
+                    scale_cols(my + TM_XS, G.eg[C - 1]);
                 }
                 tc::fence_before();
-                tc::bar_sync(BAR_EPI, 128);
+                tc::bar_sync(BAR_SEPI, 128);
                 if (m == 0) {
-                    tc::mbar_arrive(bar(B_RSREADY));
-                    tc::mbar_arrive(bar(B_EMPTY + s));  // V rows consumed
+                    tc::mbar_arrive(bar(B_RSF));
+                    tc::mbar_arrive(bar(B_VRE + n % RV));
+                    tc::mbar_arrive(bar(B_GE + n % RG));
                 }
-            }
-            if (!ok) break;
-            // ---- emit the finished pair: T[i][m] = Xt_T[m][i], S[i][m] = Xt_S[m][i]
-            bool w = true;
-            if (m == 0) w = wait_bar(bar(B_DSDONE), (n - 1) & 1, abort_flag);
-            if (!tc::bar_and(BAR_EPI, 128, w)) { ok = false; break; }
-            tc::fence_after();
-            {
-                float x[32];
+                if (c + 1 == it.nch) {
+                    // emit S[i][m] = Xt_S[m][i] once the last update is done
+                    w = true;
+                    if (m == 0) w = wait_bar(bar(B_XSD), n & 1, abort_flag);
+                    if (!tc::bar_and(BAR_SEPI, 128, w)) { ok = false; break; }
+                    tc::fence_after();
+                    float x[32];
+#pragma unroll 1
+                    for (int cc = 0; cc < D; cc += 32) {
+                        tc::tmem_ld32(my + TM_XS + cc, x);
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    tc::tmem_ld32(my + TM_XT + cc, x);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) To[(size_t)(cc + i) * D] = x[i];
-                    tc::tmem_ld32(my + TM_XS + cc, x);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) So[(size_t)(cc + i) * D] = x[i];
+                        for (int i = 0; i < 32; ++i) So[(size_t)(cc + i) * D] = x[i];
+                    }
                 }
             }
         }
@@ -931,8 +1071,6 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
     if (tid == 0 && *abort_flag) atomicOr(a.status, 1);
     if (warp == 0) tc::tmem_dealloc(tb, TM_COLS);
 }
-
-int g_num_sms = 0;
 
 cudaError_t make_token_map(CUtensorMap *map, const void *base, const Dims &dm, int32_t N, int rows)
 {
@@ -956,17 +1094,16 @@ cudaError_t launch_build_tc(const BuildArgs &a, const SegTable &tab, cudaStream_
     const int n_items = tab.n_seg * a.dm.L * a.dm.H;
     if (n_items == 0) return cudaSuccess;
     cudaError_t e;
-    if (g_num_sms == 0) {
-        int dev = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    }
+    // the SM count of the device this launch runs on (cheap; no caching across devices)
+    int dev = 0, n_sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int rows = C + (a.dm.conv_k > 0 ? a.dm.conv_k - 1 : 0);
     CUtensorMap tmK, tmV;
     if ((e = make_token_map(&tmK, a.tok.k, a.dm, a.tok.N, rows)) != cudaSuccess) return e;
     if ((e = make_token_map(&tmV, a.tok.v, a.dm, a.tok.N, rows)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.status, 0, sizeof(int), st)) != cudaSuccess) return e;
-    const int grid = n_items < g_num_sms ? n_items : g_num_sms;
+    const int grid = n_items < n_sms ? n_items : n_sms;
     // the activation after the conv is a template flag: no cost when off
     auto kern = a.dm.conv_k == 0 ? build_tc_kernel<0, false>
                                  : (a.dm.act ? build_tc_kernel<4, true> : build_tc_kernel<4, false>);

@@ -156,7 +156,10 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                   const __grid_constant__ TokMaps tmX)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // the 1024-aligned base, derived from the shared array itself so that every
+    // access through it stays a shared-memory access
+    const uint32_t raw_u32 = tc::smem_u32(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
     const uint32_t s_base = tc::smem_u32(sm);
     auto bar = [&](int i) { return s_base + SM_BAR + 8u * i; };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SM_MISC);
