@@ -340,12 +340,20 @@ def test_silu():
 
 
 def test_l2_normalize():
+    """Hand-computed rows: (3, 4) has norm 5, so with eps = 0 it maps to
+    (0.6, 0.8) and with eps = 11 (sqrt(25 + 11) = 6) to (1/2, 2/3); (1, 2, 2)
+    has norm 3, so with eps = 7 (sqrt(9 + 7) = 4) it maps to (1/4, 1/2, 1/2).
+    Rows are normalised independently; a zero row stays zero; the result is
+    invariant to scaling the row when eps = 0."""
+    x = np.array([[3.0, 4.0], [0.0, 0.0], [-4.0, 3.0]])
+    np.testing.assert_allclose(oracle.l2_normalize(x, eps=0.0)[[0, 2]], [[0.6, 0.8], [-0.8, 0.6]], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(oracle.l2_normalize(x, eps=11.0), [[0.5, 2.0 / 3.0], [0.0, 0.0], [-2.0 / 3.0, 0.5]],
+                               rtol=0, atol=1e-15)
+    np.testing.assert_allclose(oracle.l2_normalize(np.array([[1.0, 2.0, 2.0]]), eps=7.0), [[0.25, 0.5, 0.5]],
+                               rtol=0, atol=1e-15)
     rng = np.random.default_rng(19)
-    x = rng.standard_normal((10, 16)) * 5
-    y = oracle.l2_normalize(x)
-    nx = np.linalg.norm(x, axis=1)
-    np.testing.assert_allclose(np.linalg.norm(y, axis=1), nx / np.sqrt(nx ** 2 + oracle.L2_EPS), rtol=1e-12)
-    np.testing.assert_allclose(oracle.l2_normalize(3.0 * x, eps=0.0), oracle.l2_normalize(x, eps=0.0), rtol=1e-12)
+    y = rng.standard_normal((10, 16)) * 5
+    np.testing.assert_allclose(oracle.l2_normalize(3.0 * y, eps=0.0), oracle.l2_normalize(y, eps=0.0), rtol=1e-12)
     assert np.all(oracle.l2_normalize(np.zeros((1, 4))) == 0)
 
 
@@ -398,3 +406,45 @@ def test_body_outputs_end_on_the_pair(name):
         lo, hi = int(wl.seg_off[s]), int(wl.seg_off[s + 1])
         q, _, _, _, _ = ref.chain_stream(wl.tok, d["mode"], l, h, np.arange(lo, hi), d.get("conv_k", 0))
         np.testing.assert_allclose(o[-1], S.T @ q[-1], rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [GATED_DELTA, SCALAR_DECAY, DIAG_GATE, KDA])
+def test_body_outputs_brute_force(mode):
+    """Every per-token output of a segment body's first prefill, against
+    dense brute force on a tiny case (d = 4): S_t = A_t S_{t-1} + W_t from
+    S = 0 at the body's first token, o_t = S_t^T q_t.  An off-by-one in which
+    state is dotted with q, a skipped seam offset or a transposed S fails."""
+    from oracle import reference as ref
+    rng = np.random.default_rng(300 + mode)
+    L, H, dk, w = 1, 2, 4, 2
+    lens = [5, 1, 7]
+    N = sum(lens)
+    seg_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tok = {"q": np.zeros((L, N, H, dk)), "k": np.zeros((L, N, H, dk)), "v": np.zeros((L, N, H, dk)),
+           "beta": None, "conv_w": None}
+    per_head = []
+    for h in range(H):
+        q, k, v, a, b = _rand_tokens(rng, N, dk, dk, mode, slow=True)
+        tok["q"][0, :, h], tok["k"][0, :, h], tok["v"][0, :, h] = q, k, v
+        per_head.append((q, k, v, a, b))
+    if mode == SCALAR_DECAY:
+        tok["alpha"] = np.array([[per_head[h][3][0] for h in range(H)]])
+    elif mode in (DIAG_GATE, KDA):
+        tok["alpha"] = np.stack([ph[3] for ph in per_head], axis=1)[None]
+    else:
+        tok["alpha"] = np.stack([ph[3] for ph in per_head], axis=1)[None]
+    if mode in (GATED_DELTA, KDA):
+        tok["beta"] = np.stack([ph[4] for ph in per_head], axis=1)[None]
+    desc = dict(mode=mode, seam_w=w, conv_k=0, conv_act=0)
+    items = [(0, s, h) for s in range(len(lens)) for h in range(H)]
+    outs = ref.body_output_reference(desc, tok, seg_off, items)
+    for (l, s, h), o in zip(items, outs):
+        q, k, v, a, b = per_head[h]
+        lo, hi = int(seg_off[s]), int(seg_off[s + 1])
+        body = range(lo + min(w, hi - lo), hi)
+        assert o.shape == (len(body), dk)
+        S = np.zeros((dk, dk))
+        for i, t in enumerate(body):
+            S = _dense_A(mode, k[t], a[t], None if b is None else b[t]) @ S + \
+                _dense_W(mode, k[t], v[t], None if b is None else b[t])
+            np.testing.assert_allclose(o[i], S.T @ q[t], rtol=0, atol=1e-12)
