@@ -37,6 +37,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 WORKLOAD = "cold_30l"
+# the fp64 oracle's bounded sample, the same in both of its legs (the GPU arm's
+# cpu_baseline and --impl reference): layer 0, every head, the request's first
+# ORACLE_SEGS segments (~19k tokens of the cold prompt, a few seconds per run)
+ORACLE_HEADS, ORACLE_SEGS = 32, 40
 METRIC = "segment-build Mtok/s and compose segs/s per layer, % of roofline (1 GB300)"
 UNIT = "Mtok/s"
 
@@ -200,6 +204,100 @@ def oracle_sample(wl, n_heads, n_segments):
     return dt, layer_tokens
 
 
+def _compose_bytes(wl):
+    """Algorithmic bytes of one compose with fused seams: every entry's pair
+    read (T and S, fp32), each seam token's raw q, k, v (bf16) and gates read
+    and its fp32 outputs written, the final state written."""
+    d = wl.desc
+    L, H, D, w = d["n_layers"], d["n_heads"], d["d_k"], d["seam_w"]
+    n_ord = len(wl.order)
+    pair_bytes = L * n_ord * H * 2 * D * D * 4
+    seam_tok = int(sum(min(w, int(wl.lengths[s])) for s in wl.order))
+    seam_bytes = L * seam_tok * H * (3 * D * 2 + 2 * 2 + D * 4)
+    return pair_bytes, pair_bytes + seam_bytes + L * H * D * D * 4
+
+
+def _config_leg(name, args, peaks, dev, stream):
+    """Build, compose with seams and compose alone on one named workload, each
+    timed with CUDA events over repeated calls (inputs larger than L2)."""
+    import torch
+    from linear_attn_state_chunked_gb300 import hypic, workloads as W
+    wl = W.make(name, device=dev)
+    d = wl.desc
+    L, H, D, w = d["n_layers"], d["n_heads"], d["d_k"], d["seam_w"]
+    n_ord = len(wl.order)
+    tshape, sshape = hypic.pair_shapes(d, wl.n_seg)
+    T = torch.empty(tshape, device=dev)
+    S = torch.empty(sshape, device=dev)
+    Sf = torch.empty((L, H, D, D), device=dev)
+    o = torch.empty((L, n_ord, max(w, 1), H, D), device=dev)
+    wsp = torch.empty(hypic.workspace_size(d), dtype=torch.uint8, device=dev)
+    d0 = dict(d, seam_w=0, conv_k=0)
+    reps = max(3, min(args.steps, 10))
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    build_ms = timed(lambda: hypic.segment_build(d, wl.tok, wl.seg_off, T, S, wsp, stream=stream))
+    comp_ms = timed(lambda: hypic.compose(d, wl.tok, wl.seg_off, wl.order, T, S, Sf, o_out=o, stream=stream))
+    scan_ms = timed(lambda: hypic.compose(d0, wl.tok, wl.seg_off, wl.order, T, S, Sf, stream=stream))
+    hypic.workspace_status(wsp, stream)
+    hypic.async_status(stream)
+    body_tokens = int(sum(max(0, int(x) - min(w, int(x))) for x in wl.lengths))
+    flops = body_tokens * L * H * 4.0 * D * (2 * D)
+    tf32_peak = peaks["bf16_sustained"] * 1.1 / 2.25
+    pair_bytes, comp_bytes = _compose_bytes(wl)
+    out = {
+        "workload": "%s: %d layer(s) x %d heads, d=%d, %d segments (%d tokens), seam w=%d, order %s"
+                    % (name, L, H, D, wl.n_seg, wl.n_tokens, w,
+                       "random" if name == "warm_30l" else "in sequence"),
+        "build": {"ms": build_ms, "mtok_s_per_layer": body_tokens * L / (build_ms * 1e-3) / 1e6,
+                  "tflops": flops / (build_ms * 1e-3) / 1e12,
+                  "frac_tf32": flops / (build_ms * 1e-3) / 1e12 / tf32_peak},
+        "compose_with_seams": {"ms": comp_ms, "segs_s_per_layer": n_ord * L / (comp_ms * 1e-3),
+                               "gbs": comp_bytes / (comp_ms * 1e-3) / 1e9,
+                               "hbm_frac": comp_bytes / (comp_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                               "algorithmic_bytes": comp_bytes},
+        "compose_alone": {"ms": scan_ms, "gbs": pair_bytes / (scan_ms * 1e-3) / 1e9,
+                          "hbm_frac": pair_bytes / (scan_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+    }
+    del T, S, Sf, o, wsp, wl
+    torch.cuda.empty_cache()
+    return out
+
+
+def _q_rows_read(wl):
+    """Token rows of q that the calls read: each request entry's seam tokens
+    and the conv history before them (the previous entries' last conv_k - 1
+    tokens in request order), merged into sorted ranges [r0, r1)."""
+    d = wl.desc
+    w, hist = d["seam_w"], max(0, d.get("conv_k", 0) - 1)
+    off, order = wl.seg_off, [int(x) for x in wl.order]
+    stream = np.concatenate([np.arange(off[s], off[s + 1]) for s in order]) if order else np.zeros(0, np.int64)
+    starts = np.cumsum([0] + [int(off[s + 1] - off[s]) for s in order])
+    rows = set()
+    for e, s in enumerate(order):
+        sw = min(w, int(off[s + 1] - off[s]))
+        lo = max(0, int(starts[e]) - hist)
+        rows.update(int(x) for x in stream[lo:int(starts[e]) + sw])
+    ranges = []
+    for r in sorted(rows):
+        if ranges and ranges[-1][1] == r:
+            ranges[-1][1] = r + 1
+        else:
+            ranges.append([r, r + 1])
+    return [tuple(x) for x in ranges]
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -215,7 +313,7 @@ def run_reference(args):
     from linear_attn_state_chunked_gb300 import workloads as W
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     wl = W.make(WORKLOAD, device=dev, layers=1)
-    heads, segs = 4, 12
+    heads, segs = ORACLE_HEADS, ORACLE_SEGS
     for _ in range(args.warmup):
         oracle_sample(wl, heads, segs)
     tot_t, tot_tok = 0.0, 0.0
@@ -407,7 +505,15 @@ def run_gpu(args):
                 host[key].copy_(v)
         h_Sf = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
         h_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        # q is read only for the seam tokens and their conv history: those rows
+        # alone cross the link (one contiguous copy per layer and range); the
+        # other q rows on the device are poisoned with NaN first, so a kernel
+        # that read them would show in the outputs checked below
+        q_ranges = _q_rows_read(wl)
+        q_rows = sum(r1 - r0 for r0, r1 in q_ranges)
+        wl.tok["q"].fill_(float("nan"))
+        row_bytes = H * D * wl.tok["q"].element_size()
+        h2d = sum(v.numel() * v.element_size() for k_, v in host.items() if k_ != "q") + L * q_rows * row_bytes
         d2h = Sf.numel() * 4 + o.numel() * 4
         n_e2e = max(1, min(args.steps, 3))
         n_groups = min(L, args.e2e_groups)
@@ -424,7 +530,12 @@ def run_gpu(args):
             for (l0, l1) in groups:
                 with torch.cuda.stream(cs_in):
                     for key, hv in host.items():
-                        wl.tok[key][l0:l1].copy_(hv[l0:l1], non_blocking=True)
+                        if key == "q":
+                            for l in range(l0, l1):
+                                for r0, r1 in q_ranges:
+                                    wl.tok["q"][l, r0:r1].copy_(hv[l, r0:r1], non_blocking=True)
+                        else:
+                            wl.tok[key][l0:l1].copy_(hv[l0:l1], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(cs_in)
                 ev_in.append(ev)
@@ -456,21 +567,44 @@ def run_gpu(args):
         e1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = _reduce_max(e0.elapsed_time(e1), ws) / n_e2e
+        # the end-to-end outputs are those of the device-resident step
+        o_dev, Sf_dev = o.clone(), Sf.clone()
+        hypic.segment_build(d, wl.tok, wl.seg_off, T, S, wsp, stream=stream)
+        hypic.compose(d, wl.tok, wl.seg_off, wl.order, T, S, Sf, o_out=o, stream=stream)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(h_o, o.cpu()) and torch.equal(h_Sf, Sf.cpu()) and torch.isfinite(h_o).all()
+                    and torch.isfinite(h_Sf).all())
+        del o_dev, Sf_dev
+        wl.tok["q"].copy_(host["q"])  # the whole q again, for the legs below
         e2e = {"value": tokens * L * ws / (ms_e2e * 1e-3) / 1e6, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": n_e2e, "ms_per_step": ms_e2e,
                "h2d_gbs": h2d / (ms_e2e * 1e-3) / 1e9,
-               "schedule": "%d layer groups; group g+1's inputs copy while group g computes" % len(groups)}
+               "outputs_match_device_step": same,
+               "schedule": "%d layer groups; group g+1's inputs copy while group g computes; k, v, alpha, "
+                           "beta, conv weights whole, q only for the %d rows the seams read (seam tokens and "
+                           "conv history)" % (len(groups), q_rows)}
         del host
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        heads, segs = 32, 120
+        heads, segs = ORACLE_HEADS, ORACLE_SEGS
         dt, lt = oracle_sample(wl, heads, segs)
         cpu = {"value": lt / dt / 1e6, "unit": UNIT, "cores": _cores(), "kind": "oracle",
                "sample": "fp64 oracle on layer 0, all %d heads, first %d segments of the request "
                          "(%d tokens): conv, body pairs, compose, seams; %.1f s"
                          % (heads, segs, int(lt * d["n_heads"] / heads), dt)}
+
+    # the other configurations of the workload set, each on its own after the
+    # cold prompt's tensors are released: the single-layer gated-delta request
+    # (build, compose with seams, compose alone) and the warm-cache 30-layer
+    # request (its pairs built once, then the compose with seams it is about)
+    configs = None
+    if rank == 0 and not args.layers and not args.no_configs:
+        del T, S, Sf, o, wsp, wl
+        torch.cuda.empty_cache()
+        configs = {name: _config_leg(name, args, peaks, dev, stream)
+                   for name in ("gdn_bf16", "warm_30l")}
 
     if rank == 0:
         line = {
@@ -500,6 +634,7 @@ def run_gpu(args):
                 "compose_with_seams": {"segs_s_per_layer": comp_segs, "ms": comp_ms,
                                        "gbs": comp_gbs, "hbm_frac": comp_gbs / peaks["hbm_gbs"],
                                        "launches_per_step": 1}},
+            "configs": configs,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -522,6 +657,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the single-layer gated-delta and warm-cache 30-layer legs")
     ap.add_argument("--e2e-groups", type=int, default=6,
                     help="layer groups of the end-to-end step (copies overlap compute)")
     ap.add_argument("--layers", type=int, default=None,

@@ -43,7 +43,12 @@
  * Conventions shared by every call
  * --------------------------------
  * - All device pointers are caller-owned device memory; the library never
- *   allocates or frees device memory and keeps no device state between calls.
+ *   allocates or frees device memory.  It keeps two kinds of device state,
+ *   both static variables compiled into it (held by every GPU that loads the
+ *   library until exit): one status word per device, into which compose and
+ *   seam-advance kernels report a bounded wait that gave up
+ *   (hypic_async_status), and the scratch block of
+ *   hypic_segment_build_noalloc (hypic_noalloc_status).
  *   Host pointers (segment offsets, request order, descriptors) are read
  *   before the call returns and may be freed afterwards.
  * - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
@@ -83,7 +88,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_ABI_VERSION 3
+#define HYPIC_ABI_VERSION 4
 #define HYPIC_MAX_SEGMENTS 2048
 
 typedef struct CUstream_st *hypic_stream; /* same type as cudaStream_t */
@@ -149,9 +154,9 @@ const char *hypic_last_error(void);
 
 /*
  * Bytes of device workspace hypic_segment_build needs (always > 0, a
- * multiple of 256).  The workspace carries the build's work-queue counter and
- * its device status word; it need not be initialised and may be reused by
- * consecutive calls on one stream.
+ * multiple of 256).  The workspace carries the build's device status word;
+ * it need not be initialised and may be reused by consecutive calls on one
+ * stream.
  */
 size_t hypic_workspace_size(const hypic_desc *desc);
 
@@ -163,6 +168,17 @@ size_t hypic_workspace_size(const hypic_desc *desc);
  * clears the word.
  */
 int hypic_workspace_status(const void *workspace, hypic_stream stream);
+
+/*
+ * Device status of the calls that take no workspace (hypic_compose,
+ * hypic_seam_advance) on the current device: waits for `stream`, then
+ * returns HYPIC_OK, or HYPIC_ERR_TIMEOUT if one of their kernels' bounded
+ * device-side waits gave up since the last query (that call's outputs are
+ * incomplete; the kernel returned instead of hanging), and clears the word.
+ * The word is shared by every such call on the device, whatever the stream:
+ * a give-up is reported to whichever caller queries first.
+ */
+int hypic_async_status(hypic_stream stream);
 
 /*
  * Segment forward: the per-token outputs of every segment body computed from
@@ -195,7 +211,9 @@ int hypic_segment_forward(const hypic_desc *desc, const hypic_tokens *tok,
  * leave as soon as it sees the flag.  hypic_workspace_status then returns
  * HYPIC_ERR_TIMEOUT with status 3 (1: the flag was raised; 2: the second
  * waiter left without the phase completing).  The device stays usable.
- * max_cycles in [1, 2^34]; workspace as for hypic_segment_build.
+ * max_cycles in [1, 2^34]; workspace as for hypic_segment_build, or NULL to
+ * report through (after clearing) the device status word that
+ * hypic_async_status reads.
  */
 int hypic_selftest_bounded_wait(void *workspace, int64_t max_cycles, hypic_stream stream);
 
@@ -238,11 +256,21 @@ int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok,
  * device address (cudaGetSymbolAddress, with that device current); make that
  * first call before any stream capture.  All calls share the block and it
  * keeps the last call's contents (the build clears what must start at zero):
- * calls whose work overlaps on the GPU race on it.  Nothing is allocated.
+ * calls whose work overlaps on the GPU race on it, status word included.
+ * Nothing is allocated.
  */
 int hypic_segment_build_noalloc(const hypic_desc *desc, const hypic_tokens *tok,
                                 const int64_t *seg_off, int32_t n_seg,
                                 float *T_out, float *S_out, hypic_stream stream);
+
+/*
+ * Device status of the last hypic_segment_build_noalloc on the current
+ * device, as hypic_workspace_status reports it for a workspace: waits for
+ * `stream`, then HYPIC_OK or HYPIC_ERR_TIMEOUT (a bounded device-side wait of
+ * that build gave up).  The word lives in the shared static scratch block, so
+ * overlapping no-alloc builds share it too.
+ */
+int hypic_noalloc_status(hypic_stream stream);
 
 /*
  * Compose: the running state of every (layer, head) over the request
@@ -290,7 +318,7 @@ int hypic_compose(const hypic_desc *desc, const hypic_tokens *tok,
  * recurrence up to rounding); the other modes step token by token.  At
  * d = 128 with seam_w <= 8 the kernel is persistent and pipelined; its
  * device-side waits are bounded, and if one gives up the outputs are left
- * incomplete instead of the kernel hanging.
+ * incomplete instead of the kernel hanging and hypic_async_status reports it.
  */
 int hypic_seam_advance(const hypic_desc *desc, const hypic_tokens *tok,
                        const int64_t *seg_off, int32_t n_seg,

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <numeric>
 #include <vector>
 
@@ -153,7 +154,41 @@ int cuda_fail(cudaError_t e, const char *what)
     return fail(HYPIC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// One status word per device for the calls that take no workspace (compose,
+// seam advance): a kernel whose bounded device-side wait gives up ORs 1 into
+// it, and hypic_async_status reads and clears it.  The word is a static device
+// variable (every GPU that loads the library holds it until exit); its device
+// address is looked up once per device, with that device current.
+__device__ int g_async_status;
+constexpr int kMaxDevices = 64;
+std::once_flag g_status_once[kMaxDevices];
+int *g_status_ptr[kMaxDevices];
+cudaError_t g_status_err[kMaxDevices];
+
+int async_status_ptr(int **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(HYPIC_ERR_UNSUPPORTED, "device %d beyond the %d devices served", dev, kMaxDevices);
+    std::call_once(g_status_once[dev], [dev]() {
+        void *p = nullptr;
+        g_status_err[dev] = cudaGetSymbolAddress(&p, g_async_status);
+        g_status_ptr[dev] = static_cast<int *>(p);
+    });
+    if (g_status_err[dev] != cudaSuccess || !g_status_ptr[dev])
+        return cuda_fail(g_status_err[dev], "status word address");
+    *out = g_status_ptr[dev];
+    return HYPIC_OK;
+}
+
 }  // namespace
+
+namespace hypic {
+// The device status word of the current device (api.cu); for selftest.cu.
+int async_status_word(int **out) { return async_status_ptr(out); }
+}  // namespace hypic
 
 namespace hypic {
 int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
@@ -200,7 +235,6 @@ int hypic_segment_build(const hypic_desc *desc, const hypic_tokens *tok, const i
     a.tok = make_tok(tok);
     a.T_out = T_out;
     a.S_out = S_out;
-    a.work_counter = static_cast<unsigned int *>(workspace);
     a.status = reinterpret_cast<int *>(static_cast<char *>(workspace) + 128);
     // Gated delta at d = 128 with bf16 inputs runs on the tensor cores (tf32
     // products, 2e-3 class); everything else, including every fp32-input
@@ -252,6 +286,23 @@ int hypic_workspace_status(const void *workspace, hypic_stream stream)
     return HYPIC_OK;
 }
 
+int hypic_async_status(hypic_stream stream)
+{
+    g_err[0] = 0;
+    int *word = nullptr;
+    int rc;
+    if ((rc = async_status_ptr(&word))) return rc;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (v == 0) return HYPIC_OK;
+    e = cudaMemset(word, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return fail(HYPIC_ERR_TIMEOUT, "a device-side wait of a compose or seam-advance call gave up (status %d)", v);
+}
+
 int hypic_compose(const hypic_desc *desc, const hypic_tokens *tok, const int64_t *seg_off,
                   int32_t n_seg, const int32_t *order, int32_t n_order, const float *T,
                   const float *S, const float *S_init, float *S_prefix_out, float *S_final,
@@ -289,6 +340,7 @@ int hypic_compose(const hypic_desc *desc, const hypic_tokens *tok, const int64_t
     a.S_prefix = S_prefix_out;
     a.S_final = S_final;
     a.o_out = o_out;
+    if ((rc = async_status_ptr(&a.status))) return rc;
     cudaError_t e = launch_compose(a, tab, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "compose launch");
     return HYPIC_OK;
@@ -320,6 +372,7 @@ int hypic_seam_advance(const hypic_desc *desc, const hypic_tokens *tok, const in
     a.S_in = S_in;
     a.o_out = o_out;
     a.S_out = S_out;
+    if ((rc = async_status_ptr(&a.status))) return rc;
     cudaError_t e = launch_seam(a, tab, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "seam advance launch");
     return HYPIC_OK;

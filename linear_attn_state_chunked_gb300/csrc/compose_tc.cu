@@ -94,9 +94,9 @@ enum {
     B_COUNT
 };
 
-__device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
+__device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag, int *status)
 {
-    return tc::wait_bounded(mbar, parity, abort_flag, kWaitCycles);
+    return tc::wait_bounded(mbar, parity, abort_flag, kWaitCycles, status);
 }
 
 struct TokMaps {
@@ -246,7 +246,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             tc::commit(bar(B_SEAMDONE));
         };
         auto issue_body = [&](int e) -> bool {
-            if (!wait_bar(bar(B_FULLT), e & 1, abort_flag)) return false;
+            if (!wait_bar(bar(B_FULLT), e & 1, abort_flag, a.status)) return false;
             tc::fence_after();
             // Y = Xhi T_C^T, i.e. (T_C S)^T
 #pragma unroll 1
@@ -261,7 +261,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
         auto seam_scale = [&](int e, bool &okw) -> float {
             if (w == 0) return 1.f;
             bool wt = true;
-            if (tid == 0) wt = wait_bar(bar(B_STAGED0 + (e & 1)), (e >> 1) & 1, abort_flag);
+            if (tid == 0) wt = wait_bar(bar(B_STAGED0 + (e & 1)), (e >> 1) & 1, abort_flag, a.status);
             okw = tc::bar_and(BAR_STATE, NS, wt);
             return reinterpret_cast<const float *>(sm + SM_BUF + (e & 1) * BUF_BYTES + BF_SMALL)[SMALL_GL];
         };
@@ -311,7 +311,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             bool wt = true;
             if (w > 0) {
                 // ---- seam outputs and the update operand W
-                if (tid == 0) wt = wait_bar(bar(B_SEAMDONE), e & 1, abort_flag);
+                if (tid == 0) wt = wait_bar(bar(B_SEAMDONE), e & 1, abort_flag, a.status);
                 if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
                 tc::fence_after();
                 const float *smf = reinterpret_cast<const float *>(buf + BF_SMALL);
@@ -373,7 +373,7 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
                     }
                 }
                 // ---- Xhi of the state after the seam (operand of the body MMA)
-                if (tid == 0) wt = wait_bar(bar(B_UPDDONE), e & 1, abort_flag);
+                if (tid == 0) wt = wait_bar(bar(B_UPDDONE), e & 1, abort_flag, a.status);
                 if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
                 tc::fence_after();
 #pragma unroll
@@ -394,8 +394,8 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             const float gn = last ? 1.f : seam_scale(e + 1, ok);
             if (!ok) break;
             if (tid == 0 && wt) {
-                wt = wait_bar(bar(B_BODYDONE), e & 1, abort_flag);
-                if (wt) wt = wait_bar(bar(B_FULLSC), e & 1, abort_flag);
+                wt = wait_bar(bar(B_BODYDONE), e & 1, abort_flag, a.status);
+                if (wt) wt = wait_bar(bar(B_FULLSC), e & 1, abort_flag, a.status);
             }
             if (!tc::bar_and(BAR_STATE, NS, wt)) { ok = false; break; }
             tc::fence_after();
@@ -493,8 +493,8 @@ compose_tc_kernel(const __grid_constant__ ComposeArgs a, const __grid_constant__
             gab_next = (e + 1 < n_ent) ? gate(nx1) : 0.f;  // in flight while this entry is staged
             bool wt = true;
             if (c == 0) {
-                if (e >= 2) wt = wait_bar(bar(B_BUFFREE0 + b), ((e - 2) >> 1) & 1, abort_flag);
-                if (wt) wt = wait_bar(bar(B_FULLR0 + b), (e >> 1) & 1, abort_flag);
+                if (e >= 2) wt = wait_bar(bar(B_BUFFREE0 + b), ((e - 2) >> 1) & 1, abort_flag, a.status);
+                if (wt) wt = wait_bar(bar(B_FULLR0 + b), (e >> 1) & 1, abort_flag, a.status);
             }
             if (!tc::bar_and(BAR_STAGE, NG, wt)) { ok = false; break; }
             // ---- conv (along the request stream) and L2 normalisation of q, k

@@ -12,7 +12,6 @@ struct BuildArgs {
     float *T_out;                // may be null (segment forward without the transition product)
     float *S_out;                // may be null (segment forward)
     float *o_out;                // per-token body outputs (segment forward), else null
-    unsigned int *work_counter;  // device, zeroed by the caller's stream before launch
     int *status;                 // device status word (0 = ok)
 };
 
@@ -25,6 +24,7 @@ struct ComposeArgs {
     float *S_prefix;      // may be null
     float *S_final;
     float *o_out;         // may be null when w == 0
+    int *status;          // device word a kernel's bounded wait ORs 1 into when it gives up
 };
 
 struct SeamArgs {
@@ -33,6 +33,7 @@ struct SeamArgs {
     const float *S_in;
     float *o_out;
     float *S_out;  // may be null; may alias S_in
+    int *status;   // device word a kernel's bounded wait ORs 1 into when it gives up
 };
 
 cudaError_t launch_build_rec(const BuildArgs &a, const SegTable &tab, cudaStream_t st);

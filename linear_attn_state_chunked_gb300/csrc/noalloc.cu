@@ -37,18 +37,12 @@ cudaError_t g_scratch_err[kMaxDevices];
 
 }  // namespace
 
-extern "C" int hypic_segment_build_noalloc(const hypic_desc *desc, const hypic_tokens *tok,
-                                           const int64_t *seg_off, int32_t n_seg, float *T_out,
-                                           float *S_out, hypic_stream stream)
+namespace {
+
+// This device's scratch address, looked up on first use (see above).
+int scratch_of_current_device(void **out)
 {
     char msg[256];
-    const size_t need = hypic_workspace_size(desc);
-    if (need > kScratchBytes) {
-        snprintf(msg, sizeof(msg),
-                 "this build needs %zu bytes of scratch; the library's static scratch holds %zu",
-                 need, kScratchBytes);
-        return hypic::report_error(HYPIC_ERR_WORKSPACE, msg);
-    }
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -69,8 +63,38 @@ extern "C" int hypic_segment_build_noalloc(const hypic_desc *desc, const hypic_t
                  cudaGetErrorString(g_scratch_err[dev]));
         return hypic::report_error(HYPIC_ERR_CUDA, msg);
     }
+    *out = g_scratch_ptr[dev];
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+extern "C" int hypic_noalloc_status(hypic_stream stream)
+{
+    void *scratch = nullptr;
+    const int rc = scratch_of_current_device(&scratch);
+    if (rc != HYPIC_OK) return rc;
+    // the scratch is laid out like a build workspace: its status word is the
+    // one hypic_workspace_status reads
+    return hypic_workspace_status(scratch, stream);
+}
+
+extern "C" int hypic_segment_build_noalloc(const hypic_desc *desc, const hypic_tokens *tok,
+                                           const int64_t *seg_off, int32_t n_seg, float *T_out,
+                                           float *S_out, hypic_stream stream)
+{
+    char msg[256];
+    const size_t need = hypic_workspace_size(desc);
+    if (need > kScratchBytes) {
+        snprintf(msg, sizeof(msg),
+                 "this build needs %zu bytes of scratch; the library's static scratch holds %zu",
+                 need, kScratchBytes);
+        return hypic::report_error(HYPIC_ERR_WORKSPACE, msg);
+    }
+    void *scratch = nullptr;
+    const int rc = scratch_of_current_device(&scratch);
+    if (rc != HYPIC_OK) return rc;
     // The build clears what must start at zero (its status word) on `stream`
     // before its kernel runs.
-    return hypic_segment_build(desc, tok, seg_off, n_seg, T_out, S_out, g_scratch_ptr[dev], kScratchBytes,
-                               stream);
+    return hypic_segment_build(desc, tok, seg_off, n_seg, T_out, S_out, scratch, kScratchBytes, stream);
 }

@@ -431,9 +431,9 @@ template <typename Tin> struct Layout {
                   PSCR % 16 == 0 && CSCR % 16 == 0, "alignment");
 };
 
-__device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
+__device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag, int *status)
 {
-    return tc::wait_bounded(mbar, parity, abort_flag, kWaitCycles);
+    return tc::wait_bounded(mbar, parity, abort_flag, kWaitCycles, status);
 }
 
 // Plain (generic-address) read of a staged raw element as fp32.
@@ -524,7 +524,7 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
         int i = 0;
         for (long long u = u_beg; u < u_end; ++u, ++i) {
             const int stg = i & 1;
-            if (i >= 2 && !wait_bar(bar(B_EMPTYS + stg), ((i - 2) >> 1) & 1, abort_flag)) break;
+            if (i >= 2 && !wait_bar(bar(B_EMPTYS + stg), ((i - 2) >> 1) & 1, abort_flag, a.status)) break;
             tc::mbar_arrive_expect_tx(bar(B_FULLS + stg), LY::S_STAGE);
             tc::bulk_load(sb + LY::S + stg * LY::S_STAGE, a.S_in + u * (D * D), LY::S_STAGE, bar(B_FULLS + stg));
             if (u + 2 < u_end) tc::bulk_prefetch_l2(a.S_in + (u + 2) * (D * D), LY::S_STAGE);
@@ -551,7 +551,7 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
         for (long long u = u_beg; u < u_end; ++u, ++i, pc.next(dm, tab.n_perm)) {
             const int stg = i & 1;
             bool ok = true;
-            if (i >= 2 && lane == 0) ok = wait_bar(bar(B_EMPTYR + stg), ((i - 2) >> 1) & 1, abort_flag);
+            if (i >= 2 && lane == 0) ok = wait_bar(bar(B_EMPTYR + stg), ((i - 2) >> 1) & 1, abort_flag, a.status);
             if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
             const int l = pc.l, ent = pc.ent, h = pc.h;
             if (ent != cur_ent) {
@@ -628,8 +628,8 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
             const int stg = i & 1, b = i & 1;
             bool ok = true;
             if (ch == 0) {
-                if (i >= 2) ok = wait_bar(bar(B_PFREE + b), ((i - 2) >> 1) & 1, abort_flag);
-                if (ok) ok = wait_bar(bar(B_FULLR + stg), (i >> 1) & 1, abort_flag);
+                if (i >= 2) ok = wait_bar(bar(B_PFREE + b), ((i - 2) >> 1) & 1, abort_flag, a.status);
+                if (ok) ok = wait_bar(bar(B_FULLR + stg), (i >> 1) & 1, abort_flag, a.status);
             }
             if (!tc::bar_and(BAR_P, NP, ok)) break;
             PrepOut &po = pout(b);
@@ -806,8 +806,8 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
         const int stg = i & 1, b = i & 1;
         bool ok = true;
         if (tid == 0) {
-            ok = wait_bar(bar(B_PREPPED + b), (i >> 1) & 1, abort_flag);
-            if (ok) ok = wait_bar(bar(B_FULLS + stg), (i >> 1) & 1, abort_flag);
+            ok = wait_bar(bar(B_PREPPED + b), (i >> 1) & 1, abort_flag, a.status);
+            if (ok) ok = wait_bar(bar(B_FULLS + stg), (i >> 1) & 1, abort_flag, a.status);
         }
         if (!tc::bar_and(BAR_C, NC, ok)) break;
         const PrepOut &po = pout(b);
@@ -966,13 +966,12 @@ template <typename Tin> cudaError_t launch_d(const SeamArgs &a, const SegTable &
 
 template <typename Tin, int CK> cudaError_t launch_pipe_t(const SeamArgs &a, const SegTable &tab, cudaStream_t st)
 {
-    static int n_sm = 0;
+    // the SM count of the device this launch runs on (a cheap query; nothing is
+    // cached across calls, which may come from several devices and threads)
+    int n_sm = 0, dev = 0;
     cudaError_t err;
-    if (n_sm == 0) {
-        int dev = 0;
-        if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-        if ((err = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-    }
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     const long long units = (long long)tab.n_perm * a.dm.L * a.dm.H;
     if (units == 0) return cudaSuccess;
     auto kern = seam_pipe_kernel<Tin, CK>;

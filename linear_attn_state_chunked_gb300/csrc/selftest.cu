@@ -6,6 +6,7 @@
 
 namespace hypic {
 int report_error(int code, const char *msg);  // api.cu: sets hypic_last_error()
+int async_status_word(int **out);             // api.cu: this device's status word
 }
 
 namespace {
@@ -39,11 +40,19 @@ __global__ void wait_probe_kernel(int *status, long long max_cycles)
 
 extern "C" int hypic_selftest_bounded_wait(void *workspace, int64_t max_cycles, hypic_stream stream)
 {
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
         return hypic::report_error(HYPIC_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
     if (max_cycles < 1 || max_cycles > ((int64_t)1 << 34))
         return hypic::report_error(HYPIC_ERR_SHAPE, "max_cycles out of [1, 2^34]");
-    int *status = reinterpret_cast<int *>(static_cast<char *>(workspace) + 128);
+    // with a workspace: its status word (read by hypic_workspace_status); without:
+    // the device's word that compose and seam advance report to (hypic_async_status)
+    int *status = nullptr;
+    if (workspace) {
+        status = reinterpret_cast<int *>(static_cast<char *>(workspace) + 128);
+    } else {
+        const int rc = hypic::async_status_word(&status);
+        if (rc != HYPIC_OK) return rc;
+    }
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), (cudaStream_t)stream);
     if (e == cudaSuccess) {
         wait_probe_kernel<<<1, 64, 0, (cudaStream_t)stream>>>(status, (long long)max_cycles);

@@ -283,13 +283,14 @@ __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int c0, int c1
 // in which case this thread raises the flag.  Every pipelined kernel waits
 // this way, so that a missing arrival ends the CTA instead of hanging it.
 __device__ __forceinline__ bool wait_bounded(uint32_t mbar, uint32_t parity, volatile int *abort_flag,
-                                             long long max_cycles)
+                                             long long max_cycles, int *status = nullptr)
 {
     const long long t0 = clock64();
     while (!mbar_try(mbar, parity)) {
         if (*abort_flag) return false;
         if (clock64() - t0 > max_cycles) {
             *abort_flag = 1;
+            if (status) atomicOr(status, 1);  // the host reads it after the call
             return false;
         }
     }

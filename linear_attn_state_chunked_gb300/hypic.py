@@ -24,9 +24,9 @@ STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_INVALID_ARG", 2: "HYPIC_ERR_SHAPE", 3: "H
 
 # Every symbol include/hypic.h declares.
 EXPORTS = ("hypic_version", "hypic_last_error", "hypic_workspace_size",
-           "hypic_workspace_status", "hypic_segment_build", "hypic_segment_build_noalloc",
-           "hypic_compose", "hypic_seam_advance", "hypic_selftest_bounded_wait",
-           "hypic_segment_forward")
+           "hypic_workspace_status", "hypic_async_status", "hypic_segment_build",
+           "hypic_segment_build_noalloc", "hypic_noalloc_status", "hypic_compose",
+           "hypic_seam_advance", "hypic_selftest_bounded_wait", "hypic_segment_forward")
 
 
 class HypicError(RuntimeError):
@@ -66,6 +66,10 @@ def lib():
         L.hypic_workspace_size.argtypes = [ctypes.POINTER(Desc)]
         L.hypic_workspace_status.restype = ctypes.c_int
         L.hypic_workspace_status.argtypes = [vp, vp]
+        L.hypic_async_status.restype = ctypes.c_int
+        L.hypic_async_status.argtypes = [vp]
+        L.hypic_noalloc_status.restype = ctypes.c_int
+        L.hypic_noalloc_status.argtypes = [vp]
         L.hypic_selftest_bounded_wait.restype = ctypes.c_int
         L.hypic_selftest_bounded_wait.argtypes = [vp, ctypes.c_int64, vp]
         L.hypic_segment_build.restype = ctypes.c_int
@@ -148,9 +152,23 @@ def workspace_status(workspace, stream=None):
     _check(lib().hypic_workspace_status(_p(workspace), _stream(stream)))
 
 
+def async_status(stream=None):
+    """Raise HypicError(HYPIC_ERR_TIMEOUT) if a device-side wait of a compose or
+    seam-advance call on the current device gave up since the last query
+    (clears the report); waits for the stream."""
+    _check(lib().hypic_async_status(_stream(stream)))
+
+
+def noalloc_status(stream=None):
+    """Raise HypicError(HYPIC_ERR_TIMEOUT) if a device-side wait of the last
+    segment_build_noalloc on the current device gave up; waits for the stream."""
+    _check(lib().hypic_noalloc_status(_stream(stream)))
+
+
 def selftest_bounded_wait(workspace, max_cycles, stream=None):
     """Run the bounded-wait self-test into the workspace status word (read it
-    back with workspace_status, which then raises HYPIC_ERR_TIMEOUT)."""
+    back with workspace_status, which then raises HYPIC_ERR_TIMEOUT); with
+    workspace=None into the device status word that async_status reads."""
     _check(lib().hypic_selftest_bounded_wait(_p(workspace), int(max_cycles), _stream(stream)))
 
 

@@ -40,3 +40,27 @@ def test_bounded_wait_gives_up_and_reports():
     items = [(l, s, h) for l in range(d["n_layers"]) for s in range(wl.n_seg) for h in range(d["n_heads"])]
     check_pairs(wl, out, items, tol_of(d))
     assert torch.equal(out["T"], T) and torch.equal(out["S"], S)
+
+
+def test_async_status_reports_and_clears():
+    """Calls without a workspace (compose, seam advance) report a bounded wait
+    that gave up through the device's status word: the self-test writes into
+    it, the query raises HYPIC_ERR_TIMEOUT once and clears it, and a compose
+    afterwards leaves it clear."""
+    try:  # whatever an earlier call left is reported once and cleared
+        hypic.async_status()
+    except hypic.HypicError:
+        pass
+    try:
+        hypic.async_status()
+    except hypic.HypicError:
+        pytest.fail("the first query did not clear the word")
+    hypic.selftest_bounded_wait(None, 20_000_000)
+    with pytest.raises(hypic.HypicError) as ei:
+        hypic.async_status()
+    assert ei.value.status == 7 and "status 3" in str(ei.value), str(ei.value)
+    hypic.async_status()  # cleared by the query above
+    out = run_pipeline(W.make("stress_tiny", device="cuda", seam_w=8, in_dtype=W.BF16, d_k=128, d_v=128,
+                              n_heads=2, lengths=[64, 9, 40, 64], order=[2, 0, 3, 1]))
+    assert torch.isfinite(out["S_final"]).all()
+    hypic.async_status()

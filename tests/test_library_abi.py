@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(L):
     assert set(syms) == set(hypic.EXPORTS)
     for s in syms:
         assert hasattr(L, s), s
-    assert L.hypic_version() == 3
+    assert L.hypic_version() == 4
     assert b"" == L.hypic_last_error()
 
 
@@ -170,8 +170,8 @@ def test_binding_raises_with_message(L):
 def test_selftest_rejects_bad_arguments(L):
     """Argument checks of the bounded-wait self-test happen on the host,
     before anything is launched (no GPU needed)."""
-    assert L.hypic_selftest_bounded_wait(None, 1000, None) == 5
     assert L.hypic_selftest_bounded_wait(FAKE + 16, 1000, None) == 5
+    assert L.hypic_selftest_bounded_wait(None, 0, None) == 2  # NULL: the device status word
     assert L.hypic_selftest_bounded_wait(FAKE, 0, None) == 2
     assert L.hypic_selftest_bounded_wait(FAKE, (1 << 34) + 1, None) == 2
     assert b"max_cycles" in L.hypic_last_error()

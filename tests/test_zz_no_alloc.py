@@ -46,6 +46,8 @@ def test_noalloc_build_matches_workspace_build_twice():
         ws = torch.empty(hypic.workspace_size(d), dtype=torch.uint8, device="cuda")
         T0, S0 = _pairs(wl, lambda T, S: hypic.segment_build(d, wl.tok, wl.seg_off, T, S, ws))
         T1, S1 = _pairs(wl, lambda T, S: hypic.segment_build_noalloc(d, wl.tok, wl.seg_off, T, S))
+        hypic.noalloc_status()  # raises if a device-side wait of that build gave up
+        hypic.workspace_status(ws)
         assert np.isfinite(T1).all() and np.isfinite(S1).all()
         tol = tol_of(d)
         worst = 0.0
