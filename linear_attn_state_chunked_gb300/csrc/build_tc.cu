@@ -11,12 +11,16 @@
 // (d_k x 2d, T from I and S from 0) advances per chunk as
 //   X <- Gamma_C X + U~^T R,   R = [0 | V] - diag(Gamma) K X,
 //   U~ = (I + L)^{-T} D K      (C x d_k).
-// U~ solves the unit upper triangular system (I + L)^T U~ = D K.  In blocks
-// of 16 tokens, with M_ii = (I + L_ii)^{-1} the inverse of a diagonal block,
-//   U~_i = (D_i M_ii)^T K_i - sum_{j > i} (L_ji M_ii)^T U~_j ,  i = 3, 2, 1, 0,
-// and the columns (channels) of U~ are independent, so each warp of the
-// solve group back-substitutes its own 32 channels with warp-level MMAs and no
-// synchronisation with the others.
+// The decays drop out of the triangular system: entry by entry
+// L^T D = D L''^T with L''_tj = beta_t k_t.k_j (j < t), so
+// (I + L)^T D = D (I + L'')^T and
+//   U~ = D W^T K ,   W = (I + L'')^{-1}  (unit lower triangular, no exponentials).
+// W is built by doubling: the eight 8 x 8 diagonal blocks by forward
+// substitution, then the block rule
+//   [[A, 0], [B, C]]^{-1} = [[A^-1, 0], [-C^-1 B A^-1, C^-1]]
+// at 16, 32 and 64 tokens with warp-level tf32 MMAs.  In 16-token blocks
+//   U~_i = D_i sum_{j >= i} W_ji^T K_j ,
+// ten independent block products per 32-channel slice of U~.
 //
 // Kernel form: X is kept transposed in tensor memory (Xt = X^T, two 128-lane
 // halves: Xt_T = T^T and Xt_S = S^T).  Per chunk
@@ -42,13 +46,15 @@
 //                (operand of the Gram, Pt and the solve) and into bf16 (in
 //                place in the raw ring stage, operand of the correction), and
 //                the chunk's gates;
-//   warps 12-15  solve: L from the Gram, the four 16 x 16 diagonal inverses,
-//                the (L_ji M_ii)^T blocks, and U~ by block back substitution
+//   warps 12-15  solve: L'' from the Gram, W = (I + L'')^{-1}, and U~ = D W^T K
 //                into the 128-byte-swizzled B operand of the Xt update;
-//   warps 0-3    T epilogue: Rt_T, then (after the update) Xt_T scaled by the
-//                next chunk's Gamma_C and its bf16 low part; emits T;
-//   warps 4-7    S epilogue: Rt_S (conv of V in registers) and the Gamma_C
-//                rescale of Xt_S; emits S.
+//   warps 0-7    epilogue, each pass split over two warps per lane quadrant:
+//                Rt_S (conv of V in registers, done before Pt_S is ready) and
+//                the Gamma_C rescale of Xt_S; Rt_T; after the update Xt_T
+//                scaled by the next chunk's Gamma_C and its bf16 low part;
+//                emits T and S;
+//   warp 18      gates: the chunk's cumulative log-gates, decays and beta
+//                factors from alpha and beta (loaded a chunk ahead).
 // Work items arrive longest body first; CTA b takes items b, b + grid, ... --
 // the greedy LPT order of that article's "段并行" section as a single-GPU
 // stand-in for its scatter workers.
@@ -70,9 +76,9 @@ constexpr int RK = 3;    // raw-K ring stages
 constexpr int RV = 2;    // raw-V ring stages
 constexpr int RG = 4;    // gate ring stages
 constexpr int HMAX = 3;  // conv history rows kept per chunk (conv_k <= 4)
-constexpr int NT = 576;  // 18 warps
-constexpr int WARP_MMA = 16, WARP_TMA = 17;
-constexpr int BAR_TEPI = 1, BAR_SEPI = 2, BAR_CONV = 3, BAR_SOLVE = 4;
+constexpr int NT = 608;  // 19 warps
+constexpr int WARP_MMA = 16, WARP_TMA = 17, WARP_GATE = 18;
+constexpr int BAR_EPI = 1, BAR_CONV = 3, BAR_SOLVE = 4;
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds
 // Largest log-decay span g_0 - g_{C-1} of a chunk for which Xt_T is
 // pre-multiplied by Gamma_C (the factors Gamma_t / Gamma_C stay below e^80).
@@ -92,17 +98,19 @@ constexpr uint32_t KR_STAGE = 17408;  // raw K rows [C + 3][128] bf16, then K in
 constexpr uint32_t VR_STAGE = 17152;  // raw V rows [C + 3][128] bf16
 constexpr uint32_t G_STAGE = 2176;    // Gates
 constexpr int LP = C + 4;             // row pitch of L (16-byte rows for ldmatrix)
-constexpr int BP = 20;                // row pitch of the 16 x 16 blocks
-constexpr uint32_t BLK = NB * BP * 4; // bytes of one 16 x 16 block
 constexpr uint32_t SM_KR = 0;
 constexpr uint32_t SM_VR = SM_KR + RK * KR_STAGE;
 constexpr uint32_t SM_GATE = SM_VR + RV * VR_STAGE;
 constexpr uint32_t SM_K32 = (SM_GATE + RG * G_STAGE + 1023) / 1024 * 1024;  // 2 x K [64][128] tf32, sw128
 constexpr uint32_t SM_UT = SM_K32 + 2 * 32768;  // U~^T [128][64] tf32, sw128 (B of the Xt update)
-constexpr uint32_t SM_L = SM_UT + 32768;        // L [64][LP]; upper blocks hold -(L_ji M_ii)^T
-constexpr uint32_t SM_A1 = SM_L + C * LP * 4;   // 4 x (D_i M_ii)^T [16][BP]
-constexpr uint32_t SM_MT = SM_A1 + 4 * BLK;     // 4 x M_ii^T [16][BP]
-constexpr uint32_t SM_WK = SM_MT + 4 * BLK;     // K conv weights of the current item [4 lags][128]
+constexpr uint32_t SM_L = SM_UT + 32768;        // Z [64][LP]: L'' below the diagonal, W^T on and above
+constexpr int TP = 20;                          // row pitch of the 16 x 16 solve tiles
+constexpr int TMP_MROW = 0;                     // 4 x M_q = W_qq row-major [16][TP]
+constexpr int TMP_W32 = TMP_MROW + 4 * 16 * TP; // W_32 row-major [16][TP]
+constexpr int TMP_X = TMP_W32 + 16 * TP;        // 4 x [16][TP] per-warp scratch (G^T, Q, Y^T)
+constexpr int TMP_FLOATS = TMP_X + 4 * 16 * TP;
+constexpr uint32_t SM_TMP = SM_L + C * LP * 4;  // solve tiles
+constexpr uint32_t SM_WK = SM_TMP + TMP_FLOATS * 4;  // K conv weights of the current item [4 lags][128]
 constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 40 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
@@ -110,15 +118,14 @@ constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
 static_assert(KR_STAGE % 1024 == 0 && SM_K32 % 1024 == 0 && SM_UT % 1024 == 0, "tile alignment");
 static_assert((C + HMAX) * D * 2 <= (int)KR_STAGE && (C + HMAX) * D * 2 <= (int)VR_STAGE, "ring stage size");
 static_assert(SM_VR % 128 == 0 && VR_STAGE % 128 == 0, "TMA destination alignment");
-static_assert(SM_L % 16 == 0 && SM_A1 % 16 == 0 && SM_MT % 16 == 0, "ldmatrix row alignment");
+static_assert(SM_L % 16 == 0 && SM_TMP % 16 == 0 && (LP * 4) % 16 == 0 && (TP * 4) % 16 == 0,
+              "ldmatrix and float4 row alignment");
 static_assert(SMEM_DYN <= 232448, "shared memory budget");
 
 struct Gates {
-    float g[C];   // inclusive log-gate sums
-    float eg[C];  // exp(g_t)
+    float eg[C];  // exp(g_t), g_t the inclusive log-gate sum
     float dc[C];  // beta_j exp(g_C - g_j)
     float b[C];   // beta
-    float fb[C];  // beta_j exp(g_m - g_j), g_m = (g_0 + g_C) / 2
     float nrc[C]; // -exp(g_t - g_C) (used when the chunk is pre-scaled)
     float neg[C]; // -exp(g_t)
     int safe;     // g_0 - g_C <= kSpan
@@ -132,7 +139,7 @@ enum {
     B_VRF = B_KRE + RK,   // [RV] raw V stage loaded                    TMA -> S epilogue
     B_VRE = B_VRF + RV,   // [RV] stage free                            S epilogue -> TMA
     B_GF = B_VRE + RV,    // [RG] gates written                         conversion -> solve, epilogues
-    B_GE = B_GF + RG,     // [RG] gates consumed (3 arrivals)           solve, epilogues -> conversion
+    B_GE = B_GF + RG,     // [RG] gates consumed (2 arrivals)           solve, epilogue -> gates
     B_KRDY = B_GE + RG,   // [2] K tf32 + bf16 written                  conversion -> MMA
     B_K32E = B_KRDY + 2,  // [2] K tf32 free (2 arrivals)               MMA, solve -> conversion
     B_GRAMF = B_K32E + 2, // Gram done                                  MMA -> solve
@@ -203,17 +210,12 @@ __device__ __forceinline__ void mma16x8x8(float (&c)[4], const uint32_t (&a)[4],
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Warp-level tf32 MMA operands straight from shared memory (ldmatrix of 8 x 4
+// Warp-level tf32 MMA A operand straight from shared memory (ldmatrix of 8 x 4
 // fp32 tiles: lane 4g + t receives element (g, t) of each tile).
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr) : "memory");
 }
 
 // A fragment of the 16 x 8 tile at (r0, k0) of a row-major fp32 matrix with
@@ -228,7 +230,25 @@ __device__ __forceinline__ void frag_a(uint32_t (&a)[4], uint32_t base, int pitc
 // row-major with the given pitch (row n holds column n of the matrix).
 __device__ __forceinline__ void frag_b(uint32_t (&b)[2], uint32_t base, int pitch, int k0, int n0, int lane)
 {
-    ldsm_x2(b, base + ((n0 + (lane & 7)) * pitch + k0 + ((lane >> 3) & 1) * 4) * 4);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(b[0]), "=r"(b[1])
+                 : "r"(base + ((n0 + (lane & 7)) * pitch + k0 + ((lane >> 3) & 1) * 4) * 4)
+                 : "memory");
+}
+
+// acc (a 16 x 8 accumulator tile) += A B with A the 16 x 16 tile at a (row-major,
+// pitch pa) and B (16 x 8) given transposed: row n of the tile at bt (pitch pb)
+// holds column n of B.  Operands are tf32 values.
+__device__ __forceinline__ void mma_tile(float (&acc)[4], uint32_t a, int pa, uint32_t bt, int pb, int lane)
+{
+    uint32_t af[2][4], bf[2][2];
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        frag_a(af[ks], a, pa, 0, 8 * ks, lane);
+        frag_b(bf[ks], bt, pb, 8 * ks, 0, lane);
+    }
+    mma16x8x8(acc, af[0], bf[0]);
+    mma16x8x8(acc, af[1], bf[1]);
 }
 
 // Cursor over this CTA's chunks (non-empty items only), used by the MMA issuer.
@@ -272,12 +292,13 @@ __device__ __forceinline__ void issue_gram(uint32_t tb, uint32_t sK32)
                    ks > 0);
 }
 
-// Xt_T <- s Xt_T and its truncated-away low part in bf16 (this thread's lane).
-__device__ __forceinline__ void scale_split_xt(uint32_t my, float s)
+// Xt_T <- s Xt_T and its truncated-away low part in bf16, columns c0 .. c0+63
+// of this thread's lane.
+__device__ __forceinline__ void scale_split_xt(uint32_t my, int c0, float s)
 {
     const float2 s2 = make_float2(s, s), m1 = make_float2(-1.f, -1.f);
 #pragma unroll 1
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = c0; cc < c0 + 64; cc += 32) {
         float x[32];
         uint32_t lo[16];
         tc::tmem_ld32(my + TM_XT + cc, x);
@@ -297,12 +318,12 @@ __device__ __forceinline__ void scale_split_xt(uint32_t my, float s)
     }
 }
 
-// 128 consecutive columns of this thread's lane scaled by s.
+// 64 consecutive columns of this thread's lane scaled by s.
 __device__ __forceinline__ void scale_cols(uint32_t taddr, float s)
 {
     const float2 s2 = make_float2(s, s);
 #pragma unroll 1
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = 0; cc < 64; cc += 32) {
         float x[32];
         tc::tmem_ld32(taddr + cc, x);
 #pragma unroll
@@ -343,7 +364,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t cnt = 1;
-            if (i >= B_GE && i < B_GE + RG) cnt = 3;
+            if (i >= B_GE && i < B_GE + RG) cnt = 2;
             if (i >= B_K32E && i < B_K32E + 2) cnt = 2;
             tc::mbar_init(bar(i), cnt);
         }
@@ -471,30 +492,11 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         const int ct = tid - 256;       // 0 .. 127
         const int c0 = lane * 4;        // the 4 channels this thread converts ...
         const int r0 = 16 * (warp - 8); // ... in chunk rows r0 .. r0+15 (one warp per 16 rows)
-        const uint16_t *ap = static_cast<const uint16_t *>(a.tok.alpha);
-        const uint16_t *bp = static_cast<const uint16_t *>(a.tok.beta);
-        // bf16 bits of (alpha, beta) of tokens 2 lane, 2 lane + 1 of a chunk, packed
-        // alpha | beta << 16 (padding: alpha = 1, beta = 0); warp 8 loads them one
-        // chunk ahead so that the global-load latency hides behind a conversion
-        auto load_gates = [&](const Item &itg, int cg, uint32_t (&gv)[2]) {
-            const int ncg = min(C, (int)(itg.n - cg * C));
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int tt = 2 * lane + u;
-                gv[u] = 0x3F80u;
-                if (tt < ncg) {
-                    const size_t gi = gate_index(dm, N, itg.l, itg.b0 + cg * C + tt, itg.h);
-                    gv[u] = static_cast<uint32_t>(ap[gi]) | (static_cast<uint32_t>(bp[gi]) << 16);
-                }
-            }
-        };
-        uint32_t gcur[2] = {0x3F80u, 0x3F80u};
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
             const Item it = decode_item(itx, dm, tab);
             if (it.nch == 0) continue;
-            if (warp == 8 && n == 0) load_gates(it, 0, gcur);
             if (CK > 0) {
                 // K conv weights of this item (the previous chunk's readers
                 // passed the group barrier that ends it); read after the
@@ -512,10 +514,17 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 bool w = true;
                 if (ct == 0) w = wait_bar(bar(B_KRF + n % RK), (n / RK) & 1, abort_flag);
                 if (ct == 32 && n >= 2) w = wait_bar(bar(B_K32E + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
-                if (ct == 64 && n >= RG) w = wait_bar(bar(B_GE + n % RG), ((n / RG) - 1) & 1, abort_flag);
                 if (!tc::bar_and(BAR_CONV, 128, w)) { ok = false; break; }
                 uint8_t *stg = sm + SM_KR + (n % RK) * KR_STAGE;
                 uint8_t *k32 = sm + SM_K32 + (n & 1) * 32768;
+                // K conv weights of this thread's four channels (lag j, channel pairs)
+                float2 w2[CK > 0 ? CK : 1][2];
+#pragma unroll
+                for (int j = 0; j < (CK > 0 ? CK : 1); ++j) {
+                    const float4 wa = *reinterpret_cast<const float4 *>(sm + SM_WK + (j * D + c0) * 4);
+                    w2[j][0] = make_float2(wa.x, wa.y);
+                    w2[j][1] = make_float2(wa.z, wa.w);
+                }
 #pragma unroll 1
                 for (int hf = 0; hf < 4; ++hf) {
                     const int rb = r0 + 4 * hf;
@@ -530,13 +539,6 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             kx[r][1] = make_float2(bf16_lo(u.y), bf16_hi(u.y));
                         }
                     } else {
-                        float2 w2[CK > 0 ? CK : 1][2];
-#pragma unroll
-                        for (int j = 0; j < (CK > 0 ? CK : 1); ++j) {
-                            const float4 wa = *reinterpret_cast<const float4 *>(sm + SM_WK + (j * D + c0) * 4);
-                            w2[j][0] = make_float2(wa.x, wa.y);
-                            w2[j][1] = make_float2(wa.z, wa.w);
-                        }
 #pragma unroll
                         for (int r = 0; r < 4; ++r) kx[r][0] = kx[r][1] = make_float2(0.f, 0.f);
                         // each staged row is unpacked once and feeds every output row that uses it
@@ -593,22 +595,6 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             make_float4(tc::round_tf32(kx[r][0].x), tc::round_tf32(kx[r][0].y),
                                         tc::round_tf32(kx[r][1].x), tc::round_tf32(kx[r][1].y));
                 }
-                uint32_t gnext[2] = {0x3F80u, 0x3F80u};
-                if (warp == 8) {
-                    // the next chunk of this CTA: the next one of this item, else the first
-                    // of the next non-empty item
-                    if (c + 1 < it.nch) {
-                        load_gates(it, c + 1, gnext);
-                    } else {
-                        for (int nx = itx + gridDim.x; nx < n_items; nx += gridDim.x) {
-                            const Item itn = decode_item(nx, dm, tab);
-                            if (itn.nch > 0) {
-                                load_gates(itn, 0, gnext);
-                                break;
-                            }
-                        }
-                    }
-                }
                 tc::bar_sync(BAR_CONV, 128);  // every raw row of the stage has been read
                 // K in bf16, in place over the raw rows: bf16 of the tf32 values just
                 // written (the correction product it feeds is ~2^-11 of Pt_T, so the
@@ -622,54 +608,108 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
                 }
                 tc::fence_async_smem();
-                if (warp == 8) {
-                    Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (n % RG) * G_STAGE);
-                    const float al0 = __uint_as_float(gcur[0] << 16), al1 = __uint_as_float(gcur[1] << 16);
-                    const float be[2] = {__uint_as_float(gcur[0] & 0xffff0000u), __uint_as_float(gcur[1] & 0xffff0000u)};
-                    const float x0 = fmaxf(logf(al0), -88.f);  // alpha = 0 -> exp(-88)
-                    const float x1 = fmaxf(logf(al1), -88.f);
-                    float sum = x0 + x1;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, sum, o);
-                        if (lane >= o) sum += y;
-                    }
-                    const float total = __shfl_sync(0xffffffffu, sum, 31);
-                    const float first = __shfl_sync(0xffffffffu, x0, 0);
-                    const float g1 = sum, g0 = sum - x1;
-                    const float gm = 0.5f * (first + total);
-                    G.g[2 * lane] = g0;
-                    G.g[2 * lane + 1] = g1;
-                    G.eg[2 * lane] = expf(g0);
-                    G.eg[2 * lane + 1] = expf(g1);
-                    G.b[2 * lane] = be[0];
-                    G.b[2 * lane + 1] = be[1];
-                    G.dc[2 * lane] = be[0] * expf(total - g0);
-                    G.dc[2 * lane + 1] = be[1] * expf(total - g1);
-                    G.fb[2 * lane] = be[0] * __expf(fmaxf(gm - g0, -87.f));
-                    G.fb[2 * lane + 1] = be[1] * __expf(fmaxf(gm - g1, -87.f));
-                    *reinterpret_cast<float2 *>(&G.nrc[2 * lane]) =
-                        make_float2(-expf(fminf(g0 - total, 88.f)), -expf(fminf(g1 - total, 88.f)));
-                    *reinterpret_cast<float2 *>(&G.neg[2 * lane]) = make_float2(-expf(g0), -expf(g1));
-                    if (lane == 0) G.safe = (first - total <= kSpan) ? 1 : 0;
-                }
                 tc::bar_sync(BAR_CONV, 128);
-                if (ct == 0) {
-                    tc::mbar_arrive(bar(B_KRDY + (n & 1)));
-                    tc::mbar_arrive(bar(B_GF + n % RG));
+                if (ct == 0) tc::mbar_arrive(bar(B_KRDY + (n & 1)));
+            }
+        }
+    } else if (warp == WARP_GATE) {
+        // ------------------------------------------------------------ gates
+        // The chunk's gates from alpha and beta (lane: tokens 2 lane, 2 lane + 1).
+        // The bf16 bits of the next chunk's alpha and beta are loaded while
+        // this chunk's are turned into gates (padding: alpha = 1, beta = 0).
+        const uint16_t *ap = static_cast<const uint16_t *>(a.tok.alpha);
+        const uint16_t *bp = static_cast<const uint16_t *>(a.tok.beta);
+        auto load_raw = [&](const Item &itg, int cg, uint32_t (&ra)[2], uint32_t (&rb)[2]) {
+            const int ncg = min(C, (int)(itg.n - cg * C));
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int tt = 2 * lane + u;
+                ra[u] = 0x3F80u;
+                rb[u] = 0u;
+                if (tt < ncg) {
+                    const size_t gi = gate_index(dm, N, itg.l, itg.b0 + cg * C + tt, itg.h);
+                    ra[u] = ap[gi];
+                    rb[u] = bp[gi];
                 }
-                gcur[0] = gnext[0];
-                gcur[1] = gnext[1];
+            }
+        };
+        uint32_t ca[2] = {0x3F80u, 0x3F80u}, cb[2] = {0u, 0u};
+        bool first = true;
+        int n = 0;
+        bool ok = true;
+        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
+            const Item it = decode_item(itx, dm, tab);
+            if (it.nch == 0) continue;
+            if (first) {
+                load_raw(it, 0, ca, cb);
+                first = false;
+            }
+            for (int c = 0; c < it.nch; ++c, ++n) {
+                // the next chunk of this CTA: the next one of this item, else the
+                // first of the next non-empty item
+                uint32_t na[2] = {0x3F80u, 0x3F80u}, nb[2] = {0u, 0u};
+                if (c + 1 < it.nch) {
+                    load_raw(it, c + 1, na, nb);
+                } else {
+                    for (int nx = itx + gridDim.x; nx < n_items; nx += gridDim.x) {
+                        const Item itn = decode_item(nx, dm, tab);
+                        if (itn.nch > 0) {
+                            load_raw(itn, 0, na, nb);
+                            break;
+                        }
+                    }
+                }
+                if (n >= RG && !wait_bar(bar(B_GE + n % RG), ((n / RG) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                Gates &G = *reinterpret_cast<Gates *>(sm + SM_GATE + (n % RG) * G_STAGE);
+                const float al0 = __uint_as_float(ca[0] << 16), al1 = __uint_as_float(ca[1] << 16);
+                const float be[2] = {__uint_as_float(cb[0] << 16), __uint_as_float(cb[1] << 16)};
+                const float x0 = fmaxf(logf(al0), -88.f);  // alpha = 0 -> exp(-88)
+                const float x1 = fmaxf(logf(al1), -88.f);
+                float sum = x0 + x1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, sum, o);
+                    if (lane >= o) sum += y;
+                }
+                const float total = __shfl_sync(0xffffffffu, sum, 31);
+                const float first_g = __shfl_sync(0xffffffffu, x0, 0);
+                const float g1 = sum, g0 = sum - x1;
+                G.eg[2 * lane] = expf(g0);
+                G.eg[2 * lane + 1] = expf(g1);
+                G.b[2 * lane] = be[0];
+                G.b[2 * lane + 1] = be[1];
+                G.dc[2 * lane] = be[0] * expf(total - g0);
+                G.dc[2 * lane + 1] = be[1] * expf(total - g1);
+                *reinterpret_cast<float2 *>(&G.nrc[2 * lane]) =
+                    make_float2(-expf(fminf(g0 - total, 88.f)), -expf(fminf(g1 - total, 88.f)));
+                *reinterpret_cast<float2 *>(&G.neg[2 * lane]) = make_float2(-expf(g0), -expf(g1));
+                if (lane == 0) G.safe = (first_g - total <= kSpan) ? 1 : 0;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(B_GF + n % RG));
+                ca[0] = na[0];
+                ca[1] = na[1];
+                cb[0] = nb[0];
+                cb[1] = nb[1];
             }
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ solve
         const int sp = tid - 384;  // 0 .. 127
-        const int q = warp & 3;    // lane quadrant; diagonal block; channels 32q .. 32q+31
+        const int q = warp & 3;    // lane quadrant; 16-token block; channels 32q .. 32q+31
         const int g = lane >> 2, t4 = lane & 3;
-        float *Ls = reinterpret_cast<float *>(sm + SM_L);
-        const uint32_t sL = s_base + SM_L, sA1 = s_base + SM_A1, sMT = s_base + SM_MT, sUT = s_base + SM_UT;
-        uint8_t *ut = sm + SM_UT;
+        // Z: L'' strictly below the diagonal, W^T on and above it (tf32 values)
+        float *Z = reinterpret_cast<float *>(sm + SM_L);
+        float *tmp = reinterpret_cast<float *>(sm + SM_TMP);
+        const uint32_t sZ = s_base + SM_L, sT = s_base + SM_TMP;
+        // byte address of element (r, c) of Z and of a solve tile
+        auto zaddr = [&](int r, int c) { return sZ + static_cast<uint32_t>((r * LP + c) * 4); };
+        auto taddr = [&](int t0, int r, int c) { return sT + static_cast<uint32_t>((t0 + r * TP + c) * 4); };
+        // the upper-right 8 x 8 of each row-major M_q is zero
+        for (int e = sp; e < 4 * 64; e += 128)
+            tmp[TMP_MROW + (e >> 6) * 16 * TP + ((e >> 3) & 7) * TP + 8 + (e & 7)] = 0.f;
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
@@ -682,113 +722,179 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 tc::fence_after();
                 const Gates &G = gates(n);
                 {
-                    // L from the Gram rows: row 16q + i sits in lane 32q + i (i < 16);
-                    // lanes 0-15 take its columns 0-31, lanes 16-31 columns 32-63
+                    // L''_tj = beta_t k_t.k_j from the Gram rows: row 16q + i sits in lane
+                    // 32q + i (i < 16); lanes 0-15 take its columns 0-31, lanes 16-31
+                    // columns 32-63.  Entries on and above the diagonal are overwritten
+                    // by W^T before anything reads them.
                     float gr[32];
                     tc::tmem_ld16x2_32(my + TM_G, gr);
                     const int t = 16 * q + (lane & 15);
                     const int j0 = (lane >= 16) ? 32 : 0;
-                    const float gt_t = G.g[t];
-                    if (G.safe) {
-                        // exp(g_t - g_j) = exp(g_t - g_m) exp(g_m - g_j), g_m the chunk midpoint:
-                        // both factors stay within e^{+-40}, one exp per row
-                        const float gm = 0.5f * (G.g[0] + G.g[C - 1]);
-                        const float et = __expf(gt_t - gm);
-                        const float2 e2 = make_float2(et, et);
-                        const float2 *fb2 = reinterpret_cast<const float2 *>(G.fb + j0);
-                        // entries on and above the diagonal are never read (the inverses use
-                        // the strictly lower part; the upper blocks are overwritten below), so
-                        // they are written unmasked: finite, as both factors are bounded
+                    const float2 b2 = make_float2(G.b[t], G.b[t]);
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            const float2 v = __fmul2_rn(__fmul2_rn(fb2[j / 2], e2), make_float2(gr[j], gr[j + 1]));
-                            gr[j] = tc::round_tf32(v.x);
-                            gr[j + 1] = tc::round_tf32(v.y);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            gr[j] = (j0 + j < t) ? tc::round_tf32(G.b[j0 + j] * __expf(gt_t - G.g[j0 + j]) * gr[j])
-                                                 : 0.f;
+                    for (int j = 0; j < 32; j += 2) {
+                        const float2 v = __fmul2_rn(b2, make_float2(gr[j], gr[j + 1]));
+                        gr[j] = tc::round_tf32(v.x);
+                        gr[j + 1] = tc::round_tf32(v.y);
                     }
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(Ls + t * LP + j0 + j) = make_float4(gr[j], gr[j + 1], gr[j + 2], gr[j + 3]);
+                        *reinterpret_cast<float4 *>(Z + t * LP + j0 + j) = make_float4(gr[j], gr[j + 1], gr[j + 2], gr[j + 3]);
                 }
                 tc::fence_before();
                 tc::bar_sync(BAR_SOLVE, 128);
                 if (sp == 0) tc::mbar_arrive(bar(B_GRAME));
-                if (lane < NB) {
-                    // column `lane` of M_qq = (I + L_qq)^{-1} by forward substitution
-                    const float *Lb = Ls + (NB * q) * LP + NB * q;
-                    float x[NB];
+                if (lane < 16) {
+                    // column j of the 8 x 8 diagonal block E_b = (I + L''_bb)^{-1}, b = 2q + lane / 8,
+                    // by forward substitution; column r of L''_bb is loaded one step ahead
+                    const int hb = lane >> 3, base = 16 * q + 8 * hb, j = lane & 7;
+                    const float *Lb = Z + base * LP + base;
+                    float x[8];
 #pragma unroll
-                    for (int r = 0; r < NB; ++r) x[r] = (r == lane) ? 1.f : 0.f;
-                    // column r of L_qq is loaded one step ahead of its use
-                    float col[NB - 1];
+                    for (int r = 0; r < 8; ++r) x[r] = (r == j) ? 1.f : 0.f;
+                    float col[7];
 #pragma unroll
-                    for (int k = 0; k < NB - 1; ++k) col[k] = Lb[(k + 1) * LP];
+                    for (int k = 0; k < 7; ++k) col[k] = Lb[(k + 1) * LP];
 #pragma unroll
-                    for (int r = 0; r < NB - 1; ++r) {
-                        float nxt[NB - 1];
+                    for (int r = 0; r < 7; ++r) {
+                        float nxt[6];
 #pragma unroll
-                        for (int k = 0; k < NB - 2 - r; ++k) nxt[k] = Lb[(r + 2 + k) * LP + r + 1];
+                        for (int k = 0; k < 6 - r; ++k) nxt[k] = Lb[(r + 2 + k) * LP + r + 1];
                         asm volatile("" ::: "memory");  // issue them before this step's products
 #pragma unroll
-                        for (int k = 0; k < NB - 1 - r; ++k) x[r + 1 + k] = fmaf(-col[k], x[r], x[r + 1 + k]);
+                        for (int k = 0; k < 7 - r; ++k) x[r + 1 + k] = fmaf(-col[k], x[r], x[r + 1 + k]);
 #pragma unroll
-                        for (int k = 0; k < NB - 2 - r; ++k) col[k] = nxt[k];
+                        for (int k = 0; k < 6 - r; ++k) col[k] = nxt[k];
                     }
-                    // M^T row `lane` = column `lane` of M; (D M)^T row `lane` = d_k M[k][lane]
-                    float *mt = reinterpret_cast<float *>(sm + SM_MT + q * BLK) + lane * BP;
-                    float *a1 = reinterpret_cast<float *>(sm + SM_A1 + q * BLK) + lane * BP;
 #pragma unroll
-                    for (int k = 0; k < NB; k += 4) {
-                        *reinterpret_cast<float4 *>(mt + k) =
-                            make_float4(tc::round_tf32(x[k]), tc::round_tf32(x[k + 1]), tc::round_tf32(x[k + 2]),
-                                        tc::round_tf32(x[k + 3]));
-                        *reinterpret_cast<float4 *>(a1 + k) = make_float4(
-                            tc::round_tf32(G.dc[NB * q + k] * x[k]), tc::round_tf32(G.dc[NB * q + k + 1] * x[k + 1]),
-                            tc::round_tf32(G.dc[NB * q + k + 2] * x[k + 2]),
-                            tc::round_tf32(G.dc[NB * q + k + 3] * x[k + 3]));
+                    for (int k = 0; k < 8; ++k) x[k] = tc::round_tf32(x[k]);
+                    __syncwarp(0x0000ffffu);  // every read of L''_bb is done
+                    // row j of E_b^T into Z (its strictly lower part, zero, replaces the
+                    // consumed L''_bb) and column j of E_b into the row-major M_q
+                    float *wr = Z + (base + j) * LP + base;
+                    *reinterpret_cast<float4 *>(wr) = make_float4(x[0], x[1], x[2], x[3]);
+                    *reinterpret_cast<float4 *>(wr + 4) = make_float4(x[4], x[5], x[6], x[7]);
+                    float *mr = tmp + TMP_MROW + q * 16 * TP + (8 * hb) * TP + 8 * hb + j;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mr[k * TP] = x[k];
+                }
+                __syncwarp();
+                {
+                    // M_q = (I + L''_qq)^{-1}: its lower-left 8 x 8 F = -E_{2q+1} L''_{2q+1,2q} E_{2q}
+                    // (lane: row r, columns c0, c0 + 1), in fp32
+                    const int r = lane >> 2, c0 = 2 * (lane & 3), b0 = 16 * q;
+                    const float *lrow = Z + (b0 + 8 + r) * LP + b0;
+                    const float4 la = *reinterpret_cast<const float4 *>(lrow);
+                    const float4 lb = *reinterpret_cast<const float4 *>(lrow + 4);
+                    float *gt = tmp + TMP_X + q * 64;  // G^T [8][8], G = L''_{2q+1,2q} E_{2q}
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float *ec = Z + (b0 + c0 + u) * LP + b0;  // column c0 + u of E_{2q}
+                        const float4 ea = *reinterpret_cast<const float4 *>(ec);
+                        const float4 eb = *reinterpret_cast<const float4 *>(ec + 4);
+                        float gv = la.x * ea.x;
+                        gv = fmaf(la.y, ea.y, gv);
+                        gv = fmaf(la.z, ea.z, gv);
+                        gv = fmaf(la.w, ea.w, gv);
+                        gv = fmaf(lb.x, eb.x, gv);
+                        gv = fmaf(lb.y, eb.y, gv);
+                        gv = fmaf(lb.z, eb.z, gv);
+                        gv = fmaf(lb.w, eb.w, gv);
+                        gt[(c0 + u) * 8 + r] = gv;
+                    }
+                    __syncwarp();
+                    float er[8];  // row r of E_{2q+1}
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) er[k] = Z[(b0 + 8 + k) * LP + b0 + 8 + r];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float4 ga = *reinterpret_cast<const float4 *>(gt + (c0 + u) * 8);
+                        const float4 gb = *reinterpret_cast<const float4 *>(gt + (c0 + u) * 8 + 4);
+                        float f = er[0] * ga.x;
+                        f = fmaf(er[1], ga.y, f);
+                        f = fmaf(er[2], ga.z, f);
+                        f = fmaf(er[3], ga.w, f);
+                        f = fmaf(er[4], gb.x, f);
+                        f = fmaf(er[5], gb.y, f);
+                        f = fmaf(er[6], gb.z, f);
+                        f = fmaf(er[7], gb.w, f);
+                        f = tc::round_tf32(-f);
+                        Z[(b0 + c0 + u) * LP + b0 + 8 + r] = f;  // W^T[b0 + c][b0 + 8 + r]
+                        tmp[TMP_MROW + q * 16 * TP + (8 + r) * TP + c0 + u] = f;
+                        Z[(b0 + 8 + r) * LP + b0 + c0 + u] = 0.f;  // upper-right 8 x 8 of M_q
                     }
                 }
                 tc::bar_sync(BAR_SOLVE, 128);
                 {
-                    // -(L_ji M_ii)^T for j > i into the upper block (i, j) of L
-                    // (pairs (1,0) (2,0) (3,0) (2,1) (3,1) (3,2); warp q takes q and q + 4)
-#pragma unroll 1
-                    for (int pi = q; pi < 6; pi += 4) {
-                        const int jj = pi < 3 ? pi + 1 : (pi < 5 ? pi - 1 : 3);
-                        const int ii = pi < 3 ? 0 : (pi < 5 ? 1 : 2);
+                    // 32-token blocks, transposed: W_ji^T = -(M_i^T L''_ji^T) M_j^T for
+                    // (j, i) = (1, 0), (3, 2); warp: pair w / 2, output columns 8 (w % 2) ..
+                    const int jb = (q >> 1) ? 3 : 1, ib = jb - 1, nt = q & 1;
+                    const int xq = TMP_X + q * 16 * TP;  // Q = M_i^T L''_ji^T, row-major
 #pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            float cc[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int qt = 0; qt < 2; ++qt) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_tile(acc, zaddr(16 * ib, 16 * ib), LP, zaddr(16 * jb + 8 * qt, 16 * ib), LP, lane);
+                        tmp[xq + g * TP + 8 * qt + 2 * t4] = tc::round_tf32(acc[0]);
+                        tmp[xq + g * TP + 8 * qt + 2 * t4 + 1] = tc::round_tf32(acc[1]);
+                        tmp[xq + (g + 8) * TP + 8 * qt + 2 * t4] = tc::round_tf32(acc[2]);
+                        tmp[xq + (g + 8) * TP + 8 * qt + 2 * t4 + 1] = tc::round_tf32(acc[3]);
+                    }
+                    __syncwarp();
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_tile(acc, taddr(xq, 0, 0), TP, taddr(TMP_MROW + jb * 16 * TP, 8 * nt, 0), TP, lane);
+                    const int cc = 16 * jb + 8 * nt + 2 * t4;
 #pragma unroll
-                            for (int ks = 0; ks < 2; ++ks) {
-                                uint32_t af[4], bf[2];
-                                frag_a(af, sL, LP, NB * jj, NB * ii + 8 * ks, lane);
-                                frag_b(bf, sMT + ii * BLK, BP, 8 * ks, 8 * nt, lane);
-                                mma16x8x8(cc, af, bf);
-                            }
-                            const int nn = NB * ii + 8 * nt + 2 * t4, rr = NB * jj + g;
-                            Ls[nn * LP + rr] = tc::round_tf32(-cc[0]);
-                            Ls[(nn + 1) * LP + rr] = tc::round_tf32(-cc[1]);
-                            Ls[nn * LP + rr + 8] = tc::round_tf32(-cc[2]);
-                            Ls[(nn + 1) * LP + rr + 8] = tc::round_tf32(-cc[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float v = tc::round_tf32(-acc[e]);
+                        const int rr = g + 8 * (e >> 1), ce = cc + (e & 1);
+                        Z[(16 * ib + rr) * LP + ce] = v;
+                        if (jb == 3) tmp[TMP_W32 + (ce - 48) * TP + rr] = v;  // W_32 row-major
+                    }
+                }
+                tc::bar_sync(BAR_SOLVE, 128);
+                {
+                    // 64 tokens: Y^T = W_a^T L''_ba^T (warp: block (w / 2, w % 2) of Y, transposed)
+                    const int yr = q >> 1, yc = q & 1;
+                    const int yq = TMP_X + q * 16 * TP;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int kb = yc; kb < 2; ++kb)
+                            mma_tile(acc, zaddr(16 * yc, 16 * kb), LP, zaddr(16 * (2 + yr) + 8 * nt, 16 * kb), LP, lane);
+                        tmp[yq + g * TP + 8 * nt + 2 * t4] = tc::round_tf32(acc[0]);
+                        tmp[yq + g * TP + 8 * nt + 2 * t4 + 1] = tc::round_tf32(acc[1]);
+                        tmp[yq + (g + 8) * TP + 8 * nt + 2 * t4] = tc::round_tf32(acc[2]);
+                        tmp[yq + (g + 8) * TP + 8 * nt + 2 * t4 + 1] = tc::round_tf32(acc[3]);
+                    }
+                }
+                tc::bar_sync(BAR_SOLVE, 128);
+                {
+                    // W_ba^T = -Y^T W_b^T (warp: block (2 + w / 2, w % 2) of W, transposed)
+                    const int wr = 2 + (q >> 1), wc = q & 1;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int kb = 2; kb <= wr; ++kb) {
+                            const int yt = TMP_X + ((kb - 2) * 2 + wc) * 16 * TP;
+                            const int wt = (kb == wr) ? TMP_MROW + wr * 16 * TP : TMP_W32;
+                            mma_tile(acc, taddr(yt, 0, 0), TP, taddr(wt, 8 * nt, 0), TP, lane);
                         }
+                        const int cc = 16 * wr + 8 * nt + 2 * t4;
+                        Z[(16 * wc + g) * LP + cc] = tc::round_tf32(-acc[0]);
+                        Z[(16 * wc + g) * LP + cc + 1] = tc::round_tf32(-acc[1]);
+                        Z[(16 * wc + g + 8) * LP + cc] = tc::round_tf32(-acc[2]);
+                        Z[(16 * wc + g + 8) * LP + cc + 1] = tc::round_tf32(-acc[3]);
                     }
                 }
                 w = true;
                 if (sp == 0 && n > 0) w = wait_bar(bar(B_UTE), (n - 1) & 1, abort_flag);  // U~^T free
                 if (!tc::bar_and(BAR_SOLVE, 128, w)) { ok = false; break; }
                 {
-                    // U~ for channels 32q .. 32q+31, token blocks 3, 2, 1, 0.  The swizzled
-                    // offsets below are those of tc::sw128_f32 with the block-dependent
-                    // terms split off (token blocks are multiples of 8 rows / 16 columns).
+                    // U~_i = D_i sum_{j >= i} W_ji^T K_j for channels 32q .. 32q+31.  The swizzled
+                    // offsets below are those of tc::sw128_f32 with the block-dependent terms
+                    // split off (token blocks are multiples of 8 rows / 16 columns).
                     const uint32_t k32 = s_base + SM_K32 + (n & 1) * 32768;
-                    const int h = (lane >> 3) & 1, l7 = lane & 7;
-                    // B of the K_i product: K[16 i + 8 ks + t4 (+4)][32 q + 8 nt + g]
+                    // B of the K_j product: K[16 j + 8 ks + t4 (+4)][32 q + 8 nt + g]
                     uint32_t kofs[4][2];
 #pragma unroll
                     for (int nt = 0; nt < 4; ++nt)
@@ -796,12 +902,6 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         for (int bb = 0; bb < 2; ++bb)
                             kofs[nt][bb] = q * 8192 + (t4 + 4 * bb) * 128 +
                                            ((((2 * nt + (g >> 2)) ^ (t4 + 4 * bb)) << 4) + (g & 3) * 4);
-                    // B of the U~_j products (ldmatrix rows = channels): swizzle of column
-                    // group 4 (j & 1) + 2 ks + h
-                    uint32_t sx[4];
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) sx[v] = (((2 * v + h) ^ l7) << 4);
-                    const uint32_t ubase = sUT + (32 * q + l7) * 128;
                     // C stores: element e = (channel + (e & 1), token + 8 (e >> 1))
                     uint32_t so[2][4];
 #pragma unroll
@@ -811,50 +911,41 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             so[i1][e] = (e & 1) * 128 +
                                         ((((4 * i1 + (g >> 2) + 2 * (e >> 1)) ^ (2 * t4 + (e & 1))) << 4) + (g & 3) * 4);
                     const uint32_t sbase = SM_UT + (32 * q + 2 * t4) * 128;
-                    const uint32_t a1row = (((lane & 7) + h * 8) * BP + (lane >> 4) * 4) * 4;
-                    const uint32_t lrow = (((lane & 7) + h * 8) * LP + (lane >> 4) * 4) * 4;
+                    const uint32_t zrow = (((lane & 7) + ((lane >> 3) & 1) * 8) * LP + (lane >> 4) * 4) * 4;
 #pragma unroll 1
-                    for (int i = 3; i >= 0; --i) {
+                    for (int i = 0; i < 4; ++i) {
                         float acc[4][4];
 #pragma unroll
                         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            uint32_t af[4];
-                            ldsm_x4(af, sA1 + i * BLK + a1row + ks * 32);
-                            const uint32_t kb = k32 + (NB * i + 8 * ks) * 128;
-#pragma unroll
-                            for (int nt = 0; nt < 4; ++nt) {
-                                uint32_t bf[2];
-                                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[0]) : "r"(kb + kofs[nt][0]));
-                                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[1]) : "r"(kb + kofs[nt][1]));
-                                mma16x8x8(acc[nt], af, bf);
-                            }
-                        }
 #pragma unroll 1
-                        for (int j = i + 1; j < 4; ++j)
+                        for (int j = i; j < 4; ++j) {
+                            // every operand of the term first, then its eight MMAs
+                            uint32_t af[2][4], bf[2][4][2];
 #pragma unroll
                             for (int ks = 0; ks < 2; ++ks) {
-                                uint32_t af[4];
-                                ldsm_x4(af, sL + (NB * i * LP + NB * j + 8 * ks) * 4 + lrow);
-                                const uint32_t ub = ubase + (j >> 1) * 16384 + ((j & 1) ? sx[2 + ks] : sx[ks]);
+                                ldsm_x4(af[ks], sZ + ((NB * i) * LP + NB * j + 8 * ks) * 4 + zrow);
+                                const uint32_t kb = k32 + (NB * j + 8 * ks) * 128;
 #pragma unroll
                                 for (int nt = 0; nt < 4; ++nt) {
-                                    uint32_t bf[2];
-                                    ldsm_x2(bf, ub + nt * 1024);
-                                    mma16x8x8(acc[nt], af, bf);
+                                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[ks][nt][0]) : "r"(kb + kofs[nt][0]));
+                                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[ks][nt][1]) : "r"(kb + kofs[nt][1]));
                                 }
                             }
+#pragma unroll
+                            for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                                for (int nt = 0; nt < 4; ++nt) mma16x8x8(acc[nt], af[ks], bf[ks][nt]);
+                        }
                         uint8_t *ub = sm + sbase + (i >> 1) * 16384;
+                        const float dd[2] = {G.dc[NB * i + g], G.dc[NB * i + g + 8]};
 #pragma unroll
                         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
                                 *reinterpret_cast<float *>(ub + nt * 1024 + ((i & 1) ? so[1][e] : so[0][e])) =
-                                    tc::round_tf32(acc[nt][e]);
-                        __syncwarp();
+                                    tc::round_tf32(acc[nt][e] * dd[e >> 1]);
                     }
                 }
                 tc::fence_async_smem();
@@ -866,29 +957,46 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 }
             }
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ T epilogue (warps 0-3)
-        const int m = tid;  // row of Xt_T / Pt_T = tensor-memory lane = column m of T
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 0-7)
+        // Warp w works on tensor-memory lane quadrant w % 4 -- lane m is row m of Xt_T,
+        // Pt_T, Xt_S and Pt_S: column m of T and of S, value channel m -- and on half
+        // h = w / 4 of every pass: tokens 32h .. 32h+31 of Rt_S and Rt_T, columns
+        // 64h .. 64h+63 of Xt_T and Xt_S.
+        const int m = (warp & 3) * 32 + lane;
+        const int et = tid;              // 0 .. 255
+        const int pc = 32 * (warp >> 2); // Pt columns (tokens) of this thread
+        const int xc = 64 * (warp >> 2); // Xt columns of this thread
+        float wvr[CK > 0 ? CK : 1];
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
             const Item it = decode_item(itx, dm, tab);
             const size_t pair = ((size_t)it.l * tab.n_seg + it.s) * dm.H + it.h;
             float *To = a.T_out + pair * D * D + m;
+            float *So = a.S_out + pair * D * D + m;
             if (it.nch == 0) {
-                for (int i = 0; i < D; ++i) To[(size_t)i * D] = (i == m) ? 1.f : 0.f;
+                for (int i = xc; i < xc + 64; ++i) {
+                    To[(size_t)i * D] = (i == m) ? 1.f : 0.f;
+                    So[(size_t)i * D] = 0.f;
+                }
                 continue;
             }
-            // Xt_T = s I with s = Gamma_C of the first chunk (pre-scaled) or 1
+            if (CK > 0) {
+                const float *wv = a.tok.conv_w + (((size_t)it.l * 3 + 2) * dm.H + it.h) * D * CK;
+#pragma unroll
+                for (int j = 0; j < (CK > 0 ? CK : 1); ++j) wvr[j] = __ldg(wv + m * CK + j);
+            }
+            // Xt_T = s I with s = Gamma_C of the first chunk (pre-scaled) or 1, its low part; Xt_S = 0
             bool w = true;
-            if (m == 0) w = wait_bar(bar(B_GF + n % RG), (n / RG) & 1, abort_flag);
-            if (!tc::bar_and(BAR_TEPI, 128, w)) { ok = false; break; }
+            if (et == 0) w = wait_bar(bar(B_GF + n % RG), (n / RG) & 1, abort_flag);
+            if (!tc::bar_and(BAR_EPI, 256, w)) { ok = false; break; }
             {
                 const Gates &G0 = gates(n);
                 const float s = G0.safe ? G0.eg[C - 1] : 1.f;
                 const float slo = s - __uint_as_float(__float_as_uint(s) & 0xffffe000u);
 #pragma unroll 1
-                for (int cc = 0; cc < D; cc += 32) {
+                for (int cc = xc; cc < xc + 64; cc += 32) {
                     float v[32];
                     uint32_t lo[16];
 #pragma unroll
@@ -898,168 +1006,138 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         lo[i] = pack_bf16((cc + 2 * i == m) ? slo : 0.f, (cc + 2 * i + 1 == m) ? slo : 0.f);
                     tc::tmem_st32_async(my + TM_XT + cc, v);
                     tc::tmem_st16_async(my + TM_XLO + cc / 2, lo);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    tc::tmem_st32_async(my + TM_XS + cc, v);
                     tc::tmem_wait_st();
                 }
             }
             tc::fence_before();
-            tc::bar_sync(BAR_TEPI, 128);
-            if (m == 0) tc::mbar_arrive(bar(B_XTR));
+            tc::bar_sync(BAR_EPI, 256);
+            if (et == 0) {
+                tc::mbar_arrive(bar(B_XTR));
+                tc::mbar_arrive(bar(B_XSI));
+            }
             for (int c = 0; c < it.nch; ++c, ++n) {
+                const int nc = min(C, (int)(it.n - c * C));
+                const uint8_t *stg = sm + SM_VR + (n % RV) * VR_STAGE;
                 w = true;
-                if (m == 0) w = wait_bar(bar(B_PTF), n & 1, abort_flag);
-                if (!tc::bar_and(BAR_TEPI, 128, w)) { ok = false; break; }
-                tc::fence_after();
+                if (et == 32) w = wait_bar(bar(B_VRF + n % RV), (n / RV) & 1, abort_flag);
+                if (et == 64) w = wait_bar(bar(B_GF + n % RG), (n / RG) & 1, abort_flag);
+                if (!tc::bar_and(BAR_EPI, 256, w)) { ok = false; break; }
                 const Gates &G = gates(n);
-                const bool safe = G.safe != 0;
                 {
-                    float p[32];
-#pragma unroll 1
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        // pre-scaled: Rt_T = -Pt_T Gamma_t / Gamma_C; else -Pt_T Gamma_t
-                        const float2 *f = reinterpret_cast<const float2 *>((safe ? G.nrc : G.neg) + h2 * 32);
-                        tc::tmem_ld32(my + TM_PT + h2 * 32, p);
+                    // conv of raw V, channel m, tokens pc .. pc+31 (0 past the chunk's end);
+                    // it does not wait for Pt_S
+                    float vv[32];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float2 r = __fmul2_rn(f[i], make_float2(p[2 * i], p[2 * i + 1]));
-                            p[2 * i] = tc::round_tf32(r.x);
-                            p[2 * i + 1] = tc::round_tf32(r.y);
+                    for (int qq = 0; qq < 2; ++qq) {
+                        // staged rows tq .. tq + 15 + HIST: lag j of token t is staged row t + HIST - j
+                        const int tq = pc + 16 * qq;
+                        float v[16 + HIST];
+#pragma unroll
+                        for (int i = 0; i < 16 + HIST; ++i) v[i] = bf16_at(stg, tq + i, m);
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            float2 x;
+                            if (CK == 0) {
+                                x = make_float2(v[i], v[i + 1]);
+                            } else {
+                                x = make_float2(0.f, 0.f);
+#pragma unroll
+                                for (int j = 0; j < (CK > 0 ? CK : 1); ++j)
+                                    x = __ffma2_rn(make_float2(wvr[j], wvr[j]),
+                                                   make_float2(v[i + HIST - j], v[i + 1 + HIST - j]), x);
+                                if (ACT) x = make_float2(silu(x.x), silu(x.y));
+                            }
+                            vv[16 * qq + i] = (tq + i < nc) ? x.x : 0.f;
+                            vv[16 * qq + i + 1] = (tq + i + 1 < nc) ? x.y : 0.f;
                         }
-                        tc::tmem_st32(my + TM_PT + h2 * 32, p);
                     }
-                    // not pre-scaled: Xt_T <- Gamma_C Xt_T here, after Pt_T has read it
-                    if (!safe) scale_cols(my + TM_XT, G.eg[C - 1]);
+                    w = true;
+                    if (et == 0) w = wait_bar(bar(B_PSF), n & 1, abort_flag);
+                    if (!tc::bar_and(BAR_EPI, 256, w)) { ok = false; break; }
+                    tc::fence_after();
+                    // Rt_S = V^T - Pt_S diag(Gamma), then Xt_S <- Gamma_C Xt_S (Pt_S has read it)
+                    uint32_t p[32];
+                    tc::tmem_ld32_issue(my + TM_PS + pc, p);
+                    tc::tmem_wait_ld32(p);
+                    const float2 *ng = reinterpret_cast<const float2 *>(G.neg + pc);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 r = __ffma2_rn(ng[i], make_float2(__uint_as_float(p[2 * i]), __uint_as_float(p[2 * i + 1])),
+                                                    make_float2(vv[2 * i], vv[2 * i + 1]));
+                        p[2 * i] = __float_as_uint(tc::round_tf32(r.x));
+                        p[2 * i + 1] = __float_as_uint(tc::round_tf32(r.y));
+                    }
+                    tc::tmem_st32_async(my + TM_PS + pc, reinterpret_cast<const float *>(p));
+                    scale_cols(my + TM_XS + xc, G.eg[C - 1]);
                 }
                 tc::fence_before();
-                tc::bar_sync(BAR_TEPI, 128);
-                if (m == 0) {
+                tc::bar_sync(BAR_EPI, 256);
+                if (et == 0) {
+                    tc::mbar_arrive(bar(B_RSF));
+                    tc::mbar_arrive(bar(B_VRE + n % RV));
+                }
+                w = true;
+                if (et == 0) w = wait_bar(bar(B_PTF), n & 1, abort_flag);
+                if (!tc::bar_and(BAR_EPI, 256, w)) { ok = false; break; }
+                tc::fence_after();
+                const bool safe = G.safe != 0;
+                {
+                    // pre-scaled: Rt_T = -Pt_T Gamma_t / Gamma_C; else -Pt_T Gamma_t
+                    float p[32];
+                    const float2 *f = reinterpret_cast<const float2 *>((safe ? G.nrc : G.neg) + pc);
+                    tc::tmem_ld32(my + TM_PT + pc, p);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 r = __fmul2_rn(f[i], make_float2(p[2 * i], p[2 * i + 1]));
+                        p[2 * i] = tc::round_tf32(r.x);
+                        p[2 * i + 1] = tc::round_tf32(r.y);
+                    }
+                    tc::tmem_st32(my + TM_PT + pc, p);
+                    // not pre-scaled: Xt_T <- Gamma_C Xt_T here, after Pt_T has read it
+                    if (!safe) scale_cols(my + TM_XT + xc, G.eg[C - 1]);
+                }
+                tc::fence_before();
+                tc::bar_sync(BAR_EPI, 256);
+                if (et == 0) {
                     tc::mbar_arrive(bar(B_RTF));
                     tc::mbar_arrive(bar(B_GE + n % RG));
                 }
                 const bool last = c + 1 == it.nch;
                 w = true;
-                if (m == 0) {
+                if (et == 0) {
                     w = wait_bar(bar(B_XTD), n & 1, abort_flag);
                     if (w && !last) w = wait_bar(bar(B_GF + (n + 1) % RG), ((n + 1) / RG) & 1, abort_flag);
                 }
-                if (!tc::bar_and(BAR_TEPI, 128, w)) { ok = false; break; }
+                if (!tc::bar_and(BAR_EPI, 256, w)) { ok = false; break; }
                 tc::fence_after();
                 if (last) {
-                    // emit T[i][m] = Xt_T[m][i]
+                    // emit T[i][m] = Xt_T[m][i], then S[i][m] = Xt_S[m][i] once the last update is done
                     float x[32];
 #pragma unroll 1
-                    for (int cc = 0; cc < D; cc += 32) {
+                    for (int cc = xc; cc < xc + 64; cc += 32) {
                         tc::tmem_ld32(my + TM_XT + cc, x);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) To[(size_t)(cc + i) * D] = x[i];
                     }
-                } else {
-                    const Gates &G1 = gates(n + 1);
-                    scale_split_xt(my, G1.safe ? G1.eg[C - 1] : 1.f);
-                    tc::fence_before();
-                    tc::bar_sync(BAR_TEPI, 128);
-                    if (m == 0) tc::mbar_arrive(bar(B_XTR));
-                }
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ S epilogue (warps 4-7)
-        const int m = tid - 128;  // row of Xt_S / Pt_S = column m of S (and value channel m)
-        float wvr[CK > 0 ? CK : 1];
-        int n = 0;
-        bool ok = true;
-        for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
-            const Item it = decode_item(itx, dm, tab);
-            const size_t pair = ((size_t)it.l * tab.n_seg + it.s) * dm.H + it.h;
-            float *So = a.S_out + pair * D * D + m;
-            if (it.nch == 0) {
-                for (int i = 0; i < D; ++i) So[(size_t)i * D] = 0.f;
-                continue;
-            }
-            if (CK > 0) {
-                const float *wv = a.tok.conv_w + (((size_t)it.l * 3 + 2) * dm.H + it.h) * D * CK;
-#pragma unroll
-                for (int j = 0; j < (CK > 0 ? CK : 1); ++j) wvr[j] = __ldg(wv + m * CK + j);
-            }
-            {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < D; cc += 32) tc::tmem_st32_async(my + TM_XS + cc, v);
-                tc::tmem_wait_st();
-            }
-            tc::fence_before();
-            tc::bar_sync(BAR_SEPI, 128);
-            if (m == 0) tc::mbar_arrive(bar(B_XSI));
-            for (int c = 0; c < it.nch; ++c, ++n) {
-                const int nc = min(C, (int)(it.n - c * C));
-                const uint8_t *stg = sm + SM_VR + (n % RV) * VR_STAGE;
-                bool w = true;
-                if (m == 0) w = wait_bar(bar(B_PSF), n & 1, abort_flag);
-                if (m == 32) w = wait_bar(bar(B_VRF + n % RV), (n / RV) & 1, abort_flag);
-                if (m == 64) w = wait_bar(bar(B_GF + n % RG), (n / RG) & 1, abort_flag);
-                if (!tc::bar_and(BAR_SEPI, 128, w)) { ok = false; break; }
-                tc::fence_after();
-                const Gates &G = gates(n);
-                {
-                    float p[32];
-#pragma unroll 1
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        tc::tmem_ld32(my + TM_PS + h2 * 32, p);
-                        const float2 *ng = reinterpret_cast<const float2 *>(G.neg + h2 * 32);
-#pragma unroll
-                        for (int qq = 0; qq < 2; ++qq) {
-                            // raw V of channel m, tokens t0 - HIST .. t0 + 15 (staged rows t0 ..)
-                            const int t0 = h2 * 32 + qq * 16;
-                            float v[16 + HIST];
-#pragma unroll
-                            for (int i = 0; i < 16 + HIST; ++i) v[i] = bf16_at(stg, t0 + i, m);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int t = t0 + 2 * i, e = qq * 16 + 2 * i;
-                                float2 vv;
-                                if (CK == 0) {
-                                    vv = make_float2(v[2 * i], v[2 * i + 1]);
-                                } else {
-                                    // token t + u uses staged row t + u + HIST - j (lag j)
-                                    vv = make_float2(0.f, 0.f);
-#pragma unroll
-                                    for (int j = 0; j < (CK > 0 ? CK : 1); ++j)
-                                        vv = __ffma2_rn(make_float2(wvr[j], wvr[j]),
-                                                        make_float2(v[2 * i + HIST - j], v[2 * i + 1 + HIST - j]), vv);
-                                    if (ACT) vv = make_float2(silu(vv.x), silu(vv.y));
-                                }
-                                if (t >= nc) vv.x = 0.f;
-                                if (t + 1 >= nc) vv.y = 0.f;
-                                const float2 r = __ffma2_rn(ng[qq * 8 + i], make_float2(p[e], p[e + 1]), vv);
-                                p[e] = tc::round_tf32(r.x);
-                                p[e + 1] = tc::round_tf32(r.y);
-                            }
-                        }
-                        tc::tmem_st32(my + TM_PS + h2 * 32, p);
-                    }
-                    scale_cols(my + TM_XS, G.eg[C - 1]);
-                }
-                tc::fence_before();
-                tc::bar_sync(BAR_SEPI, 128);
-                if (m == 0) {
-                    tc::mbar_arrive(bar(B_RSF));
-                    tc::mbar_arrive(bar(B_VRE + n % RV));
-                    tc::mbar_arrive(bar(B_GE + n % RG));
-                }
-                if (c + 1 == it.nch) {
-                    // emit S[i][m] = Xt_S[m][i] once the last update is done
                     w = true;
-                    if (m == 0) w = wait_bar(bar(B_XSD), n & 1, abort_flag);
-                    if (!tc::bar_and(BAR_SEPI, 128, w)) { ok = false; break; }
+                    if (et == 0) w = wait_bar(bar(B_XSD), n & 1, abort_flag);
+                    if (!tc::bar_and(BAR_EPI, 256, w)) { ok = false; break; }
                     tc::fence_after();
-                    float x[32];
 #pragma unroll 1
-                    for (int cc = 0; cc < D; cc += 32) {
+                    for (int cc = xc; cc < xc + 64; cc += 32) {
                         tc::tmem_ld32(my + TM_XS + cc, x);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) So[(size_t)(cc + i) * D] = x[i];
                     }
+                } else {
+                    const Gates &G1 = gates(n + 1);
+                    scale_split_xt(my, xc, G1.safe ? G1.eg[C - 1] : 1.f);
+                    tc::fence_before();
+                    tc::bar_sync(BAR_EPI, 256);
+                    if (et == 0) tc::mbar_arrive(bar(B_XTR));
                 }
             }
         }

@@ -29,6 +29,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile laid out in the
+// 128-byte swizzle: atoms of 8 K-rows x 128 bytes along MN (1024 bytes, 8-row
+// groups along K 1024 bytes apart), consecutive atoms along MN `lbo` bytes
+// apart; tile base 1024-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Byte offset of fp32 element (r, k) in a K-major 128-byte-swizzled tile of
 // R rows: K runs in atoms of 32 elements; atom a holds all R rows.
 __host__ __device__ __forceinline__ uint32_t sw128_f32(int r, int k, int R)
@@ -55,6 +70,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor: fp32 accumulate, fp16 A (MN-major) and B (K-major), kind::f16.
+__host__ __device__ constexpr uint32_t idesc_f16_amn(int M, int N)
+{
+    return (1u << 4) | (1u << 15) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Round to the nearest tf32 value (10 stored mantissa bits), ties away from
@@ -89,6 +110,15 @@ __device__ __forceinline__ void mma_ts_bf16(uint32_t d, uint32_t a, uint64_t b, 
     asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
                  :: "r"(d), "r"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with 16-bit operands (kind::f16; element
+// types and operand majors in the instruction descriptor).
+__device__ __forceinline__ void mma_ss_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc)
+{
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                 :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc));
 }
 
 // Arrive once on the mbarrier when every MMA this thread issued has completed.
@@ -150,6 +180,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
                  : "r"(taddr) : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns per thread, without waiting: r
+// must not be read before tmem_wait_ld32(r), which waits for every earlier
+// load of this thread and, by naming r as an operand, keeps every use of r
+// after it.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31])
+                 : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]),"+r"(r[8]),"+r"(r[9]),"+r"(r[10]),"+r"(r[11]),"+r"(r[12]),"+r"(r[13]),"+r"(r[14]),"+r"(r[15]),"+r"(r[16]),"+r"(r[17]),"+r"(r[18]),"+r"(r[19]),"+r"(r[20]),"+r"(r[21]),"+r"(r[22]),"+r"(r[23]),"+r"(r[24]),"+r"(r[25]),"+r"(r[26]),"+r"(r[27]),"+r"(r[28]),"+r"(r[29]),"+r"(r[30]),"+r"(r[31])
+                 :: "memory");
 }
 
 // M = 64 accumulator layout (rows in lanes 0-15 of the warp's quadrant): threads
