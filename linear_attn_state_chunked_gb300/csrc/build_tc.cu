@@ -42,10 +42,12 @@
 //   warp 16      one thread issues every tcgen05.mma of chunk n: Pt_S, Pt_T
 //                (+ its bf16 correction), the Gram of chunk n+1, the Xt_T and
 //                Xt_S updates, each behind a bounded mbarrier wait;
-//   warps 8-11   conversion: causal conv + L2 normalisation of K into tf32
-//                (operand of the Gram, Pt and the solve) and into bf16 (in
-//                place in the raw ring stage, operand of the correction), and
-//                the chunk's gates;
+//   warps 8-11   conversion: causal conv + L2 normalisation of K, rounded to
+//                tf32 and stored in fp16 (double-buffered; fp16 holds those
+//                values exactly: operand of the fp16 Gram and of the solve),
+//                copied to bf16 (in place in the raw ring stage, operand of
+//                the correction) and, once the previous Pt_T is done, to tf32
+//                (single buffer, operand of Pt);
 //   warps 12-15  solve: L'' from the Gram, W = (I + L'')^{-1}, and U~ = D W^T K
 //                into the 128-byte-swizzled B operand of the Xt update;
 //   warps 0-7    epilogue, each pass split over two warps per lane quadrant:
@@ -60,6 +62,7 @@
 // stand-in for its scatter workers.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -72,7 +75,7 @@ namespace {
 constexpr int D = 128;   // head width
 constexpr int C = 64;    // chunk length
 constexpr int NB = 16;   // block of the back substitution
-constexpr int RK = 3;    // raw-K ring stages
+constexpr int RK = 2;    // raw-K ring stages
 constexpr int RV = 2;    // raw-V ring stages
 constexpr int RG = 4;    // gate ring stages
 constexpr int HMAX = 3;  // conv history rows kept per chunk (conv_k <= 4)
@@ -96,13 +99,14 @@ constexpr uint32_t TM_COLS = 512;
 // shared memory (byte offsets from a 1024-aligned base)
 constexpr uint32_t KR_STAGE = 17408;  // raw K rows [C + 3][128] bf16, then K in bf16, sw128
 constexpr uint32_t VR_STAGE = 17152;  // raw V rows [C + 3][128] bf16
-constexpr uint32_t G_STAGE = 2176;    // Gates
+constexpr uint32_t G_STAGE = 1296;    // Gates
 constexpr int LP = C + 4;             // row pitch of L (16-byte rows for ldmatrix)
 constexpr uint32_t SM_KR = 0;
 constexpr uint32_t SM_VR = SM_KR + RK * KR_STAGE;
 constexpr uint32_t SM_GATE = SM_VR + RV * VR_STAGE;
-constexpr uint32_t SM_K32 = (SM_GATE + RG * G_STAGE + 1023) / 1024 * 1024;  // 2 x K [64][128] tf32, sw128
-constexpr uint32_t SM_UT = SM_K32 + 2 * 32768;  // U~^T [128][64] tf32, sw128 (B of the Xt update)
+constexpr uint32_t SM_K32 = (SM_GATE + RG * G_STAGE + 1023) / 1024 * 1024;  // K [64][128] tf32, sw128 (B of Pt)
+constexpr uint32_t SM_KH = SM_K32 + 32768;      // 2 x K [64][128] fp16, token-major sw128 (Gram, U~)
+constexpr uint32_t SM_UT = SM_KH + 2 * 16384;   // U~^T [128][64] tf32, sw128 (B of the Xt update)
 constexpr uint32_t SM_L = SM_UT + 32768;        // Z [64][LP]: L'' below the diagonal, W^T on and above
 constexpr int TP = 20;                          // row pitch of the 16 x 16 solve tiles
 constexpr int TMP_MROW = 0;                     // 4 x M_q = W_qq row-major [16][TP]
@@ -115,7 +119,7 @@ constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 40 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
-static_assert(KR_STAGE % 1024 == 0 && SM_K32 % 1024 == 0 && SM_UT % 1024 == 0, "tile alignment");
+static_assert(KR_STAGE % 1024 == 0 && SM_K32 % 1024 == 0 && SM_KH % 1024 == 0 && SM_UT % 1024 == 0, "tile alignment");
 static_assert((C + HMAX) * D * 2 <= (int)KR_STAGE && (C + HMAX) * D * 2 <= (int)VR_STAGE, "ring stage size");
 static_assert(SM_VR % 128 == 0 && VR_STAGE % 128 == 0, "TMA destination alignment");
 static_assert(SM_L % 16 == 0 && SM_TMP % 16 == 0 && (LP * 4) % 16 == 0 && (TP * 4) % 16 == 0,
@@ -141,8 +145,10 @@ enum {
     B_GF = B_VRE + RV,    // [RG] gates written                         conversion -> solve, epilogues
     B_GE = B_GF + RG,     // [RG] gates consumed (2 arrivals)           solve, epilogue -> gates
     B_KRDY = B_GE + RG,   // [2] K tf32 + bf16 written                  conversion -> MMA
-    B_K32E = B_KRDY + 2,  // [2] K tf32 free (2 arrivals)               MMA, solve -> conversion
-    B_GRAMF = B_K32E + 2, // Gram done                                  MMA -> solve
+    B_KHE = B_KRDY + 2,   // [2] K fp16 free (2 arrivals)               MMA, solve -> conversion
+    B_K32E = B_KHE + 2,   // K tf32 free (Pt_T done)                    MMA -> conversion
+    B_K32R,               // K tf32 written                             conversion -> MMA
+    B_GRAMF,              // Gram done                                  MMA -> solve
     B_GRAME,              // Gram read into L                           solve -> MMA
     B_UTF,                // U~^T written                               solve -> MMA
     B_UTE,                // U~^T consumed (Xt_S update done)           MMA -> solve
@@ -195,6 +201,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&p);
 }
 
+// Two floats as fp16 (round to nearest even), the first in the low half.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
+{
+    const __half2 p = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&p);
+}
+
 // Bounded wait by one thread; any failure (or another role's) aborts the CTA.
 __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatile int *abort_flag)
 {
@@ -205,6 +218,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatil
 __device__ __forceinline__ void mma16x8x8(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
 {
     asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Warp-level fp16 MMA, 16 x 8 x 16, fp32 accumulate into c.
+__device__ __forceinline__ void mma16x8x16_f16(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
                  "{%0,%1,%2,%3};"
                  : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
@@ -284,12 +306,14 @@ __device__ __forceinline__ void cursor_next(Cursor &cu, int n_items, const Dims 
     }
 }
 
-__device__ __forceinline__ void issue_gram(uint32_t tb, uint32_t sK32)
+// Gram K K^T (M = N = 64 tokens) from the fp16 K tile: 16 channels per MMA.
+// fp16 holds the tf32-rounded K exactly (same 10-bit mantissa; |k| <= 1).
+__device__ __forceinline__ void issue_gram(uint32_t tb, uint32_t sKH)
 {
 #pragma unroll
-    for (int ks = 0; ks < D / 8; ++ks)
-        tc::mma_ss(tb + TM_G, tc::sdesc_kstep(sK32, C, ks), tc::sdesc_kstep(sK32, C, ks), tc::idesc_tf32(64, 64),
-                   ks > 0);
+    for (int ks = 0; ks < D / 16; ++ks)
+        tc::mma_ss_f16(tb + TM_G, tc::sdesc_kstep(sKH, C, ks), tc::sdesc_kstep(sKH, C, ks), tc::idesc_f16(64, 64),
+                       ks > 0);
 }
 
 // Xt_T <- s Xt_T and its truncated-away low part in bf16, columns c0 .. c0+63
@@ -365,7 +389,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t cnt = 1;
             if (i >= B_GE && i < B_GE + RG) cnt = 2;
-            if (i >= B_K32E && i < B_K32E + 2) cnt = 2;
+            if (i >= B_KHE && i < B_KHE + 2) cnt = 2;
             tc::mbar_init(bar(i), cnt);
         }
         tc::fence_mbar_init();
@@ -424,16 +448,18 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 ok = wait_bar(bar(B_KRDY), 0, abort_flag);
                 tc::fence_after();
                 if (ok) {
-                    issue_gram(tb, s_base + SM_K32);
+                    issue_gram(tb, s_base + SM_KH);
                     tc::commit(bar(B_GRAMF));
+                    tc::commit(bar(B_KHE));
                 }
             }
             while (ok && mc.item < n_items) {
                 const int n = mc.n;
                 const uint32_t par = n & 1;
-                const uint32_t sK = s_base + SM_K32 + (n & 1) * 32768;
+                const uint32_t sK = s_base + SM_K32;
                 const uint32_t sK16 = s_base + SM_KR + (n % RK) * KR_STAGE;
                 if (mc.c == 0 && !wait_bar(bar(B_XSI), mc.xi & 1, abort_flag)) break;
+                if (!wait_bar(bar(B_K32R), par, abort_flag)) break;
                 tc::fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 8; ++ks)
@@ -451,7 +477,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     tc::mma_ts_bf16(tb + TM_PT, tb + TM_XLO + ks * 8, tc::sdesc_kstep(sK16, C, ks),
                                     tc::idesc_bf16(128, 64), 1);
                 tc::commit(bar(B_PTF));
-                tc::commit(bar(B_K32E + (n & 1)));
+                tc::commit(bar(B_K32E));
                 tc::commit(bar(B_KRE + n % RK));
                 Cursor nx = mc;
                 cursor_next(nx, n_items, dm, tab);
@@ -460,8 +486,9 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     if (!wait_bar(bar(B_KRDY + (n1 & 1)), (n1 >> 1) & 1, abort_flag)) break;
                     if (!wait_bar(bar(B_GRAME), par, abort_flag)) break;
                     tc::fence_after();
-                    issue_gram(tb, s_base + SM_K32 + (n1 & 1) * 32768);
+                    issue_gram(tb, s_base + SM_KH + (n1 & 1) * 16384);
                     tc::commit(bar(B_GRAMF));
+                    tc::commit(bar(B_KHE + (n1 & 1)));
                 }
                 if (!wait_bar(bar(B_UTF), par, abort_flag)) break;
                 if (!wait_bar(bar(B_RTF), par, abort_flag)) break;
@@ -513,10 +540,14 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 const int nc = min(C, (int)(it.n - c * C));
                 bool w = true;
                 if (ct == 0) w = wait_bar(bar(B_KRF + n % RK), (n / RK) & 1, abort_flag);
-                if (ct == 32 && n >= 2) w = wait_bar(bar(B_K32E + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
+                if (ct == 32 && n >= 2) w = wait_bar(bar(B_KHE + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
                 if (!tc::bar_and(BAR_CONV, 128, w)) { ok = false; break; }
                 uint8_t *stg = sm + SM_KR + (n % RK) * KR_STAGE;
-                uint8_t *k32 = sm + SM_K32 + (n & 1) * 32768;
+                uint8_t *kh = sm + SM_KH + (n & 1) * 16384;
+                // byte offset of channels c0 .. c0+3 of row `row` in a 16-bit token-major sw128 tile
+                auto o16 = [&](int row) {
+                    return (c0 >> 6) * 8192 + row * 128 + ((((c0 & 63) >> 3) ^ (row & 7)) << 4) + (c0 & 7) * 2;
+                };
                 // K conv weights of this thread's four channels (lag j, channel pairs)
                 float2 w2[CK > 0 ? CK : 1][2];
 #pragma unroll
@@ -588,28 +619,48 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             kx[r][1] = __fmul2_rn(kx[r][1], i2);
                         }
                     }
-                    // K in tf32 (sw128): a row's 32 16-byte chunks, one per lane -- conflict-free
+                    // K rounded to tf32, stored in fp16 (which holds it exactly): a row's
+                    // 32 8-byte pieces, one per lane
 #pragma unroll
                     for (int r = 0; r < 4; ++r)
-                        *reinterpret_cast<float4 *>(k32 + tc::sw128_f32(rb + r, c0, C)) =
-                            make_float4(tc::round_tf32(kx[r][0].x), tc::round_tf32(kx[r][0].y),
-                                        tc::round_tf32(kx[r][1].x), tc::round_tf32(kx[r][1].y));
+                        *reinterpret_cast<uint2 *>(kh + o16(rb + r)) =
+                            make_uint2(pack_f16(tc::round_tf32(kx[r][0].x), tc::round_tf32(kx[r][0].y)),
+                                       pack_f16(tc::round_tf32(kx[r][1].x), tc::round_tf32(kx[r][1].y)));
                 }
                 tc::bar_sync(BAR_CONV, 128);  // every raw row of the stage has been read
-                // K in bf16, in place over the raw rows: bf16 of the tf32 values just
-                // written (the correction product it feeds is ~2^-11 of Pt_T, so the
-                // second rounding is far below the tolerance)
+                // K in bf16, in place over the raw rows (same layout): bf16 of the values just
+                // written (the correction product it feeds is ~2^-11 of Pt_T, so the second
+                // rounding is far below the tolerance)
 #pragma unroll 4
                 for (int r = 0; r < 16; ++r) {
                     const int row = r0 + r;
-                    const float4 v = *reinterpret_cast<const float4 *>(k32 + tc::sw128_f32(row, c0, C));
-                    *reinterpret_cast<uint2 *>(stg + (c0 >> 6) * 8192 + row * 128 +
-                                               ((((c0 & 63) >> 3) ^ (row & 7)) << 4) + (c0 & 7) * 2) =
-                        make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+                    const uint2 h = *reinterpret_cast<const uint2 *>(kh + o16(row));
+                    const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));
+                    const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&h.y));
+                    *reinterpret_cast<uint2 *>(stg + o16(row)) = make_uint2(pack_bf16(a0.x, a0.y), pack_bf16(a1.x, a1.y));
                 }
                 tc::fence_async_smem();
                 tc::bar_sync(BAR_CONV, 128);
                 if (ct == 0) tc::mbar_arrive(bar(B_KRDY + (n & 1)));
+                // K in tf32 (B of Pt_S and Pt_T, single buffer) once the previous chunk's Pt_T
+                // has read it: a row's 32 16-byte chunks, one per lane
+                w = true;
+                if (ct == 0 && n > 0) w = wait_bar(bar(B_K32E), (n - 1) & 1, abort_flag);
+                if (!tc::bar_and(BAR_CONV, 128, w)) { ok = false; break; }
+                {
+                    uint8_t *k32 = sm + SM_K32;
+#pragma unroll 4
+                    for (int r = 0; r < 16; ++r) {
+                        const int row = r0 + r;
+                        const uint2 h = *reinterpret_cast<const uint2 *>(kh + o16(row));
+                        const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));
+                        const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&h.y));
+                        *reinterpret_cast<float4 *>(k32 + tc::sw128_f32(row, c0, C)) = make_float4(a0.x, a0.y, a1.x, a1.y);
+                    }
+                }
+                tc::fence_async_smem();
+                tc::bar_sync(BAR_CONV, 128);
+                if (ct == 0) tc::mbar_arrive(bar(B_K32R));
             }
         }
     } else if (warp == WARP_GATE) {
@@ -890,18 +941,19 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 if (sp == 0 && n > 0) w = wait_bar(bar(B_UTE), (n - 1) & 1, abort_flag);  // U~^T free
                 if (!tc::bar_and(BAR_SOLVE, 128, w)) { ok = false; break; }
                 {
-                    // U~_i = D_i sum_{j >= i} W_ji^T K_j for channels 32q .. 32q+31.  The swizzled
-                    // offsets below are those of tc::sw128_f32 with the block-dependent terms
-                    // split off (token blocks are multiples of 8 rows / 16 columns).
-                    const uint32_t k32 = s_base + SM_K32 + (n & 1) * 32768;
-                    // B of the K_j product: K[16 j + 8 ks + t4 (+4)][32 q + 8 nt + g]
-                    uint32_t kofs[4][2];
+                    // U~_i = D_i sum_{j >= i} W_ji^T K_j for channels 32q .. 32q+31 with fp16 warp
+                    // MMAs (m16n8k16): A = the (i, j) block of W^T, converted from Z (tf32 values,
+                    // exact in fp16); B = K_j from the fp16 tile by transposing ldmatrix.
+                    const uint32_t skh = s_base + SM_KH + (n & 1) * 16384;
+                    // ldmatrix rows: token 16 j + (lane & 7) + 8 ((lane >> 3) & 1), channel group
+                    // 8 (2 p + lane / 16) of this warp's 32 (n-tile pair p)
+                    const int lr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    uint32_t bro[2];
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                        for (int bb = 0; bb < 2; ++bb)
-                            kofs[nt][bb] = q * 8192 + (t4 + 4 * bb) * 128 +
-                                           ((((2 * nt + (g >> 2)) ^ (t4 + 4 * bb)) << 4) + (g & 3) * 4);
+                    for (int pp = 0; pp < 2; ++pp) {
+                        const int ch = 32 * q + 8 * (2 * pp + (lane >> 4));
+                        bro[pp] = (ch >> 6) * 8192 + lr * 128 + ((((ch & 63) >> 3) ^ (lr & 7)) << 4);
+                    }
                     // C stores: element e = (channel + (e & 1), token + 8 (e >> 1))
                     uint32_t so[2][4];
 #pragma unroll
@@ -911,7 +963,6 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             so[i1][e] = (e & 1) * 128 +
                                         ((((4 * i1 + (g >> 2) + 2 * (e >> 1)) ^ (2 * t4 + (e & 1))) << 4) + (g & 3) * 4);
                     const uint32_t sbase = SM_UT + (32 * q + 2 * t4) * 128;
-                    const uint32_t zrow = (((lane & 7) + ((lane >> 3) & 1) * 8) * LP + (lane >> 4) * 4) * 4;
 #pragma unroll 1
                     for (int i = 0; i < 4; ++i) {
                         float acc[4][4];
@@ -921,22 +972,30 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 #pragma unroll 1
                         for (int j = i; j < 4; ++j) {
-                            // every operand of the term first, then its eight MMAs
-                            uint32_t af[2][4], bf[2][4][2];
+                            // every operand of the term first, then its four MMAs
+                            uint32_t af[4], bf[4][2];
+                            const float *zr = Z + (NB * i + g) * LP + NB * j + 2 * t4;
+                            const float2 z0 = *reinterpret_cast<const float2 *>(zr);
+                            const float2 z1 = *reinterpret_cast<const float2 *>(zr + 8 * LP);
+                            const float2 z2 = *reinterpret_cast<const float2 *>(zr + 8);
+                            const float2 z3 = *reinterpret_cast<const float2 *>(zr + 8 * LP + 8);
 #pragma unroll
-                            for (int ks = 0; ks < 2; ++ks) {
-                                ldsm_x4(af[ks], sZ + ((NB * i) * LP + NB * j + 8 * ks) * 4 + zrow);
-                                const uint32_t kb = k32 + (NB * j + 8 * ks) * 128;
-#pragma unroll
-                                for (int nt = 0; nt < 4; ++nt) {
-                                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[ks][nt][0]) : "r"(kb + kofs[nt][0]));
-                                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bf[ks][nt][1]) : "r"(kb + kofs[nt][1]));
-                                }
+                            for (int pp = 0; pp < 2; ++pp) {
+                                uint32_t r4[4];
+                                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                                             : "=r"(r4[0]), "=r"(r4[1]), "=r"(r4[2]), "=r"(r4[3])
+                                             : "r"(skh + bro[pp] + NB * j * 128) : "memory");
+                                bf[2 * pp][0] = r4[0];
+                                bf[2 * pp][1] = r4[1];
+                                bf[2 * pp + 1][0] = r4[2];
+                                bf[2 * pp + 1][1] = r4[3];
                             }
+                            af[0] = pack_f16(z0.x, z0.y);
+                            af[1] = pack_f16(z1.x, z1.y);
+                            af[2] = pack_f16(z2.x, z2.y);
+                            af[3] = pack_f16(z3.x, z3.y);
 #pragma unroll
-                            for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-                                for (int nt = 0; nt < 4; ++nt) mma16x8x8(acc[nt], af[ks], bf[ks][nt]);
+                            for (int nt = 0; nt < 4; ++nt) mma16x8x16_f16(acc[nt], af, bf[nt]);
                         }
                         uint8_t *ub = sm + sbase + (i >> 1) * 16384;
                         const float dd[2] = {G.dc[NB * i + g], G.dc[NB * i + g + 8]};
@@ -952,7 +1011,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 tc::bar_sync(BAR_SOLVE, 128);
                 if (sp == 0) {
                     tc::mbar_arrive(bar(B_UTF));
-                    tc::mbar_arrive(bar(B_K32E + (n & 1)));
+                    tc::mbar_arrive(bar(B_KHE + (n & 1)));
                     tc::mbar_arrive(bar(B_GE + n % RG));
                 }
             }

@@ -72,6 +72,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor: fp32 accumulate, fp16 A and B, both K-major (kind::f16).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
+{
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor: fp32 accumulate, fp16 A (MN-major) and B (K-major), kind::f16.
 __host__ __device__ constexpr uint32_t idesc_f16_amn(int M, int N)
 {
