@@ -18,7 +18,8 @@
 // W is built by doubling: the eight 8 x 8 diagonal blocks by forward
 // substitution, then the block rule
 //   [[A, 0], [B, C]]^{-1} = [[A^-1, 0], [-C^-1 B A^-1, C^-1]]
-// at 16, 32 and 64 tokens with warp-level tf32 MMAs.  In 16-token blocks
+// at 16, 32 and 64 tokens with warp-level fp16 MMAs (W and L'' are O(1): fp16 keeps
+// the tf32 mantissa).  In 16-token blocks
 //   U~_i = D_i sum_{j >= i} W_ji^T K_j ,
 // ten independent block products per 32-channel slice of U~.
 //
@@ -100,21 +101,17 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t KR_STAGE = 17408;  // raw K rows [C + 3][128] bf16, then K in bf16, sw128
 constexpr uint32_t VR_STAGE = 17152;  // raw V rows [C + 3][128] bf16
 constexpr uint32_t G_STAGE = 1296;    // Gates
-constexpr int LP = C + 4;             // row pitch of L (16-byte rows for ldmatrix)
+constexpr int ZP = C + 8;             // row pitch (halves) of Z and the solve tiles: 16-byte, conflict-free ldmatrix rows
+constexpr int TP2 = 24;               // row pitch (halves) of the 16 x 16 solve tiles
 constexpr uint32_t SM_KR = 0;
 constexpr uint32_t SM_VR = SM_KR + RK * KR_STAGE;
 constexpr uint32_t SM_GATE = SM_VR + RV * VR_STAGE;
 constexpr uint32_t SM_K32 = (SM_GATE + RG * G_STAGE + 1023) / 1024 * 1024;  // K [64][128] tf32, sw128 (B of Pt)
 constexpr uint32_t SM_KH = SM_K32 + 32768;      // 2 x K [64][128] fp16, token-major sw128 (Gram, U~)
 constexpr uint32_t SM_UT = SM_KH + 2 * 16384;   // U~^T [128][64] tf32, sw128 (B of the Xt update)
-constexpr uint32_t SM_L = SM_UT + 32768;        // Z [64][LP]: L'' below the diagonal, W^T on and above
-constexpr int TP = 20;                          // row pitch of the 16 x 16 solve tiles
-constexpr int TMP_MROW = 0;                     // 4 x M_q = W_qq row-major [16][TP]
-constexpr int TMP_W32 = TMP_MROW + 4 * 16 * TP; // W_32 row-major [16][TP]
-constexpr int TMP_X = TMP_W32 + 16 * TP;        // 4 x [16][TP] per-warp scratch (G^T, Q, Y^T)
-constexpr int TMP_FLOATS = TMP_X + 4 * 16 * TP;
-constexpr uint32_t SM_TMP = SM_L + C * LP * 4;  // solve tiles
-constexpr uint32_t SM_WK = SM_TMP + TMP_FLOATS * 4;  // K conv weights of the current item [4 lags][128]
+constexpr uint32_t SM_L = SM_UT + 32768;        // Z [64][ZP] fp16: L'' below the diagonal, W^T on and above
+constexpr uint32_t SM_TMP = SM_L + C * ZP * 2;  // solve scratch: 4 x G^T [8][8] fp32, then 4 x [16][TP2] fp16
+constexpr uint32_t SM_WK = SM_TMP + 4 * 64 * 4 + 4 * 16 * TP2 * 2;  // K conv weights of the current item [4 lags][128]
 constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 40 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
@@ -122,8 +119,8 @@ constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
 static_assert(KR_STAGE % 1024 == 0 && SM_K32 % 1024 == 0 && SM_KH % 1024 == 0 && SM_UT % 1024 == 0, "tile alignment");
 static_assert((C + HMAX) * D * 2 <= (int)KR_STAGE && (C + HMAX) * D * 2 <= (int)VR_STAGE, "ring stage size");
 static_assert(SM_VR % 128 == 0 && VR_STAGE % 128 == 0, "TMA destination alignment");
-static_assert(SM_L % 16 == 0 && SM_TMP % 16 == 0 && (LP * 4) % 16 == 0 && (TP * 4) % 16 == 0,
-              "ldmatrix and float4 row alignment");
+static_assert(SM_L % 16 == 0 && SM_TMP % 16 == 0 && (ZP * 2) % 16 == 0 && (TP2 * 2) % 16 == 0,
+              "ldmatrix row alignment");
 static_assert(SMEM_DYN <= 232448, "shared memory budget");
 
 struct Gates {
@@ -214,13 +211,26 @@ __device__ __forceinline__ bool wait_bar(uint32_t mbar, uint32_t parity, volatil
     return tc::wait_bounded(mbar, parity, abort_flag, kWaitCycles);
 }
 
-// Warp-level tf32 MMA, 16 x 8 x 8, accumulate into c.
-__device__ __forceinline__ void mma16x8x8(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+// ldmatrix of four / two 8 x 8 16-bit tiles (optionally transposed).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
-    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr) : "memory");
 }
 
 // Warp-level fp16 MMA, 16 x 8 x 16, fp32 accumulate into c.
@@ -232,45 +242,22 @@ __device__ __forceinline__ void mma16x8x16_f16(float (&c)[4], const uint32_t (&a
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Warp-level tf32 MMA A operand straight from shared memory (ldmatrix of 8 x 4
-// fp32 tiles: lane 4g + t receives element (g, t) of each tile).
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
+// m16n8k16 operand fragments from row-major fp16 tiles in shared memory (base:
+// address of the tile's first element, pitch in halves):
+//   frag_a16  A (16 x 16) stored row-major;
+//   frag_b16t B (16 x 8) stored transposed (row n holds column n of B);
+//   frag_b16  B (16 x 8) stored row-major (row k), read by transposing ldmatrix.
+__device__ __forceinline__ void frag_a16(uint32_t (&a)[4], uint32_t base, int pitch, int lane)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+    ldsm_x4(a, base + (((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 8) * 2);
 }
-
-// A fragment of the 16 x 8 tile at (r0, k0) of a row-major fp32 matrix with
-// the given row pitch (floats).
-__device__ __forceinline__ void frag_a(uint32_t (&a)[4], uint32_t base, int pitch, int r0, int k0, int lane)
+__device__ __forceinline__ void frag_b16t(uint32_t (&b)[2], uint32_t base, int pitch, int lane)
 {
-    const int row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8, col = k0 + (lane >> 4) * 4;
-    ldsm_x4(a, base + (row * pitch + col) * 4);
+    ldsm_x2(b, base + ((lane & 7) * pitch + ((lane >> 3) & 1) * 8) * 2);
 }
-
-// B fragment (k0 .. k0+8) x (n0 .. n0+8) of a matrix stored transposed,
-// row-major with the given pitch (row n holds column n of the matrix).
-__device__ __forceinline__ void frag_b(uint32_t (&b)[2], uint32_t base, int pitch, int k0, int n0, int lane)
+__device__ __forceinline__ void frag_b16(uint32_t (&b)[2], uint32_t base, int pitch, int lane)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-                 : "=r"(b[0]), "=r"(b[1])
-                 : "r"(base + ((n0 + (lane & 7)) * pitch + k0 + ((lane >> 3) & 1) * 4) * 4)
-                 : "memory");
-}
-
-// acc (a 16 x 8 accumulator tile) += A B with A the 16 x 16 tile at a (row-major,
-// pitch pa) and B (16 x 8) given transposed: row n of the tile at bt (pitch pb)
-// holds column n of B.  Operands are tf32 values.
-__device__ __forceinline__ void mma_tile(float (&acc)[4], uint32_t a, int pa, uint32_t bt, int pb, int lane)
-{
-    uint32_t af[2][4], bf[2][2];
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        frag_a(af[ks], a, pa, 0, 8 * ks, lane);
-        frag_b(bf[ks], bt, pb, 8 * ks, 0, lane);
-    }
-    mma16x8x8(acc, af[0], bf[0]);
-    mma16x8x8(acc, af[1], bf[1]);
+    ldsm_x2_t(b, base + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch * 2);
 }
 
 // Cursor over this CTA's chunks (non-empty items only), used by the MMA issuer.
@@ -751,16 +738,18 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
         const int sp = tid - 384;  // 0 .. 127
         const int q = warp & 3;    // lane quadrant; 16-token block; channels 32q .. 32q+31
         const int g = lane >> 2, t4 = lane & 3;
-        // Z: L'' strictly below the diagonal, W^T on and above it (tf32 values)
-        float *Z = reinterpret_cast<float *>(sm + SM_L);
-        float *tmp = reinterpret_cast<float *>(sm + SM_TMP);
-        const uint32_t sZ = s_base + SM_L, sT = s_base + SM_TMP;
-        // byte address of element (r, c) of Z and of a solve tile
-        auto zaddr = [&](int r, int c) { return sZ + static_cast<uint32_t>((r * LP + c) * 4); };
-        auto taddr = [&](int t0, int r, int c) { return sT + static_cast<uint32_t>((t0 + r * TP + c) * 4); };
-        // the upper-right 8 x 8 of each row-major M_q is zero
-        for (int e = sp; e < 4 * 64; e += 128)
-            tmp[TMP_MROW + (e >> 6) * 16 * TP + ((e >> 3) & 7) * TP + 8 + (e & 7)] = 0.f;
+        // Z: L'' strictly below the diagonal, W^T on and above it, fp16 (the tf32-rounded
+        // values' mantissa, and |entries| stay far inside fp16's range)
+        __half *Zh = reinterpret_cast<__half *>(sm + SM_L);
+        float *gtb = reinterpret_cast<float *>(sm + SM_TMP);                  // 4 x G^T [8][8]
+        const uint32_t sZ = s_base + SM_L, sX = s_base + SM_TMP + 4 * 64 * 4; // 4 x [16][TP2] fp16
+        auto zh = [&](int r, int c) -> __half & { return Zh[r * ZP + c]; };
+        auto zad = [&](int r, int c) { return sZ + static_cast<uint32_t>((r * ZP + c) * 2); };
+        auto xad = [&](int w, int r, int c) { return sX + static_cast<uint32_t>(((w * 16 + r) * TP2 + c) * 2); };
+        // fp16 pair (row r, columns c, c + 1) of a tile
+        auto put2 = [&](uint32_t addr, float lo, float hi) {
+            *reinterpret_cast<uint32_t *>(sm + (addr - s_base)) = pack_f16(lo, hi);
+        };
         int n = 0;
         bool ok = true;
         for (int itx = blockIdx.x; itx < n_items && ok; itx += gridDim.x) {
@@ -781,82 +770,78 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     tc::tmem_ld16x2_32(my + TM_G, gr);
                     const int t = 16 * q + (lane & 15);
                     const int j0 = (lane >= 16) ? 32 : 0;
-                    const float2 b2 = make_float2(G.b[t], G.b[t]);
+                    const float bt = G.b[t];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float2 v = __fmul2_rn(b2, make_float2(gr[j], gr[j + 1]));
-                        gr[j] = tc::round_tf32(v.x);
-                        gr[j + 1] = tc::round_tf32(v.y);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(Z + t * LP + j0 + j) = make_float4(gr[j], gr[j + 1], gr[j + 2], gr[j + 3]);
+                    for (int j = 0; j < 32; j += 8)
+                        *reinterpret_cast<uint4 *>(&zh(t, j0 + j)) =
+                            make_uint4(pack_f16(bt * gr[j], bt * gr[j + 1]), pack_f16(bt * gr[j + 2], bt * gr[j + 3]),
+                                       pack_f16(bt * gr[j + 4], bt * gr[j + 5]), pack_f16(bt * gr[j + 6], bt * gr[j + 7]));
                 }
                 tc::fence_before();
                 tc::bar_sync(BAR_SOLVE, 128);
                 if (sp == 0) tc::mbar_arrive(bar(B_GRAME));
                 if (lane < 16) {
                     // column j of the 8 x 8 diagonal block E_b = (I + L''_bb)^{-1}, b = 2q + lane / 8,
-                    // by forward substitution; column r of L''_bb is loaded one step ahead
+                    // by forward substitution in fp32; column r of L''_bb is loaded one step ahead
                     const int hb = lane >> 3, base = 16 * q + 8 * hb, j = lane & 7;
-                    const float *Lb = Z + base * LP + base;
                     float x[8];
 #pragma unroll
                     for (int r = 0; r < 8; ++r) x[r] = (r == j) ? 1.f : 0.f;
                     float col[7];
 #pragma unroll
-                    for (int k = 0; k < 7; ++k) col[k] = Lb[(k + 1) * LP];
+                    for (int k = 0; k < 7; ++k) col[k] = __half2float(zh(base + k + 1, base));
 #pragma unroll
                     for (int r = 0; r < 7; ++r) {
                         float nxt[6];
 #pragma unroll
-                        for (int k = 0; k < 6 - r; ++k) nxt[k] = Lb[(r + 2 + k) * LP + r + 1];
+                        for (int k = 0; k < 6 - r; ++k) nxt[k] = __half2float(zh(base + r + 2 + k, base + r + 1));
                         asm volatile("" ::: "memory");  // issue them before this step's products
 #pragma unroll
                         for (int k = 0; k < 7 - r; ++k) x[r + 1 + k] = fmaf(-col[k], x[r], x[r + 1 + k]);
 #pragma unroll
                         for (int k = 0; k < 6 - r; ++k) col[k] = nxt[k];
                     }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[k] = tc::round_tf32(x[k]);
                     __syncwarp(0x0000ffffu);  // every read of L''_bb is done
                     // row j of E_b^T into Z (its strictly lower part, zero, replaces the
-                    // consumed L''_bb) and column j of E_b into the row-major M_q
-                    float *wr = Z + (base + j) * LP + base;
-                    *reinterpret_cast<float4 *>(wr) = make_float4(x[0], x[1], x[2], x[3]);
-                    *reinterpret_cast<float4 *>(wr + 4) = make_float4(x[4], x[5], x[6], x[7]);
-                    float *mr = tmp + TMP_MROW + q * 16 * TP + (8 * hb) * TP + 8 * hb + j;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mr[k * TP] = x[k];
+                    // consumed L''_bb)
+                    *reinterpret_cast<uint4 *>(&zh(base + j, base)) =
+                        make_uint4(pack_f16(x[0], x[1]), pack_f16(x[2], x[3]), pack_f16(x[4], x[5]), pack_f16(x[6], x[7]));
                 }
                 __syncwarp();
                 {
                     // M_q = (I + L''_qq)^{-1}: its lower-left 8 x 8 F = -E_{2q+1} L''_{2q+1,2q} E_{2q}
                     // (lane: row r, columns c0, c0 + 1), in fp32
                     const int r = lane >> 2, c0 = 2 * (lane & 3), b0 = 16 * q;
-                    const float *lrow = Z + (b0 + 8 + r) * LP + b0;
-                    const float4 la = *reinterpret_cast<const float4 *>(lrow);
-                    const float4 lb = *reinterpret_cast<const float4 *>(lrow + 4);
-                    float *gt = tmp + TMP_X + q * 64;  // G^T [8][8], G = L''_{2q+1,2q} E_{2q}
+                    float la[8];
+                    {
+                        const uint4 h = *reinterpret_cast<const uint4 *>(&zh(b0 + 8 + r, b0));
+                        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hw[k]));
+                            la[2 * k] = f.x;
+                            la[2 * k + 1] = f.y;
+                        }
+                    }
+                    float *gt = gtb + q * 64;  // G^T [8][8], G = L''_{2q+1,2q} E_{2q}
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const float *ec = Z + (b0 + c0 + u) * LP + b0;  // column c0 + u of E_{2q}
-                        const float4 ea = *reinterpret_cast<const float4 *>(ec);
-                        const float4 eb = *reinterpret_cast<const float4 *>(ec + 4);
-                        float gv = la.x * ea.x;
-                        gv = fmaf(la.y, ea.y, gv);
-                        gv = fmaf(la.z, ea.z, gv);
-                        gv = fmaf(la.w, ea.w, gv);
-                        gv = fmaf(lb.x, eb.x, gv);
-                        gv = fmaf(lb.y, eb.y, gv);
-                        gv = fmaf(lb.z, eb.z, gv);
-                        gv = fmaf(lb.w, eb.w, gv);
+                        // column c0 + u of E_{2q}: row c0 + u of E_{2q}^T
+                        const uint4 h = *reinterpret_cast<const uint4 *>(&zh(b0 + c0 + u, b0));
+                        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+                        float gv = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hw[k]));
+                            gv = fmaf(la[2 * k], f.x, gv);
+                            gv = fmaf(la[2 * k + 1], f.y, gv);
+                        }
                         gt[(c0 + u) * 8 + r] = gv;
                     }
                     __syncwarp();
                     float er[8];  // row r of E_{2q+1}
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) er[k] = Z[(b0 + 8 + k) * LP + b0 + 8 + r];
+                    for (int k = 0; k < 8; ++k) er[k] = __half2float(zh(b0 + 8 + k, b0 + 8 + r));
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const float4 ga = *reinterpret_cast<const float4 *>(gt + (c0 + u) * 8);
@@ -869,10 +854,8 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         f = fmaf(er[5], gb.y, f);
                         f = fmaf(er[6], gb.z, f);
                         f = fmaf(er[7], gb.w, f);
-                        f = tc::round_tf32(-f);
-                        Z[(b0 + c0 + u) * LP + b0 + 8 + r] = f;  // W^T[b0 + c][b0 + 8 + r]
-                        tmp[TMP_MROW + q * 16 * TP + (8 + r) * TP + c0 + u] = f;
-                        Z[(b0 + 8 + r) * LP + b0 + c0 + u] = 0.f;  // upper-right 8 x 8 of M_q
+                        zh(b0 + c0 + u, b0 + 8 + r) = __float2half_rn(-f);  // W^T[b0 + c][b0 + 8 + r]
+                        zh(b0 + 8 + r, b0 + c0 + u) = __float2half_rn(0.f);  // upper-right 8 x 8 of M_q
                     }
                 }
                 tc::bar_sync(BAR_SOLVE, 128);
@@ -880,42 +863,39 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     // 32-token blocks, transposed: W_ji^T = -(M_i^T L''_ji^T) M_j^T for
                     // (j, i) = (1, 0), (3, 2); warp: pair w / 2, output columns 8 (w % 2) ..
                     const int jb = (q >> 1) ? 3 : 1, ib = jb - 1, nt = q & 1;
-                    const int xq = TMP_X + q * 16 * TP;  // Q = M_i^T L''_ji^T, row-major
+                    uint32_t af[4], bf[2];
+                    frag_a16(af, zad(16 * ib, 16 * ib), ZP, lane);  // M_i^T
 #pragma unroll
                     for (int qt = 0; qt < 2; ++qt) {
                         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_tile(acc, zaddr(16 * ib, 16 * ib), LP, zaddr(16 * jb + 8 * qt, 16 * ib), LP, lane);
-                        tmp[xq + g * TP + 8 * qt + 2 * t4] = tc::round_tf32(acc[0]);
-                        tmp[xq + g * TP + 8 * qt + 2 * t4 + 1] = tc::round_tf32(acc[1]);
-                        tmp[xq + (g + 8) * TP + 8 * qt + 2 * t4] = tc::round_tf32(acc[2]);
-                        tmp[xq + (g + 8) * TP + 8 * qt + 2 * t4 + 1] = tc::round_tf32(acc[3]);
+                        frag_b16t(bf, zad(16 * jb + 8 * qt, 16 * ib), ZP, lane);  // L''_ji rows = (L''_ji^T) columns
+                        mma16x8x16_f16(acc, af, bf);
+                        put2(xad(q, g, 8 * qt + 2 * t4), acc[0], acc[1]);
+                        put2(xad(q, g + 8, 8 * qt + 2 * t4), acc[2], acc[3]);
                     }
                     __syncwarp();
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_tile(acc, taddr(xq, 0, 0), TP, taddr(TMP_MROW + jb * 16 * TP, 8 * nt, 0), TP, lane);
-                    const int cc = 16 * jb + 8 * nt + 2 * t4;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float v = tc::round_tf32(-acc[e]);
-                        const int rr = g + 8 * (e >> 1), ce = cc + (e & 1);
-                        Z[(16 * ib + rr) * LP + ce] = v;
-                        if (jb == 3) tmp[TMP_W32 + (ce - 48) * TP + rr] = v;  // W_32 row-major
-                    }
+                    frag_a16(af, xad(q, 0, 0), TP2, lane);
+                    frag_b16(bf, zad(16 * jb, 16 * jb + 8 * nt), ZP, lane);  // M_j^T, row-major
+                    mma16x8x16_f16(acc, af, bf);
+                    put2(zad(16 * ib + g, 16 * jb + 8 * nt + 2 * t4), -acc[0], -acc[1]);
+                    put2(zad(16 * ib + g + 8, 16 * jb + 8 * nt + 2 * t4), -acc[2], -acc[3]);
                 }
                 tc::bar_sync(BAR_SOLVE, 128);
                 {
                     // 64 tokens: Y^T = W_a^T L''_ba^T (warp: block (w / 2, w % 2) of Y, transposed)
                     const int yr = q >> 1, yc = q & 1;
-                    const int yq = TMP_X + q * 16 * TP;
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int kb = yc; kb < 2; ++kb)
-                            mma_tile(acc, zaddr(16 * yc, 16 * kb), LP, zaddr(16 * (2 + yr) + 8 * nt, 16 * kb), LP, lane);
-                        tmp[yq + g * TP + 8 * nt + 2 * t4] = tc::round_tf32(acc[0]);
-                        tmp[yq + g * TP + 8 * nt + 2 * t4 + 1] = tc::round_tf32(acc[1]);
-                        tmp[yq + (g + 8) * TP + 8 * nt + 2 * t4] = tc::round_tf32(acc[2]);
-                        tmp[yq + (g + 8) * TP + 8 * nt + 2 * t4 + 1] = tc::round_tf32(acc[3]);
+                        for (int kb = yc; kb < 2; ++kb) {
+                            uint32_t af[4], bf[2];
+                            frag_a16(af, zad(16 * yc, 16 * kb), ZP, lane);
+                            frag_b16t(bf, zad(16 * (2 + yr) + 8 * nt, 16 * kb), ZP, lane);
+                            mma16x8x16_f16(acc, af, bf);
+                        }
+                        put2(xad(q, g, 8 * nt + 2 * t4), acc[0], acc[1]);
+                        put2(xad(q, g + 8, 8 * nt + 2 * t4), acc[2], acc[3]);
                     }
                 }
                 tc::bar_sync(BAR_SOLVE, 128);
@@ -926,15 +906,13 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     for (int nt = 0; nt < 2; ++nt) {
                         float acc[4] = {0.f, 0.f, 0.f, 0.f};
                         for (int kb = 2; kb <= wr; ++kb) {
-                            const int yt = TMP_X + ((kb - 2) * 2 + wc) * 16 * TP;
-                            const int wt = (kb == wr) ? TMP_MROW + wr * 16 * TP : TMP_W32;
-                            mma_tile(acc, taddr(yt, 0, 0), TP, taddr(wt, 8 * nt, 0), TP, lane);
+                            uint32_t af[4], bf[2];
+                            frag_a16(af, xad((kb - 2) * 2 + wc, 0, 0), TP2, lane);
+                            frag_b16(bf, zad(16 * kb, 16 * wr + 8 * nt), ZP, lane);  // W_{wr,kb}^T, row-major
+                            mma16x8x16_f16(acc, af, bf);
                         }
-                        const int cc = 16 * wr + 8 * nt + 2 * t4;
-                        Z[(16 * wc + g) * LP + cc] = tc::round_tf32(-acc[0]);
-                        Z[(16 * wc + g) * LP + cc + 1] = tc::round_tf32(-acc[1]);
-                        Z[(16 * wc + g + 8) * LP + cc] = tc::round_tf32(-acc[2]);
-                        Z[(16 * wc + g + 8) * LP + cc + 1] = tc::round_tf32(-acc[3]);
+                        put2(zad(16 * wc + g, 16 * wr + 8 * nt + 2 * t4), -acc[0], -acc[1]);
+                        put2(zad(16 * wc + g + 8, 16 * wr + 8 * nt + 2 * t4), -acc[2], -acc[3]);
                     }
                 }
                 w = true;
@@ -942,8 +920,8 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 if (!tc::bar_and(BAR_SOLVE, 128, w)) { ok = false; break; }
                 {
                     // U~_i = D_i sum_{j >= i} W_ji^T K_j for channels 32q .. 32q+31 with fp16 warp
-                    // MMAs (m16n8k16): A = the (i, j) block of W^T, converted from Z (tf32 values,
-                    // exact in fp16); B = K_j from the fp16 tile by transposing ldmatrix.
+                    // MMAs (m16n8k16): A = the (i, j) block of W^T from Z; B = K_j from the fp16
+                    // K tile by transposing ldmatrix.
                     const uint32_t skh = s_base + SM_KH + (n & 1) * 16384;
                     // ldmatrix rows: token 16 j + (lane & 7) + 8 ((lane >> 3) & 1), channel group
                     // 8 (2 p + lane / 16) of this warp's 32 (n-tile pair p)
@@ -974,26 +952,16 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                         for (int j = i; j < 4; ++j) {
                             // every operand of the term first, then its four MMAs
                             uint32_t af[4], bf[4][2];
-                            const float *zr = Z + (NB * i + g) * LP + NB * j + 2 * t4;
-                            const float2 z0 = *reinterpret_cast<const float2 *>(zr);
-                            const float2 z1 = *reinterpret_cast<const float2 *>(zr + 8 * LP);
-                            const float2 z2 = *reinterpret_cast<const float2 *>(zr + 8);
-                            const float2 z3 = *reinterpret_cast<const float2 *>(zr + 8 * LP + 8);
+                            frag_a16(af, zad(NB * i, NB * j), ZP, lane);
 #pragma unroll
                             for (int pp = 0; pp < 2; ++pp) {
                                 uint32_t r4[4];
-                                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                                             : "=r"(r4[0]), "=r"(r4[1]), "=r"(r4[2]), "=r"(r4[3])
-                                             : "r"(skh + bro[pp] + NB * j * 128) : "memory");
+                                ldsm_x4_t(r4, skh + bro[pp] + NB * j * 128);
                                 bf[2 * pp][0] = r4[0];
                                 bf[2 * pp][1] = r4[1];
                                 bf[2 * pp + 1][0] = r4[2];
                                 bf[2 * pp + 1][1] = r4[3];
                             }
-                            af[0] = pack_f16(z0.x, z0.y);
-                            af[1] = pack_f16(z1.x, z1.y);
-                            af[2] = pack_f16(z2.x, z2.y);
-                            af[3] = pack_f16(z3.x, z3.y);
 #pragma unroll
                             for (int nt = 0; nt < 4; ++nt) mma16x8x16_f16(acc[nt], af, bf[nt]);
                         }
