@@ -98,7 +98,7 @@ constexpr uint32_t TM_XLO = 448;  // Xt_T - trunc(Xt_T) in bf16 pairs: 64 column
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory (byte offsets from a 1024-aligned base)
-constexpr uint32_t KR_STAGE = 17408;  // raw K rows [C + 3][128] bf16, then K in bf16, sw128
+constexpr uint32_t KR_STAGE = 17408;  // raw K rows [C + 3][128] bf16
 constexpr uint32_t VR_STAGE = 17152;  // raw V rows [C + 3][128] bf16
 constexpr uint32_t G_STAGE = 1296;    // Gates
 constexpr int ZP = C + 8;             // row pitch (halves) of Z and the solve tiles: 16-byte, conflict-free ldmatrix rows
@@ -108,7 +108,8 @@ constexpr uint32_t SM_VR = SM_KR + RK * KR_STAGE;
 constexpr uint32_t SM_GATE = SM_VR + RV * VR_STAGE;
 constexpr uint32_t SM_K32 = (SM_GATE + RG * G_STAGE + 1023) / 1024 * 1024;  // K [64][128] tf32, sw128 (B of Pt)
 constexpr uint32_t SM_KH = SM_K32 + 32768;      // 2 x K [64][128] fp16, token-major sw128 (Gram, U~)
-constexpr uint32_t SM_UT = SM_KH + 2 * 16384;   // U~^T [128][64] tf32, sw128 (B of the Xt update)
+constexpr uint32_t SM_KB = SM_KH + 2 * 16384;   // 2 x K [64][128] bf16, token-major sw128 (Pt_T correction)
+constexpr uint32_t SM_UT = SM_KB + 2 * 16384;   // U~^T [128][64] tf32, sw128 (B of the Xt update)
 constexpr uint32_t SM_L = SM_UT + 32768;        // Z [64][ZP] fp16: L'' below the diagonal, W^T on and above
 constexpr uint32_t SM_TMP = SM_L + C * ZP * 2;  // solve scratch: 4 x G^T [8][8] fp32, then 4 x [16][TP2] fp16
 constexpr uint32_t SM_WK = SM_TMP + 4 * 64 * 4 + 4 * 16 * TP2 * 2;  // K conv weights of the current item [4 lags][128]
@@ -116,7 +117,8 @@ constexpr uint32_t SM_BAR = SM_WK + D * 4 * 4;
 constexpr uint32_t SM_MISC = SM_BAR + 40 * 8;
 constexpr uint32_t SM_BYTES = SM_MISC + 64;
 constexpr uint32_t SMEM_DYN = SM_BYTES + 1024;
-static_assert(KR_STAGE % 1024 == 0 && SM_K32 % 1024 == 0 && SM_KH % 1024 == 0 && SM_UT % 1024 == 0, "tile alignment");
+static_assert(KR_STAGE % 1024 == 0 && SM_K32 % 1024 == 0 && SM_KH % 1024 == 0 && SM_KB % 1024 == 0 &&
+                  SM_UT % 1024 == 0, "tile alignment");
 static_assert((C + HMAX) * D * 2 <= (int)KR_STAGE && (C + HMAX) * D * 2 <= (int)VR_STAGE, "ring stage size");
 static_assert(SM_VR % 128 == 0 && VR_STAGE % 128 == 0, "TMA destination alignment");
 static_assert(SM_L % 16 == 0 && SM_TMP % 16 == 0 && (ZP * 2) % 16 == 0 && (TP2 * 2) % 16 == 0,
@@ -136,13 +138,13 @@ static_assert(sizeof(Gates) <= G_STAGE, "gate stage size");
 // mbarriers
 enum {
     B_KRF = 0,            // [RK] raw K stage loaded                    TMA -> conversion
-    B_KRE = B_KRF + RK,   // [RK] stage free (bf16 K consumed)          MMA -> TMA
+    B_KRE = B_KRF + RK,   // [RK] stage free (raw rows converted)       conversion -> TMA
     B_VRF = B_KRE + RK,   // [RV] raw V stage loaded                    TMA -> S epilogue
     B_VRE = B_VRF + RV,   // [RV] stage free                            S epilogue -> TMA
     B_GF = B_VRE + RV,    // [RG] gates written                         conversion -> solve, epilogues
     B_GE = B_GF + RG,     // [RG] gates consumed (2 arrivals)           solve, epilogue -> gates
     B_KRDY = B_GE + RG,   // [2] K tf32 + bf16 written                  conversion -> MMA
-    B_KHE = B_KRDY + 2,   // [2] K fp16 free (2 arrivals)               MMA, solve -> conversion
+    B_KHE = B_KRDY + 2,   // [2] K fp16 and bf16 free (2 arrivals)      MMA, solve -> conversion
     B_K32E = B_KHE + 2,   // K tf32 free (Pt_T done)                    MMA -> conversion
     B_K32R,               // K tf32 written                             conversion -> MMA
     B_GRAMF,              // Gram done                                  MMA -> solve
@@ -437,14 +439,13 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 if (ok) {
                     issue_gram(tb, s_base + SM_KH);
                     tc::commit(bar(B_GRAMF));
-                    tc::commit(bar(B_KHE));
                 }
             }
             while (ok && mc.item < n_items) {
                 const int n = mc.n;
                 const uint32_t par = n & 1;
                 const uint32_t sK = s_base + SM_K32;
-                const uint32_t sK16 = s_base + SM_KR + (n % RK) * KR_STAGE;
+                const uint32_t sK16 = s_base + SM_KB + (n & 1) * 16384;
                 if (mc.c == 0 && !wait_bar(bar(B_XSI), mc.xi & 1, abort_flag)) break;
                 if (!wait_bar(bar(B_K32R), par, abort_flag)) break;
                 tc::fence_after();
@@ -465,7 +466,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                                     tc::idesc_bf16(128, 64), 1);
                 tc::commit(bar(B_PTF));
                 tc::commit(bar(B_K32E));
-                tc::commit(bar(B_KRE + n % RK));
+                tc::commit(bar(B_KHE + (n & 1)));  // its Gram and Pt_T have read K in fp16 and bf16
                 Cursor nx = mc;
                 cursor_next(nx, n_items, dm, tab);
                 if (nx.item < n_items) {
@@ -475,7 +476,6 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                     tc::fence_after();
                     issue_gram(tb, s_base + SM_KH + (n1 & 1) * 16384);
                     tc::commit(bar(B_GRAMF));
-                    tc::commit(bar(B_KHE + (n1 & 1)));
                 }
                 if (!wait_bar(bar(B_UTF), par, abort_flag)) break;
                 if (!wait_bar(bar(B_RTF), par, abort_flag)) break;
@@ -531,6 +531,7 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                 if (!tc::bar_and(BAR_CONV, 128, w)) { ok = false; break; }
                 uint8_t *stg = sm + SM_KR + (n % RK) * KR_STAGE;
                 uint8_t *kh = sm + SM_KH + (n & 1) * 16384;
+                uint8_t *kb = sm + SM_KB + (n & 1) * 16384;
                 // byte offset of channels c0 .. c0+3 of row `row` in a 16-bit token-major sw128 tile
                 auto o16 = [&](int row) {
                     return (c0 >> 6) * 8192 + row * 128 + ((((c0 & 63) >> 3) ^ (row & 7)) << 4) + (c0 & 7) * 2;
@@ -606,29 +607,23 @@ build_tc_kernel(const __grid_constant__ BuildArgs a, const __grid_constant__ Seg
                             kx[r][1] = __fmul2_rn(kx[r][1], i2);
                         }
                     }
-                    // K rounded to tf32, stored in fp16 (which holds it exactly): a row's
-                    // 32 8-byte pieces, one per lane
+                    // K rounded to tf32, stored in fp16 (which holds it exactly) and in bf16
+                    // (operand of the Pt_T correction: a second rounding ~2^-11 of a term that
+                    // is ~2^-11 of Pt_T); a row's 32 8-byte pieces, one per lane
 #pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        *reinterpret_cast<uint2 *>(kh + o16(rb + r)) =
-                            make_uint2(pack_f16(tc::round_tf32(kx[r][0].x), tc::round_tf32(kx[r][0].y)),
-                                       pack_f16(tc::round_tf32(kx[r][1].x), tc::round_tf32(kx[r][1].y)));
-                }
-                tc::bar_sync(BAR_CONV, 128);  // every raw row of the stage has been read
-                // K in bf16, in place over the raw rows (same layout): bf16 of the values just
-                // written (the correction product it feeds is ~2^-11 of Pt_T, so the second
-                // rounding is far below the tolerance)
-#pragma unroll 4
-                for (int r = 0; r < 16; ++r) {
-                    const int row = r0 + r;
-                    const uint2 h = *reinterpret_cast<const uint2 *>(kh + o16(row));
-                    const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));
-                    const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&h.y));
-                    *reinterpret_cast<uint2 *>(stg + o16(row)) = make_uint2(pack_bf16(a0.x, a0.y), pack_bf16(a1.x, a1.y));
+                    for (int r = 0; r < 4; ++r) {
+                        const float x0 = tc::round_tf32(kx[r][0].x), x1 = tc::round_tf32(kx[r][0].y);
+                        const float x2 = tc::round_tf32(kx[r][1].x), x3 = tc::round_tf32(kx[r][1].y);
+                        *reinterpret_cast<uint2 *>(kh + o16(rb + r)) = make_uint2(pack_f16(x0, x1), pack_f16(x2, x3));
+                        *reinterpret_cast<uint2 *>(kb + o16(rb + r)) = make_uint2(pack_bf16(x0, x1), pack_bf16(x2, x3));
+                    }
                 }
                 tc::fence_async_smem();
-                tc::bar_sync(BAR_CONV, 128);
-                if (ct == 0) tc::mbar_arrive(bar(B_KRDY + (n & 1)));
+                tc::bar_sync(BAR_CONV, 128);  // every raw row read, K in fp16 and bf16 written
+                if (ct == 0) {
+                    tc::mbar_arrive(bar(B_KRDY + (n & 1)));
+                    tc::mbar_arrive(bar(B_KRE + n % RK));
+                }
                 // K in tf32 (B of Pt_S and Pt_T, single buffer) once the previous chunk's Pt_T
                 // has read it: a row's 32 16-byte chunks, one per lane
                 w = true;
