@@ -276,6 +276,58 @@ def _config_leg(name, args, peaks, dev, stream):
     return out
 
 
+def _small_leg(name, args, dev, stream):
+    """Build and compose (with its seams, if the workload has any) on one of
+    the small fp32 workloads that run on the exact-fp32 token-serial CUDA-core
+    kernels (d < 128 or fp32 inputs), each timed with CUDA events over
+    repeated calls.  These calls take microseconds: the times are launch- and
+    latency-bound and are reported as such, with no roofline fraction."""
+    import torch
+    from linear_attn_state_chunked_gb300 import hypic, workloads as W
+    wl = W.make(name, device=dev)
+    d = wl.desc
+    L, H, Dk, Dv, w = d["n_layers"], d["n_heads"], d["d_k"], d["d_v"], d["seam_w"]
+    n_ord = len(wl.order)
+    tshape, sshape = hypic.pair_shapes(d, wl.n_seg)
+    T = torch.empty(tshape, device=dev)
+    S = torch.empty(sshape, device=dev)
+    Sf = torch.empty((L, H, Dk, Dv), device=dev)
+    o = torch.empty((L, n_ord, max(w, 1), H, Dv), device=dev)
+    wsp = torch.empty(hypic.workspace_size(d), dtype=torch.uint8, device=dev)
+    reps = 50
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    build_ms = timed(lambda: hypic.segment_build(d, wl.tok, wl.seg_off, T, S, wsp, stream=stream))
+    comp_ms = timed(lambda: hypic.compose(d, wl.tok, wl.seg_off, wl.order, T, S, Sf,
+                                          o_out=o if w > 0 else None, stream=stream))
+    hypic.workspace_status(wsp, stream)
+    hypic.async_status(stream)
+    body_tokens = int(sum(max(0, int(x) - min(w, int(x))) for x in wl.lengths))
+    mode = {hypic.GATED_DELTA: "gated delta", hypic.SCALAR_DECAY: "scalar decay (RetNet)",
+            hypic.DIAG_GATE: "diagonal gate (Mamba2 / GLA)"}.get(d["mode"], str(d["mode"]))
+    out = {
+        "workload": "%s: %s, %d layer(s) x %d heads, d_k=d_v=%d, %d segments (%d tokens), fp32 inputs, seam w=%d"
+                    % (name, mode, L, H, Dk, wl.n_seg, wl.n_tokens, w),
+        "path": "exact-fp32 token-serial CUDA-core kernels",
+        "build": {"ms": build_ms, "mtok_s_per_layer": body_tokens * L / (build_ms * 1e-3) / 1e6},
+        "compose": {"ms": comp_ms, "segs_s_per_layer": n_ord * L / (comp_ms * 1e-3)},
+        "note": "microsecond calls: launch- and latency-bound, no roofline fraction claimed",
+    }
+    del T, S, Sf, o, wsp, wl
+    return out
+
+
 def _q_rows_read(wl):
     """Token rows of q that the calls read: each request entry's seam tokens
     and the conv history before them (the previous entries' last conv_k - 1
@@ -598,14 +650,18 @@ def run_gpu(args):
 
     # the other configurations of the workload set, each on its own after the
     # cold prompt's tensors are released: the single-layer gated-delta request
-    # (build, compose with seams, compose alone) and the warm-cache 30-layer
+    # (build, compose with seams, compose alone), the warm-cache 30-layer
     # request (its pairs built once, then the compose with seams it is about)
+    # and the small fp32 workloads of the CUDA-core paths (tiny gated delta,
+    # RetNet decay, diagonal gate)
     configs = None
     if rank == 0 and not args.layers and not args.no_configs:
         del T, S, Sf, o, wsp, wl
         torch.cuda.empty_cache()
         configs = {name: _config_leg(name, args, peaks, dev, stream)
                    for name in ("gdn_bf16", "warm_30l")}
+        configs.update({name: _small_leg(name, args, dev, stream)
+                        for name in ("tiny_gdn", "decay_retnet", "decay_diag")})
 
     if rank == 0:
         line = {

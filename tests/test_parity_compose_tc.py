@@ -70,3 +70,32 @@ def test_tc_compose_empty_request():
     hypic.compose(d, wl.tok, wl.seg_off, [], out["T"], out["S"], Z)
     torch.cuda.synchronize()
     assert torch.count_nonzero(Z).item() == 0
+
+
+@pytest.mark.parametrize("case", ["big_state", "tiny_state", "scaled_qk"])
+def test_tc_compose_far_from_unit_scale(case):
+    """Requests whose state or seam operands sit far from unit scale, where
+    a tensor-core operand format with a narrow exponent range would lose
+    precision or overflow: a state of order 1e5 (until the decays bring it
+    back), a request whose values and state are all of order 1e-6, and,
+    without the conv (so q and k reach the seams unnormalised), q of order
+    1e3 and k of order 1e-2."""
+    conv = case != "scaled_qk"
+    base = "cold_30l" if conv else "stress_gdn"
+    wl = W.make(base, device="cuda", layers=1, lengths=LENGTHS, order=ORDER, n_heads=3)
+    d = wl.desc
+    g = torch.Generator(device="cuda").manual_seed(12)
+    S0 = torch.randn((d["n_layers"], d["n_heads"], 128, 128), generator=g, device="cuda")
+    if case == "big_state":
+        S0 *= 1e5
+    elif case == "tiny_state":
+        S0 *= 1e-6
+        wl.tok["v"].mul_(1e-6)
+    else:
+        wl.tok["q"].mul_(1e3)
+        wl.tok["k"].mul_(1e-2)
+    out = _run(wl, S0)
+    res = [check_request(wl, out, [(l, h)], tol_of(d), S_init=[S0[l, h].cpu().numpy()])
+           for (l, h) in _chains(wl)]
+    print("\ncompose tc %s: worst S_final %.2e S_prefix %.2e o %.2e" % (
+        case, max(r["final"] for r in res), max(r["prefix"] for r in res), max(r["o"] for r in res)))
