@@ -29,21 +29,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
     return d;
 }
 
-// Shared-memory matrix descriptor of an MN-major operand tile laid out in the
-// 128-byte swizzle: atoms of 8 K-rows x 128 bytes along MN (1024 bytes, 8-row
-// groups along K 1024 bytes apart), consecutive atoms along MN `lbo` bytes
-// apart; tile base 1024-byte aligned.
-__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
 // Byte offset of fp32 element (r, k) in a K-major 128-byte-swizzled tile of
 // R rows: K runs in atoms of 32 elements; atom a holds all R rows.
 __host__ __device__ __forceinline__ uint32_t sw128_f32(int r, int k, int R)
@@ -76,12 +61,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
 {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// Instruction descriptor: fp32 accumulate, fp16 A (MN-major) and B (K-major), kind::f16.
-__host__ __device__ constexpr uint32_t idesc_f16_amn(int M, int N)
-{
-    return (1u << 4) | (1u << 15) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Round to the nearest tf32 value (10 stored mantissa bits), ties away from
