@@ -407,8 +407,11 @@ struct PrepScratch {
     float nrm[NP / 32][MR];
     float alpha[WC], beta[WC];
 };
-struct CompScratch {
-    float2 red[2][MR / 2][D];  // column products of row-quarter pairs, two rows m per entry
+// RS slots of partial column products: four (one per row quarter, summed by
+// the readers after one barrier) when the shared memory allows it, else two
+// (quarters 2, 3 added into quarters 0, 1 first, a second barrier).
+template <int RS> struct CompScratch {
+    float2 red[RS][MR / 2][D];  // two rows m per entry
     float dl[WC][D];           // g(7, t) d_t (state update)
 };
 
@@ -424,7 +427,8 @@ template <typename Tin> struct Layout {
     static constexpr uint32_t POUT = INFO + 2 * sizeof(Info);
     static constexpr uint32_t PSCR = POUT + 2 * sizeof(PrepOut);
     static constexpr uint32_t CSCR = PSCR + sizeof(PrepScratch);
-    static constexpr uint32_t BAR = (CSCR + sizeof(CompScratch) + 15) / 16 * 16;
+    static constexpr int RS = sizeof(Tin) == 2 ? 4 : 2;  // fp32 raw rows leave room for two slots only
+    static constexpr uint32_t BAR = (CSCR + sizeof(CompScratch<RS>) + 15) / 16 * 16;
     static constexpr uint32_t BYTES = BAR + 8 * B_COUNT + 16;
     static_assert(BYTES <= 232448, "shared memory budget");
     static_assert(RAW % 16 == 0 && ROW % 16 == 0 && POUT % 16 == 0 && sizeof(PrepOut) % 16 == 0 &&
@@ -463,15 +467,15 @@ struct Cursor {
     }
 };
 
-// Butterfly sum of N values (N = 8 or 16) over the 32 lanes of a warp: each
-// step hands half the values to the partner lane, so after log2(N) steps
-// lane bits 4, 3, ... select which sum a lane carries; the remaining lane
-// bits are summed plainly.  Returns the sum of value index
+// Butterfly sum of N values (N = 8, 16 or 32) over the 32 lanes of a warp:
+// each step hands half the values to the partner lane, so after log2(N)
+// steps lane bits 4, 3, ... select which sum a lane carries; the remaining
+// lane bits are summed plainly.  Returns the sum of value index
 // (lane >> (5 - log2 N)) as laid out by those bits.
 template <int N> __device__ __forceinline__ float butterfly_sum(float (&v)[N], int lane)
 {
-    constexpr int LOGN = N == 16 ? 4 : 3;
-    static_assert(N == (1 << LOGN), "8 or 16 values");
+    constexpr int LOGN = N == 32 ? 5 : N == 16 ? 4 : 3;
+    static_assert(N == (1 << LOGN), "8, 16 or 32 values");
 #pragma unroll
     for (int st = 0; st < LOGN; ++st) {
         const int half = N >> (st + 1), bit = 16 >> st;
@@ -504,7 +508,8 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
     auto info = [&](int stg) -> Info & { return reinterpret_cast<Info *>(smem + LY::INFO)[stg]; };
     auto pout = [&](int b) -> PrepOut & { return reinterpret_cast<PrepOut *>(smem + LY::POUT)[b]; };
     PrepScratch &ps = *reinterpret_cast<PrepScratch *>(smem + LY::PSCR);
-    CompScratch &cs = *reinterpret_cast<CompScratch *>(smem + LY::CSCR);
+    constexpr int RS = LY::RS;
+    CompScratch<RS> &cs = *reinterpret_cast<CompScratch<RS> *>(smem + LY::CSCR);
     const Dims dm = a.dm;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const long long n_units = (long long)dm.L * tab.n_perm * dm.H;
@@ -765,31 +770,31 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
 #pragma unroll
                 for (int i2 = 0; i2 < WC; ++i2) kr[i2] = reinterpret_cast<const float4 *>(ps.kq[i2])[lane];
                 const int which = pw / 2;
+                // the warp's 32 partial dots (rows t = 4 (pw % 2) + g4, columns
+                // i2) reduced in one reduce-scatter: lane L ends with dot
+                // (g4, i2) = (L >> 3, L & 7)
+                float sv[4 * WC];
 #pragma unroll
                 for (int g4 = 0; g4 < 4; ++g4) {
-                    const int t = 4 * (pw % 2) + g4;
-                    const float4 x4 = reinterpret_cast<const float4 *>(ps.kq[which * WC + t])[lane];
-                    float sv[WC];
+                    const float4 x4 = reinterpret_cast<const float4 *>(ps.kq[which * WC + 4 * (pw % 2) + g4])[lane];
 #pragma unroll
                     for (int i2 = 0; i2 < WC; ++i2) {
                         float sdot = x4.x * kr[i2].x;
                         sdot = fmaf(x4.y, kr[i2].y, sdot);
                         sdot = fmaf(x4.z, kr[i2].z, sdot);
-                        sv[i2] = fmaf(x4.w, kr[i2].w, sdot);
-                    }
-                    const float r = butterfly_sum<WC>(sv, lane);
-                    const int i2 = lane >> 2;
-                    if ((lane & 3) == 0) {
-                        float g = 1.f, bt = 0.f;
-#pragma unroll
-                        for (int j = 0; j < WC; ++j) {
-                            if (j > i2 && j <= t) g *= al[j];
-                            if (j == t) bt = be[j];
-                        }
-                        if (which == 0) po.ck[t][i2] = i2 < t ? bt * g * r : 0.f;
-                        else po.cq[t][i2] = i2 <= t ? g * r : 0.f;
+                        sv[g4 * WC + i2] = fmaf(x4.w, kr[i2].w, sdot);
                     }
                 }
+                const float r = butterfly_sum<4 * WC>(sv, lane);
+                const int t = 4 * (pw % 2) + (lane >> 3), i2 = lane & 7;
+                float g = 1.f, bt = 0.f;
+#pragma unroll
+                for (int j = 0; j < WC; ++j) {
+                    if (j > i2 && j <= t) g *= al[j];
+                    if (j == t) bt = be[j];
+                }
+                if (which == 0) po.ck[t][i2] = i2 < t ? bt * g * r : 0.f;
+                else po.cq[t][i2] = i2 <= t ? g * r : 0.f;
             }
             tc::bar_sync(BAR_P, NP);
             if (ch == 0) tc::mbar_arrive(bar(B_PREPPED + b));
@@ -848,26 +853,29 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
                 }
             }
         }
-        // row quarters 2, 3 hand their sums to quarters 0, 1
-        if (rq >= 2) {
+        // the row quarters hand their partial sums over: each into its own
+        // slot (one barrier), or quarters 2, 3 into quarters 0, 1 (two)
+        if (RS == 4 || rq >= 2) {
 #pragma unroll
             for (int mp = 0; mp < MR / 2; ++mp) {
-                cs.red[rq - 2][mp][2 * cp] = acc[mp][0];
-                cs.red[rq - 2][mp][2 * cp + 1] = acc[mp][1];
+                cs.red[rq % RS][mp][2 * cp] = acc[mp][0];
+                cs.red[rq % RS][mp][2 * cp + 1] = acc[mp][1];
             }
         }
         tc::bar_sync(BAR_C, NC);
         // without a state to write, the state stage is consumed: hand it back
         if (a.S_out == nullptr && tid == 0) tc::mbar_arrive(bar(B_EMPTYS + stg));
-        if (rq < 2) {
+        if (RS == 2) {
+            if (rq < 2) {
 #pragma unroll
-            for (int mp = 0; mp < MR / 2; ++mp) {
-                float2 &e0 = cs.red[rq][mp][2 * cp], &e1 = cs.red[rq][mp][2 * cp + 1];
-                e0 = make_float2(e0.x + acc[mp][0].x, e0.y + acc[mp][0].y);
-                e1 = make_float2(e1.x + acc[mp][1].x, e1.y + acc[mp][1].y);
+                for (int mp = 0; mp < MR / 2; ++mp) {
+                    float2 &e0 = cs.red[rq][mp][2 * cp], &e1 = cs.red[rq][mp][2 * cp + 1];
+                    e0 = make_float2(e0.x + acc[mp][0].x, e0.y + acc[mp][0].y);
+                    e1 = make_float2(e1.x + acc[mp][1].x, e1.y + acc[mp][1].y);
+                }
             }
+            tc::bar_sync(BAR_C, NC);
         }
-        tc::bar_sync(BAR_C, NC);
 
         // ---- per column: d_t, then o_t
         if (tid < D) {
@@ -875,12 +883,17 @@ seam_pipe_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Seg
             float pk[WC], pq[WC], dt[WC];
 #pragma unroll
             for (int mp = 0; mp < WC / 2; ++mp) {
-                const float2 k0 = cs.red[0][mp][c], k1 = cs.red[1][mp][c];
-                const float2 q0 = cs.red[0][WC / 2 + mp][c], q1 = cs.red[1][WC / 2 + mp][c];
-                pk[2 * mp] = k0.x + k1.x;
-                pk[2 * mp + 1] = k0.y + k1.y;
-                pq[2 * mp] = q0.x + q1.x;
-                pq[2 * mp + 1] = q0.y + q1.y;
+                float2 k2 = cs.red[0][mp][c], q2 = cs.red[0][WC / 2 + mp][c];
+#pragma unroll
+                for (int qq = 1; qq < RS; ++qq) {
+                    const float2 kx = cs.red[qq][mp][c], qx = cs.red[qq][WC / 2 + mp][c];
+                    k2 = make_float2(k2.x + kx.x, k2.y + kx.y);
+                    q2 = make_float2(q2.x + qx.x, q2.y + qx.y);
+                }
+                pk[2 * mp] = k2.x;
+                pk[2 * mp + 1] = k2.y;
+                pq[2 * mp] = q2.x;
+                pq[2 * mp + 1] = q2.y;
             }
             float *o_base = a.o_out + (((size_t)cc.l * tab.n_perm + cc.ent) * dm.w * dm.H + cc.h) * D + c;
 #pragma unroll
