@@ -371,9 +371,11 @@ seam_chunk_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ Se
 //   compute (warps 0-7): the column products [k; q] S0 (packed fp32 FMAs),
 //     the per-column solve for d_t and the outputs o_t (and S_n).
 // So the state read of seam u + 1 and the staging of seam u + 1 both
-// overlap the column products of seam u.  What bounds it: the broadcast
-// shared-memory reads of [k; q] (16 values per state row and warp) in the
-// column products.
+// overlap the column products of seam u.  What bounds it: two latency chains
+// of about equal length per seam, the compute warps' (column products on the
+// FMA pipe with broadcast shared-memory reads of [k; q], then the
+// per-column solve) and the prep warps' (conv, norms, dots), coupled through
+// the double-buffered hand-off.
 
 namespace pipe {
 
